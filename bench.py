@@ -1,0 +1,425 @@
+"""Benchmark of the edge-packed multi-head attention forward pass on GB300.
+
+One step = one full forward pass (projections, edge attention, merge of split
+targets, out_proj) over one batch of the skewed n = 20,000 workload
+(B = 16 samples, embed_dim 128, 8 heads, 400,000 live edges with Zipf-like
+in-degrees up to 8,000), inputs resident in HBM. L2 is flushed between timed
+steps by writing a 512 MiB buffer (untimed). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path; a barrier and a max over ranks of the step time only).
+--impl reference times the fp64 CPU oracle on the host cores instead (rank 0
+only), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+WORKLOAD_ID = 3
+METRIC = "edge·head·sample scores/s and layer fwd µs at n=20k; % HBM / tensor roofline"
+UNIT = "scores/s"
+FLUSH_BYTES = 512 << 20
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def algorithmic_bytes(stage: str, w: synth.Workload, B: int, nnz: int, n_items: int) -> float | None:
+    """Compulsory HBM bytes of one launch: every tensor the kernel must touch,
+    read or written once (gathered re-reads served by L2 are not counted)."""
+    E, L, S = w.embed_dim, w.query_features, w.key_features
+    bf = 2
+    if stage == "edge_attn":
+        return (B * L * E * bf          # q rows
+                + B * S * 2 * E * bf    # k and v rows, each at least once
+                + B * L * E * bf        # mixed, written
+                + nnz * 4               # source index per CSR position
+                + n_items * 16)         # work items
+    if stage == "proj_qkv":
+        return B * L * E * bf + 3 * E * E * bf + B * L * 3 * E * bf
+    if stage == "out_proj":
+        return B * L * E * bf + E * E * bf + B * L * E * bf
+    return None
+
+
+def stage_flops(stage: str, w: synth.Workload, B: int) -> float | None:
+    E, L = w.embed_dim, w.query_features
+    if stage == "proj_qkv":
+        return 2.0 * B * L * E * 3 * E
+    if stage == "out_proj":
+        return 2.0 * B * L * E * E
+    return None
+
+
+def source_digest(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "edge_attn": ["graph_sparse_head_gb300/csrc/edge_attn.cu"],
+    "proj_qkv": ["graph_sparse_head_gb300/csrc/gemm_tc.cu"],
+    "out_proj": ["graph_sparse_head_gb300/csrc/gemm_tc.cu"],
+}
+
+
+def ncu_traffic(stage: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel; else None."""
+    p = os.path.join(PROFILE_DIR, "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(stage)
+    if not e or e.get("source_digest") != source_digest(KERNEL_SOURCES[stage]):
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return len(self.lines)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, first: int):
+        rows = [l.split(",") for _, l in self.lines[first:]]
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_seed(rank: int) -> int:
+    """Each rank draws its own batch of tokens (weak scaling); rank 0 uses the
+    workload's own token stream."""
+    return rank
+
+
+def make_rank_inputs(rank: int, batch: int):
+    w = synth.workload(WORKLOAD_ID)
+    xq, _, params = synth.make_inputs(WORKLOAD_ID, batch)
+    if shard_seed(rank):
+        rng = np.random.default_rng([1000 + WORKLOAD_ID, shard_seed(rank)])
+        xq = synth.make_tokens(rng, batch, w.query_features, w.embed_dim, w.dtype)
+    return xq, params
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_cpu_baseline(budget_s: float, src, tgt, w, xq, params):
+    """The oracle as it stands, on whole samples of the workload, until about
+    budget_s seconds of CPU time have passed (at least one sample)."""
+    import oracle
+    cores = oracle.num_threads()
+    done, t_total = 0, 0.0
+    while done < xq.shape[0]:
+        x = xq[done:done + 1]
+        t0 = time.perf_counter()
+        oracle.forward(x, x, x, params, src, tgt, w.num_heads, need_weights=False)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total >= budget_s:
+            break
+    scores = done * len(src) * w.num_heads
+    return {"value": scores / t_total, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {xq.shape[0]} samples of the workload (full graph, all {len(src)} edges), "
+                      f"fp64 C oracle, OpenMP over (sample, target), {t_total:.2f} s"}
+
+
+def bench_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.workload(WORKLOAD_ID)
+    src, tgt = synth.make_graph(WORKLOAD_ID)
+    xq, params = make_rank_inputs(0, w.batch)
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    times = []
+    for i in range(args.warmup + args.steps):
+        b = i % w.batch
+        x = xq[b:b + 1]
+        t0 = time.perf_counter()
+        oracle.forward(x, x, x, params, src, tgt, w.num_heads, need_weights=False)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    per_sample = sum(times) / len(times)
+    value = len(src) * w.num_heads / per_sample
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_sample * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch_per_step": 1, "batch": w.batch, "nnz": len(src),
+                   "embed_dim": w.embed_dim, "num_heads": w.num_heads, "n": w.query_features},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step one sample (1 of {w.batch}) of the workload, full graph"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU: the library has no CPU path")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import graph_sparse_head_gb300 as pmha
+    w = synth.workload(WORKLOAD_ID)
+    B = w.batch
+    src, tgt = synth.make_graph(WORKLOAD_ID)
+    xq_np, prm = make_rank_inputs(rank, B)
+    params = pmha.Params.from_arrays(prm, w.num_heads, torch.bfloat16, dev)
+    graph = pmha.pmha_build_csr(torch.from_numpy(src).to(dev), torch.from_numpy(tgt).to(dev),
+                                w.query_features, w.key_features)
+    nnz, H = graph.nnz, w.num_heads
+    x = torch.from_numpy(xq_np).to(torch.bfloat16).to(dev)
+    out = torch.empty_like(x)
+    ws = torch.empty(pmha.pmha_forward_workspace_size(graph, params, B, "none"), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pmha.pmha_forward(graph, params, x, x, x, "none", out=out, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    pmha.pmha_device_status()
+
+    sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    sampler.start()
+    first = sampler.mark()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = pmha.pmha_launch_count()
+    pmha.pmha_profile_enable(True)
+    pmha.pmha_profile_read()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)  # evict L2 between steps (not timed)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    pmha.pmha_profile_enable(False)
+    prof = pmha.pmha_profile_read()
+    launches = pmha.pmha_launch_count() - launches0
+    clocks = sampler.summary(first)
+    sampler.stop()
+    pmha.pmha_device_status()
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms, world, dev)
+    scores = float(B) * nnz * H
+    value = world * scores / (ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers (pinned), per step:
+    # copy the step's tokens in, run, copy the output back
+    xh = torch.from_numpy(xq_np).to(torch.bfloat16).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    ws_h = torch.empty(pmha.pmha_forward_host_workspace_size(graph, params, B, "none"), dtype=torch.uint8,
+                       device=dev)
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        pmha.pmha_forward_host(graph, params, xh, xh, xh, oh, "none", workspace=ws_h, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        pmha.pmha_forward_host(graph, params, xh, xh, xh, oh, "none", workspace=ws_h, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e_value = world * scores / (e2e_ms / 1e3)
+    h2d = xh.numel() * xh.element_size()
+    d2h = oh.numel() * oh.element_size()
+
+    # ---- roofline of the dominant kernel
+    peaks = load_peaks()
+    stages = {k: {"launches": v[0], "total_ms": v[1], "avg_us": 1e3 * v[1] / max(v[0], 1)} for k, v in prof.items()}
+    total_stage_ms = sum(v["total_ms"] for v in stages.values()) or 1.0
+    for v in stages.values():
+        v["share"] = v["total_ms"] / total_stage_ms
+    dom = max(stages, key=lambda k: stages[k]["total_ms"]) if stages else None
+    roof = None
+    if dom is not None:
+        avg_s = stages[dom]["avg_us"] / 1e6
+        alg = algorithmic_bytes(dom, w, B, nnz, work_items(tgt, w.query_features))
+        if alg is not None:
+            achieved = alg / avg_s / 1e9
+            roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom),
+                    "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
+                    "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+    for k, v in stages.items():
+        alg = algorithmic_bytes(k, w, B, nnz, work_items(tgt, w.query_features))
+        if alg is not None:
+            v["hbm_gbs_algorithmic"] = alg / (v["avg_us"] / 1e6) / 1e9
+            v["hbm_frac"] = v["hbm_gbs_algorithmic"] / peaks["hbm_gbs"]
+        fl = stage_flops(k, w, B)
+        if fl is not None:
+            v["tflops"] = fl / (v["avg_us"] / 1e6) / 1e12
+            v["tensor_frac"] = v["tflops"] / peaks["bf16_tflops"]
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        cpu = run_cpu_baseline(args.cpu_seconds, src, tgt, w, xq_np, prm)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "layer_fwd_us": ms * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch": B, "n": w.query_features, "nnz": nnz,
+                       "embed_dim": w.embed_dim, "num_heads": H, "max_in_degree": graph.max_in_degree,
+                       "l2": "flushed between timed steps (512 MiB write, untimed)",
+                       "parallelism": f"replicas x{world}, own batch per rank, no collective"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "api": "pmha_forward_host (pinned host buffers)"},
+            "gpu_launches": launches,
+            "roofline": roof,
+            "stages": stages,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    graph.destroy()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def work_items(tgt, L: int, chunk: int = 128) -> int:
+    """Work items of the edge kernel per sample: one per target, or one per
+    chunk of `chunk` edges for targets with more edges (the library's split)."""
+    deg = np.bincount(tgt, minlength=L)
+    return int(np.where(deg > chunk, (deg + chunk - 1) // chunk, 1).sum())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

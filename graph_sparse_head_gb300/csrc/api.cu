@@ -1,0 +1,665 @@
+// Host side of the C ABI declared in include/pmha.h: argument checks, the
+// workspace layout, and the order of launches for one forward pass
+// (kpnn2 PackedMultiheadAttention, Notes steps 1-5):
+//   projections (tensor-core GEMM, Q|K|V fused when the tokens are shared)
+//   -> edge attention (scores, segmented softmax, value mix)
+//   -> merge of split targets -> per-edge weights (if requested)
+//   -> out_proj GEMM.
+// Everything is queued on the caller's stream; nothing here synchronizes
+// except pmha_build_csr (once) and the explicit status / profiling reads.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pmha_internal.h"
+
+namespace pmha {
+
+// ---------------------------------------------------------------- errors
+
+static thread_local char t_err[512] = "";
+
+void set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof(t_err), fmt, ap);
+    va_end(ap);
+}
+
+pmha_status cuda_fail(cudaError_t e, const char *what)
+{
+    set_error("%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+    return PMHA_ERR_CUDA;
+}
+
+static __device__ int g_device_error;
+
+int *device_error_word()
+{
+    static std::mutex mu;
+    static int *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+            set_error("cudaGetSymbolAddress(device error word) failed");
+            return nullptr;
+        }
+        addr[dev] = (int *)p;
+    }
+    return addr[dev];
+}
+
+int num_sms()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+// ---------------------------------------------------------------- profiling
+
+static std::atomic<long long> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+struct Record {
+    const char *stage;
+    cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<Record> g_records;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+}  // namespace
+
+StageTimer::StageTimer(const char *stage_, cudaStream_t s) : stage(stage_), stream(s), slot(-1)
+{
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    Record r;
+    r.stage = stage;
+    r.start = take_event();
+    r.stop = take_event();
+    if (!r.start || !r.stop) return;
+    cudaEventRecord(r.start, stream);
+    slot = (int)g_records.size();
+    g_records.push_back(r);
+}
+
+StageTimer::~StageTimer()
+{
+    if (slot < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (slot < (int)g_records.size()) cudaEventRecord(g_records[slot].stop, stream);
+}
+
+// ---------------------------------------------------------------- helpers
+
+namespace {
+
+size_t elem_size(pmha_dtype dt) { return dt == PMHA_BF16 ? 2 : 4; }
+TcType param_type(pmha_dtype dt) { return dt == PMHA_BF16 ? TcType::BF16 : TcType::F32; }
+// q, k, v and mixed of a bf16 layer are kept in fp16 (same width, 3 more
+// mantissa bits); a float32 layer keeps them in float32.
+TcType inter_type(pmha_dtype dt) { return dt == PMHA_BF16 ? TcType::F16 : TcType::F32; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+pmha_status check_params(const pmha_graph *g, const pmha_params *p, int64_t batch)
+{
+    if (!g) {
+        set_error("graph is NULL");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (!p) {
+        set_error("params is NULL");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (p->dtype != PMHA_F32 && p->dtype != PMHA_BF16) {
+        set_error("dtype %d is neither PMHA_F32 nor PMHA_BF16", (int)p->dtype);
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (p->embed_dim < 1 || p->num_heads < 1 || p->embed_dim % p->num_heads) {
+        set_error("embed_dim %lld must be positive and divisible by num_heads %lld", (long long)p->embed_dim,
+                  (long long)p->num_heads);
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (batch < 1) {
+        set_error("batch %lld must be >= 1", (long long)batch);
+        return PMHA_ERR_INVALID_ARG;
+    }
+    const void *w[4] = {p->wq, p->wk, p->wv, p->wo};
+    for (int i = 0; i < 4; ++i)
+        if (!w[i] || !aligned16(w[i])) {
+            set_error("projection weight %d is NULL or not 16-byte aligned", i);
+            return PMHA_ERR_INVALID_ARG;
+        }
+    const void *b[4] = {p->bq, p->bk, p->bv, p->bo};
+    for (int i = 0; i < 4; ++i)
+        if (b[i] && ((uintptr_t)b[i] % elem_size(p->dtype))) {
+            set_error("bias %d is not aligned to its element size", i);
+            return PMHA_ERR_INVALID_ARG;
+        }
+    if (!edge_supported(p->embed_dim, p->num_heads, inter_type(p->dtype))) {
+        set_error("no edge kernel for embed_dim %lld, num_heads %lld in this dtype (needs a power-of-two split "
+                  "of the row and of each head over at most 32 lanes)",
+                  (long long)p->embed_dim, (long long)p->num_heads);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    if (batch * g->L * p->embed_dim > (int64_t)1 << 46 || batch * g->S * p->embed_dim > (int64_t)1 << 46) {
+        set_error("tensor too large");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    return PMHA_OK;
+}
+
+struct Layout {
+    size_t qkv = 0, mixed = 0, part = 0, ml = 0, scores = 0, wo16 = 0, total = 0;
+};
+
+bool out_proj_on_tensor_cores(const pmha_params *p)
+{
+    return p->dtype == PMHA_BF16 && gemm_tc_supported(p->embed_dim);
+}
+
+// Offsets inside the workspace. qkv holds B*L*E + B*S*(kv_width) intermediate
+// elements: Q, then K|V rows (or the fused [Q|K|V] / [Q|K] rows, which take
+// the same room); wo16 holds an fp16 copy of out_proj's weight when out_proj
+// runs on the tensor cores with fp16 operands.
+Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode wmode, bool with_values)
+{
+    const int64_t E = p->embed_dim, H = p->num_heads;
+    const size_t es = type_size(inter_type(p->dtype));
+    Layout l;
+    size_t o = 0;
+    l.qkv = o;
+    o += align256((size_t)(B * g->L * E + B * g->S * E * (with_values ? 2 : 1)) * es);
+    l.mixed = o;
+    if (with_values) o += align256((size_t)(B * g->L * E) * es);
+    l.part = o;
+    o += align256((size_t)(B * g->n_parts * (2 * H + E)) * 4);
+    l.ml = o;
+    if (wmode != PMHA_WEIGHTS_NONE) o += align256((size_t)(B * g->L * H * 2) * 4);
+    l.scores = o;
+    if (wmode == PMHA_WEIGHTS_AVG) o += align256((size_t)(B * g->nnz * H) * 4);
+    l.wo16 = o;
+    if (with_values && out_proj_on_tensor_cores(p)) o += align256((size_t)(E * E) * 2);
+    l.total = o;
+    return l;
+}
+
+// Step 1: tokens (layer dtype) -> q / k / v (intermediate type).
+pmha_status project(pmha_dtype dt, const void *X, int64_t M, int64_t E, const GemmSegments &seg, void *Y,
+                    int64_t ldy, const char *stage, cudaStream_t s)
+{
+    if (dt == PMHA_BF16 && gemm_tc_supported(E))
+        return gemm_tc(TcType::BF16, TcType::F16, X, M, E, seg, Y, ldy, stage, s);
+    return gemm_simt(param_type(dt), param_type(dt), inter_type(dt), X, M, E, seg, Y, ldy, stage, s);
+}
+
+GemmSegments segs(const void *w0, const void *b0, const void *w1 = nullptr, const void *b1 = nullptr,
+                  const void *w2 = nullptr, const void *b2 = nullptr)
+{
+    GemmSegments s;
+    s.w[0] = w0;
+    s.b[0] = b0;
+    s.w[1] = w1;
+    s.b[1] = b1;
+    s.w[2] = w2;
+    s.b[2] = b2;
+    s.n_seg = w2 ? 3 : (w1 ? 2 : 1);
+    return s;
+}
+
+// Steps 1-4 (and the weights); with_values = false stops after the scores.
+pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
+                   const void *value, int64_t B, pmha_wmode wmode, float *weights, char *ws, const Layout &lay,
+                   bool with_values, cudaStream_t s, const void **mixed_out)
+{
+    const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
+    const size_t es = type_size(inter_type(p->dtype));
+    char *qkv = ws + lay.qkv;
+    EdgeArgs a;
+    pmha_status st;
+    const bool same_qkv = query == key && (!with_values || key == value) && L == S;
+    const int width = with_values ? 3 : 2;
+    if (same_qkv) {
+        // one GEMM: rows [Q | K | V] (or [Q | K])
+        st = with_values ? project(p->dtype, query, B * L, E, segs(p->wq, p->bq, p->wk, p->bk, p->wv, p->bv), qkv,
+                                   3 * E, "proj_qkv", s)
+                         : project(p->dtype, query, B * L, E, segs(p->wq, p->bq, p->wk, p->bk), qkv, 2 * E, "proj_qk",
+                                   s);
+        if (st != PMHA_OK) return st;
+        a.q = qkv;
+        a.q_ld = width * E;
+        a.kv = qkv + E * es;
+        a.kv_ld = width * E;
+    } else {
+        char *kvbuf = qkv + (size_t)(B * L * E) * es;
+        const int64_t kv_w = with_values ? 2 * E : E;
+        st = project(p->dtype, query, B * L, E, segs(p->wq, p->bq), qkv, E, "proj_q", s);
+        if (st != PMHA_OK) return st;
+        if (with_values && key == value) {
+            st = project(p->dtype, key, B * S, E, segs(p->wk, p->bk, p->wv, p->bv), kvbuf, kv_w, "proj_kv", s);
+            if (st != PMHA_OK) return st;
+        } else {
+            st = project(p->dtype, key, B * S, E, segs(p->wk, p->bk), kvbuf, kv_w, "proj_k", s);
+            if (st != PMHA_OK) return st;
+            if (with_values) {
+                st = project(p->dtype, value, B * S, E, segs(p->wv, p->bv), kvbuf + E * es, kv_w, "proj_v", s);
+                if (st != PMHA_OK) return st;
+            }
+        }
+        a.q = qkv;
+        a.q_ld = E;
+        a.kv = kvbuf;
+        a.kv_ld = kv_w;
+    }
+    a.v_off = E;
+    a.mixed = with_values ? ws + lay.mixed : nullptr;
+    a.part = (float *)(ws + lay.part);
+    a.ml = wmode != PMHA_WEIGHTS_NONE ? (float *)(ws + lay.ml) : nullptr;
+    a.scores = wmode == PMHA_WEIGHTS_NONE ? nullptr : (wmode == PMHA_WEIGHTS_AVG ? (float *)(ws + lay.scores) : weights);
+    a.B = B;
+    a.L = L;
+    a.S = S;
+    a.E = E;
+    a.H = H;
+    a.nnz = g->nnz;
+    a.n_items = g->n_items;
+    a.n_parts = g->n_parts;
+    a.score_scale = (float)(1.4426950408889634 / sqrt((double)(E / H)));
+    a.with_values = with_values;
+    if ((st = edge_attention(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
+    if ((st = split_merge(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
+    if (wmode != PMHA_WEIGHTS_NONE)
+        if ((st = weights_finalize(g, a, wmode, weights, s)) != PMHA_OK) return st;
+    if (mixed_out) *mixed_out = a.mixed;
+    return PMHA_OK;
+}
+
+pmha_status check_wmode(pmha_wmode wmode, const float *weights, bool allow_none)
+{
+    if (wmode != PMHA_WEIGHTS_NONE && wmode != PMHA_WEIGHTS_AVG && wmode != PMHA_WEIGHTS_PER_HEAD) {
+        set_error("weight mode %d is not a pmha_wmode", (int)wmode);
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (wmode == PMHA_WEIGHTS_NONE && !allow_none) {
+        set_error("pmha_edge_weights needs PMHA_WEIGHTS_AVG or PMHA_WEIGHTS_PER_HEAD");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if ((wmode == PMHA_WEIGHTS_NONE) != (weights == nullptr)) {
+        set_error("weights must be given exactly when a weight mode is requested");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (weights && ((uintptr_t)weights & 3u)) {
+        set_error("weights must be 4-byte aligned");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    return PMHA_OK;
+}
+
+pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
+                           const void *value, int64_t B, void *output, pmha_wmode wmode, float *weights,
+                           void *workspace, size_t ws_bytes, cudaStream_t s)
+{
+    pmha_status st = check_params(g, p, B);
+    if (st != PMHA_OK) return st;
+    if ((st = check_wmode(wmode, weights, true)) != PMHA_OK) return st;
+    if (!query || !key || !value || !output || !aligned16(query) || !aligned16(key) || !aligned16(value) ||
+        !aligned16(output)) {
+        set_error("query, key, value and output must be non-NULL, 16-byte aligned device pointers");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if ((p->embed_dim * (int64_t)elem_size(p->dtype)) % 16) {
+        set_error("embed_dim %lld gives rows that are not a multiple of 16 bytes", (long long)p->embed_dim);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    const Layout lay = layout(g, p, B, wmode, true);
+    if (!workspace || ws_bytes < lay.total || ((uintptr_t)workspace & 255u)) {
+        set_error("workspace needs %zu bytes, 256-byte aligned (got %zu at %p)", lay.total, ws_bytes, workspace);
+        return PMHA_ERR_WORKSPACE;
+    }
+    char *ws = (char *)workspace;
+    const void *mixed = nullptr;
+    st = attend(g, p, query, key, value, B, wmode, weights, ws, lay, true, s, &mixed);
+    if (st != PMHA_OK) return st;
+    // step 5: out_proj over the joined heads, mixed (intermediate type) -> output (layer dtype)
+    const int64_t E = p->embed_dim;
+    if (out_proj_on_tensor_cores(p)) {
+        // both MMA operands must share one type: use an fp16 copy of Wo
+        void *wo16 = ws + lay.wo16;
+        if ((st = convert_bf16_to_f16(p->wo, wo16, E * E, s)) != PMHA_OK) return st;
+        return gemm_tc(TcType::F16, TcType::BF16, mixed, B * g->L, E, segs(wo16, p->bo), output, E, "out_proj", s);
+    }
+    return gemm_simt(inter_type(p->dtype), param_type(p->dtype), param_type(p->dtype), mixed, B * g->L, E,
+                     segs(p->wo, p->bo), output, E, "out_proj", s);
+}
+
+}  // namespace
+}  // namespace pmha
+
+using namespace pmha;
+
+extern "C" {
+
+pmha_status pmha_build_csr(const int64_t *source_index, const int64_t *target_index, int64_t nnz,
+                           int64_t query_features, int64_t key_features, int add_self_loops, pmha_stream stream,
+                           pmha_graph **out)
+{
+    if (!out) {
+        set_error("pmha_build_csr: out is NULL");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    *out = nullptr;
+    if (nnz < 1) {
+        set_error("pmha_build_csr: the index arrays are empty (nnz must be >= 1)");
+        return PMHA_ERR_EMPTY;
+    }
+    if (!source_index || !target_index) {
+        set_error("pmha_build_csr: NULL index array");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (((uintptr_t)source_index & 7u) || ((uintptr_t)target_index & 7u)) {
+        set_error("pmha_build_csr: index arrays must be 8-byte aligned");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (query_features < 1 || key_features < 1 || query_features > 0x7ffffffe || key_features > 0x7ffffffe) {
+        set_error("pmha_build_csr: query_features and key_features must be in [1, 2^31 - 2]");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (add_self_loops && query_features != key_features) {
+        set_error("pmha_build_csr: add_self_loops needs query_features == key_features");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    const int64_t cap = nnz + (add_self_loops ? query_features : 0);
+    if (cap > 0x7fffffffLL - 8192) {
+        set_error("pmha_build_csr: more than 2^31 - 8193 edges");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    cudaPointerAttributes at;
+    for (const int64_t *ptr : {source_index, target_index}) {
+        if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess || (at.type != cudaMemoryTypeDevice &&
+                                                                  at.type != cudaMemoryTypeManaged)) {
+            cudaGetLastError();
+            set_error("pmha_build_csr: index arrays must be device memory");
+            return PMHA_ERR_INVALID_ARG;
+        }
+    }
+    return build_csr(source_index, target_index, nnz, query_features, key_features, add_self_loops != 0,
+                     (cudaStream_t)stream, out);
+}
+
+pmha_status pmha_graph_info(const pmha_graph *g, int64_t *nnz_total, int64_t *L, int64_t *S, int64_t *max_deg)
+{
+    if (!g) {
+        set_error("graph is NULL");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (nnz_total) *nnz_total = g->nnz;
+    if (L) *L = g->L;
+    if (S) *S = g->S;
+    if (max_deg) *max_deg = g->max_deg;
+    return PMHA_OK;
+}
+
+pmha_status pmha_graph_export(const pmha_graph *g, int32_t *row_ptr, int32_t *col, int32_t *perm,
+                              pmha_stream stream)
+{
+    if (!g) {
+        set_error("graph is NULL");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    if (row_ptr)
+        PMHA_CUDA_TRY(cudaMemcpyAsync(row_ptr, g->row_ptr, (size_t)(g->L + 1) * 4, cudaMemcpyDeviceToDevice, s));
+    if (col) PMHA_CUDA_TRY(cudaMemcpyAsync(col, g->col, (size_t)g->nnz * 4, cudaMemcpyDeviceToDevice, s));
+    if (perm) PMHA_CUDA_TRY(cudaMemcpyAsync(perm, g->perm, (size_t)g->nnz * 4, cudaMemcpyDeviceToDevice, s));
+    return PMHA_OK;
+}
+
+void pmha_graph_destroy(pmha_graph *g)
+{
+    if (!g) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cur != g->device) cudaSetDevice(g->device);
+    cudaFree(g->mem);
+    if (cur != g->device) cudaSetDevice(cur);
+    delete g;
+}
+
+size_t pmha_forward_workspace_size(const pmha_graph *g, const pmha_params *p, int64_t batch, pmha_wmode wmode)
+{
+    if (check_params(g, p, batch) != PMHA_OK) return 0;
+    if (wmode != PMHA_WEIGHTS_NONE && wmode != PMHA_WEIGHTS_AVG && wmode != PMHA_WEIGHTS_PER_HEAD) return 0;
+    return layout(g, p, batch, wmode, true).total;
+}
+
+size_t pmha_edge_weights_workspace_size(const pmha_graph *g, const pmha_params *p, int64_t batch, pmha_wmode wmode)
+{
+    if (check_params(g, p, batch) != PMHA_OK) return 0;
+    if (wmode != PMHA_WEIGHTS_AVG && wmode != PMHA_WEIGHTS_PER_HEAD) return 0;
+    return layout(g, p, batch, wmode, false).total;
+}
+
+pmha_status pmha_forward(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
+                         const void *value, int64_t batch, void *output, pmha_wmode wmode, float *weights,
+                         void *workspace, size_t ws_bytes, pmha_stream stream)
+{
+    return forward_device(g, p, query, key, value, batch, output, wmode, weights, workspace, ws_bytes,
+                          (cudaStream_t)stream);
+}
+
+// Host-buffer variant: [inputs | output | weights | forward workspace].
+static size_t host_staging(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode wmode, size_t *off_in,
+                           size_t *off_out, size_t *off_w, size_t *off_ws)
+{
+    const size_t es = elem_size(p->dtype);
+    const size_t q = align256((size_t)(B * g->L * p->embed_dim) * es);
+    const size_t kv = align256((size_t)(B * g->S * p->embed_dim) * es);
+    size_t o = 0;
+    *off_in = o;
+    o += q + 2 * kv;
+    *off_out = o;
+    o += q;
+    *off_w = o;
+    if (wmode == PMHA_WEIGHTS_AVG) o += align256((size_t)(B * g->nnz) * 4);
+    if (wmode == PMHA_WEIGHTS_PER_HEAD) o += align256((size_t)(B * g->nnz * p->num_heads) * 4);
+    *off_ws = o;
+    return o + layout(g, p, B, wmode, true).total;
+}
+
+size_t pmha_forward_host_workspace_size(const pmha_graph *g, const pmha_params *p, int64_t batch, pmha_wmode wmode)
+{
+    if (check_params(g, p, batch) != PMHA_OK) return 0;
+    if (wmode != PMHA_WEIGHTS_NONE && wmode != PMHA_WEIGHTS_AVG && wmode != PMHA_WEIGHTS_PER_HEAD) return 0;
+    size_t a, b, c, d;
+    return host_staging(g, p, batch, wmode, &a, &b, &c, &d);
+}
+
+pmha_status pmha_forward_host(const pmha_graph *g, const pmha_params *p, const void *qh, const void *kh,
+                              const void *vh, int64_t B, void *oh, pmha_wmode wmode, float *wh, void *workspace,
+                              size_t ws_bytes, pmha_stream stream)
+{
+    pmha_status st = check_params(g, p, B);
+    if (st != PMHA_OK) return st;
+    if ((st = check_wmode(wmode, wh, true)) != PMHA_OK) return st;
+    if (!qh || !kh || !vh || !oh) {
+        set_error("pmha_forward_host: NULL host buffer");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    size_t off_in, off_out, off_w, off_ws;
+    const size_t need = host_staging(g, p, B, wmode, &off_in, &off_out, &off_w, &off_ws);
+    if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255u)) {
+        set_error("pmha_forward_host: workspace needs %zu bytes, 256-byte aligned", need);
+        return PMHA_ERR_WORKSPACE;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    const size_t es = elem_size(p->dtype);
+    const size_t qb = (size_t)(B * g->L * p->embed_dim) * es, kb = (size_t)(B * g->S * p->embed_dim) * es;
+    char *dq = ws + off_in;
+    char *dk = dq + align256(qb);
+    char *dv = dk + align256(kb);
+    const void *q_dev = dq, *k_dev = dk, *v_dev = dv;
+    {
+        StageTimer timer("h2d", s);
+        PMHA_CUDA_TRY(cudaMemcpyAsync(dq, qh, qb, cudaMemcpyHostToDevice, s));
+        if (kh == qh && g->L == g->S) k_dev = dq;
+        else PMHA_CUDA_TRY(cudaMemcpyAsync(dk, kh, kb, cudaMemcpyHostToDevice, s));
+        if (vh == kh) v_dev = k_dev;
+        else if (vh == qh && g->L == g->S) v_dev = dq;
+        else PMHA_CUDA_TRY(cudaMemcpyAsync(dv, vh, kb, cudaMemcpyHostToDevice, s));
+    }
+    float *dw = wmode != PMHA_WEIGHTS_NONE ? (float *)(ws + off_w) : nullptr;
+    st = forward_device(g, p, q_dev, k_dev, v_dev, B, ws + off_out, wmode, dw, ws + off_ws, ws_bytes - off_ws, s);
+    if (st != PMHA_OK) return st;
+    {
+        StageTimer timer("d2h", s);
+        PMHA_CUDA_TRY(cudaMemcpyAsync(oh, ws + off_out, qb, cudaMemcpyDeviceToHost, s));
+        if (dw) {
+            const size_t wb = (size_t)(B * g->nnz) * 4 * (wmode == PMHA_WEIGHTS_PER_HEAD ? p->num_heads : 1);
+            PMHA_CUDA_TRY(cudaMemcpyAsync(wh, dw, wb, cudaMemcpyDeviceToHost, s));
+        }
+    }
+    return PMHA_OK;
+}
+
+pmha_status pmha_edge_weights(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
+                              int64_t B, pmha_wmode wmode, float *weights, void *workspace, size_t ws_bytes,
+                              pmha_stream stream)
+{
+    pmha_status st = check_params(g, p, B);
+    if (st != PMHA_OK) return st;
+    if ((st = check_wmode(wmode, weights, false)) != PMHA_OK) return st;
+    if (!query || !key || !aligned16(query) || !aligned16(key)) {
+        set_error("query and key must be non-NULL, 16-byte aligned device pointers");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if ((p->embed_dim * (int64_t)elem_size(p->dtype)) % 16) {
+        set_error("embed_dim %lld gives rows that are not a multiple of 16 bytes", (long long)p->embed_dim);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    const Layout lay = layout(g, p, B, wmode, false);
+    if (!workspace || ws_bytes < lay.total || ((uintptr_t)workspace & 255u)) {
+        set_error("workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.total, ws_bytes);
+        return PMHA_ERR_WORKSPACE;
+    }
+    return attend(g, p, query, key, key, B, wmode, weights, (char *)workspace, lay, false, (cudaStream_t)stream,
+                  nullptr);
+}
+
+pmha_status pmha_device_status(pmha_stream stream)
+{
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pmha_device_status");
+    int *w = device_error_word();
+    if (!w) return PMHA_ERR_CUDA;
+    int v = 0;
+    e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "pmha_device_status");
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (v & kErrTimeoutBit) {
+            set_error("a bounded device-side wait gave up");
+            return PMHA_ERR_TIMEOUT;
+        }
+        set_error("an intermediate (q, k, v or mixed) left the fp16 range; the results since the last check "
+                  "are not valid");
+        return PMHA_ERR_OVERFLOW;
+    }
+    return PMHA_OK;
+}
+
+const char *pmha_last_error(void) { return t_err; }
+
+pmha_status pmha_profile_enable(int on)
+{
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = on != 0;
+    return PMHA_OK;
+}
+
+pmha_status pmha_profile_read(int max_stages, char *names, int64_t *launches, double *total_ms, int *n_stages)
+{
+    std::vector<Record> recs;
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        recs.swap(g_records);
+    }
+    std::vector<std::string> stage_names;
+    std::vector<int64_t> counts;
+    std::vector<double> totals;
+    pmha_status st = PMHA_OK;
+    for (const Record &r : recs) {
+        float ms = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.stop);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.start, r.stop);
+        if (e != cudaSuccess) {
+            st = cuda_fail(e, "pmha_profile_read");
+            continue;
+        }
+        size_t i = 0;
+        while (i < stage_names.size() && stage_names[i] != r.stage) ++i;
+        if (i == stage_names.size()) {
+            stage_names.push_back(r.stage);
+            counts.push_back(0);
+            totals.push_back(0.0);
+        }
+        counts[i] += 1;
+        totals[i] += ms;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        for (const Record &r : recs) {
+            g_event_pool.push_back(r.start);
+            g_event_pool.push_back(r.stop);
+        }
+    }
+    const int n = (int)stage_names.size();
+    if (n_stages) *n_stages = n;
+    for (int i = 0; i < n && i < max_stages; ++i) {
+        if (names) {
+            strncpy(names + 32 * i, stage_names[i].c_str(), 31);
+            names[32 * i + 31] = '\0';
+        }
+        if (launches) launches[i] = counts[i];
+        if (total_ms) total_ms[i] = totals[i];
+    }
+    return st;
+}
+
+int64_t pmha_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,491 @@
+// Projection GEMM on the 5th-generation tensor cores (sm_103a): tcgen05.mma
+// with fp32 accumulators in tensor memory, operands streamed into shared
+// memory by TMA, bias add and bf16 rounding fused into the epilogue.
+//
+// kpnn2 PackedMultiheadAttention, Notes step 1 (q_proj, k_proj, v_proj) and
+// step 5 (out_proj): Y = X W^T + b, W stored (out, in) like nn.Linear. The
+// head split of step 1 is a layout fact: row r of Y, columns [h*d, (h+1)*d),
+// is head h, so no data movement is needed. Up to three projections that
+// read the same X (Q|K|V of attention within one graph, K|V of a bipartite
+// map) run as one GEMM whose N axis walks the weight matrices in turn; the
+// output row then holds [Q | K | V] side by side.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0    TMA producer: X tile 128 x 64 and W tile 128 x 64 per stage,
+//             128-byte swizzle, into a 6-stage shared-memory ring
+//   warp 1    allocates 256 TMEM columns (two 128 x 128 fp32 accumulators)
+//             and issues tcgen05.mma (M=128, N=128, K=16) from one thread
+//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time, + bias, -> bf16,
+//             16-byte stores; warp w reads TMEM lanes 32*(w%4) .. +31
+// Tiles are visited m-major with the N tiles of one row block adjacent, so
+// CTAs that share an X tile run together and the re-reads hit L2.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
+// records PMHA_ERR_TIMEOUT in a device word, drains its own TMA copies and
+// MMAs (again bounded), frees its tensor memory and returns.
+#include <cuda.h>
+
+#include <mutex>
+#include <set>
+#include <type_traits>
+#include <utility>
+
+#include "pmha_internal.h"
+
+namespace pmha {
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int kStages = 6;
+constexpr int kTileABytes = BM * BK * 2;
+constexpr int kTileBBytes = BN * BK * 2;
+constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 2 * BN;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B of one 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), both
+// K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+template <typename TIn>
+__host__ __device__ constexpr uint32_t idesc()
+{
+    constexpr uint32_t f = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
+    return (1u << 4) | (f << 7) | (f << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+struct TcArgs {
+    int M, N, K, E;
+    const __nv_bfloat16 *bias[3];  // parameters are bf16
+    void *out;
+    long long ldy;
+    int *err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits until the phase with the given parity has completed. Gives up after
+// kWaitLimitNs, or at once when another role of this CTA gave up.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       int *err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeoutBit);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row atoms 1024 bytes apart.
+// start address >> 4 at bits 0-13, leading byte offset (unused for this
+// layout, 16 B) at 16-29, stride byte offset 1024 B at 32-45, descriptor
+// version 1 at bits 46-47, swizzle mode 2 (128 B) at bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(16u >> 4) << 16) |
+           ((uint64_t)(1024u >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Two fp32 values to one 32-bit word of the output type. fp16 outputs also
+// report values outside the fp16 range (or not finite) in *range_bad.
+template <typename TOut>
+__device__ __forceinline__ uint32_t pack2(float v0, float v1, bool &range_bad);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float v0, float v1, bool &)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float v0, float v1, bool &range_bad)
+{
+    if (!(fabsf(v0) <= 65504.f) || !(fabsf(v1) <= 65504.f)) range_bad = true;
+    __half2 h = __floats2half2_rn(v0, v1);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(kThreads, 1)
+k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
+          const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
+          TcArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *tiles = smem;
+    uint64_t *bars = (uint64_t *)(smem + kStages * kStageBytes);
+    uint64_t *full = bars;                    // [kStages]
+    uint64_t *empty = bars + kStages;         // [kStages]
+    uint64_t *acc_full = bars + 2 * kStages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;       // [2]
+    uint64_t *mma_done = acc_empty + 2;       // [1]
+    uint32_t *tmem_holder = (uint32_t *)(mma_done + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
+    int *issued = (int *)(tmem_holder + 2);  // [kStages]: TMA phases armed per stage
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles_n = a.N / BN;
+    const int n_tiles = ((a.M + BM - 1) / BM) * n_tiles_n;
+    const int k_blocks = a.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+            issued[s] = 0;
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&acc_full[i]), 1);
+            mbar_init(smem_u32(&acc_empty[i]), 128);
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_x)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+                const int m_blk = tile / n_tiles_n, n_blk = tile % n_tiles_n;
+                const int n_glob = n_blk * BN;
+                const int seg = n_glob / a.E;
+                const int n_loc = n_glob - seg * a.E;
+                const CUtensorMap *tw = seg == 0 ? &tm_w0 : (seg == 1 ? &tm_w1 : &tm_w2);
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err)) break;
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    issued[stage] += 1;
+                    const uint32_t sa = smem_u32(tiles + stage * kStageBytes);
+                    tma_load_2d(sa, &tm_x, kb * BK, m_blk * BM, fb);
+                    tma_load_2d(sa + kTileABytes, tw, kb * BK, n_loc, fb);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+                if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1u, abort_flag, a.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(tiles + stage * kStageBytes);
+                    const uint64_t da = smem_desc(sa), db = smem_desc(sa + kTileABytes);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // +32 bytes along K inside the swizzle atom = +2 in the address field
+                        mma_f16kind(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc<TIn>(),
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&empty[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&acc_full[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // all MMAs issued by this thread have finished once this arrives
+            mma_commit(smem_u32(mma_done));
+            int dummy = 0;
+            mbar_wait(smem_u32(mma_done), 0, (volatile int *)&dummy, a.err);
+        }
+    } else {
+        // ---------------- epilogue, 128 threads
+        const int quarter = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            if (!mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err)) break;
+            tc_fence_after();
+            const int m_blk = tile / n_tiles_n, n_blk = tile % n_tiles_n;
+            const int n_glob = n_blk * BN;
+            const int seg = n_glob / a.E;
+            const int n_loc = n_glob - seg * a.E;
+            const __nv_bfloat16 *bias = a.bias[seg];
+            const int row = m_blk * BM + quarter * 32 + lane;
+            TOut *orow = (TOut *)a.out + (long long)row * a.ldy + n_glob;
+            bool range_bad = false;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+                if (row < a.M) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
+                        if (bias) {
+                            v0 = __fadd_rn(v0, __bfloat162float(bias[n_loc + c * 32 + 2 * j]));
+                            v1 = __fadd_rn(v1, __bfloat162float(bias[n_loc + c * 32 + 2 * j + 1]));
+                        }
+                        packed[j] = pack2<TOut>(v0, v1, range_bad);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+            }
+            if (range_bad) atomicOr(a.err, kErrRangeBit);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // let the copies this CTA started land before its shared memory goes away
+        int dummy = 0;
+        for (int s = 0; s < kStages; ++s)
+            if (issued[s] > 0)
+                mbar_wait(smem_u32(&full[s]), (uint32_t)((issued[s] - 1) & 1), (volatile int *)&dummy, a.err);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    });
+    return fn;
+}
+
+// 2-D 16-bit row-major tensor (rows x cols, row stride cols), box 128 rows x 64 columns.
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, bool bf16)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int64_t E)
+{
+    return E >= BN && E % BN == 0 && E <= 65536;
+}
+
+pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, const GemmSegments &seg, void *Y,
+                    int64_t ldy, const char *stage, cudaStream_t stream)
+{
+    if (M <= 0) return PMHA_OK;
+    if (M > (int64_t)0x7fffffff - BM) {
+        set_error("gemm_tc: %lld rows exceed the 32-bit tile index", (long long)M);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    if (((uintptr_t)Y & 15) || (ldy * 2) % 16) {
+        set_error("gemm_tc: output must be 16-byte aligned with a 16-byte row pitch");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    const bool in_bf16 = in == TcType::BF16;
+    CUtensorMap mx, mw[3];
+    if (!make_map(&mx, X, M, E, in_bf16)) {
+        set_error("gemm_tc: cuTensorMapEncodeTiled failed for X (pointer %p)", X);
+        return PMHA_ERR_CUDA;
+    }
+    for (int i = 0; i < 3; ++i) {
+        const void *w = seg.w[i < seg.n_seg ? i : 0];
+        if (!make_map(&mw[i], w, E, E, in_bf16)) {
+            set_error("gemm_tc: cuTensorMapEncodeTiled failed for W (pointer %p)", w);
+            return PMHA_ERR_CUDA;
+        }
+    }
+    TcArgs a;
+    a.M = (int)M;
+    a.N = (int)(E * seg.n_seg);
+    a.K = (int)E;
+    a.E = (int)E;
+    for (int i = 0; i < 3; ++i) a.bias[i] = (const __nv_bfloat16 *)(i < seg.n_seg ? seg.b[i] : nullptr);
+    a.out = Y;
+    a.ldy = ldy;
+    a.err = device_error_word();
+    if (!a.err) return PMHA_ERR_CUDA;
+
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
+    if (in_bf16 && out == TcType::F16) kern = k_gemm_tc<__nv_bfloat16, __half>;
+    else if (in_bf16) kern = k_gemm_tc<__nv_bfloat16, __nv_bfloat16>;
+    else if (out == TcType::BF16) kern = k_gemm_tc<__half, __nv_bfloat16>;
+    else kern = k_gemm_tc<__half, __half>;
+    static std::mutex mu;
+    static std::set<std::pair<int, void *>> configured;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!configured.count({dev, (void *)kern})) {
+            PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+            configured.insert({dev, (void *)kern});
+        }
+    }
+    const int n_tiles = (int)(((M + BM - 1) / BM) * (a.N / BN));
+    const int grid = std::min(n_tiles, num_sms());
+    StageTimer timer(stage, stream);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw[0], mw[1], mw[2], a);
+    count_launch();
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+}  // namespace pmha

@@ -1,0 +1,134 @@
+// Internal declarations shared by the translation units of libpmha.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pmha.h"
+
+namespace pmha {
+
+// --------------------------------------------------------------------------
+// Graph: the live edges grouped by target, plus the work plan of the edge
+// kernel. Everything lives in one device allocation owned by the graph.
+// --------------------------------------------------------------------------
+
+// One unit of edge-kernel work: the edges [begin, end) (CSR positions) of
+// target t. slot < 0: the item covers every edge of t and writes t's result
+// directly; slot >= 0: t is split and this item writes partial softmax state
+// to partial slot `slot`, merged later.
+struct Item {
+    int32_t t, begin, end, slot;
+};
+
+// A split target: partial slots [first_slot, first_slot + n_chunks).
+struct Heavy {
+    int32_t t, first_slot, n_chunks, pad;
+};
+
+// Edges per item of a split target; targets with more edges are split.
+constexpr int kChunkEdges = 128;
+
+}  // namespace pmha
+
+struct pmha_graph {
+    int64_t L = 0, S = 0;
+    int64_t nnz_given = 0, nnz = 0;   // nnz counts appended self-loops
+    int64_t max_deg = 0;
+    int64_t n_items = 0;              // items per sample
+    int64_t n_parts = 0;              // partial slots per sample
+    int64_t n_heavy = 0;              // split targets
+    int device = 0;
+    int32_t *row_ptr = nullptr;       // L + 1
+    int32_t *col = nullptr;           // nnz, source per CSR position
+    int32_t *perm = nullptr;          // nnz, given-order edge id per CSR position
+    int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
+    pmha::Item *items = nullptr;      // n_items
+    pmha::Heavy *heavy = nullptr;     // n_heavy
+    void *mem = nullptr;              // the single allocation behind the arrays above
+};
+
+namespace pmha {
+
+// ---------------------------------------------------------------- errors
+void set_error(const char *fmt, ...);
+pmha_status cuda_fail(cudaError_t e, const char *what);
+#define PMHA_CUDA_TRY(expr)                                     \
+    do {                                                        \
+        cudaError_t _e = (expr);                                \
+        if (_e != cudaSuccess) return ::pmha::cuda_fail(_e, #expr); \
+    } while (0)
+
+// Device word of sticky error bits set by kernels: a bounded wait gave up,
+// or an fp16 intermediate left the fp16 range. Read by pmha_device_status.
+int *device_error_word();
+constexpr int kErrTimeoutBit = 1;
+constexpr int kErrRangeBit = 2;
+
+// ---------------------------------------------------------------- profiling
+// Records an event pair around a launch when profiling is on.
+struct StageTimer {
+    StageTimer(const char *stage, cudaStream_t s);
+    ~StageTimer();
+    const char *stage;
+    cudaStream_t stream;
+    int slot;
+};
+void count_launch(int n = 1);
+int num_sms();
+
+// ---------------------------------------------------------------- CSR build
+pmha_status build_csr(const int64_t *src, const int64_t *tgt, int64_t nnz, int64_t L, int64_t S,
+                      bool self_loops, cudaStream_t stream, pmha_graph **out);
+
+// ---------------------------------------------------------------- GEMMs
+// Y[m, n] = sum_k X[m, k] * W_seg[n - seg*E, k] + bias_seg[n - seg*E]
+// for n in [0, n_seg * E), where seg = n / E; X is (M, E) with row stride E,
+// Y has row stride ldy. Up to three weight segments (Q|K|V fused).
+struct GemmSegments {
+    const void *w[3];
+    const void *b[3];
+    int n_seg;
+};
+// Element types on the projection path. Layers stored in bf16 keep their
+// intermediates (q, k, v, mixed) in fp16; float32 layers stay float32.
+enum class TcType { BF16, F16, F32 };
+inline size_t type_size(TcType t) { return t == TcType::F32 ? 4 : 2; }
+
+// Tensor-core GEMM: X and W both `in` (bf16 or fp16), biases bf16, Y `out`.
+// `stage` names the launch for the stage timer (a string literal).
+bool gemm_tc_supported(int64_t E);
+pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, const GemmSegments &seg, void *Y,
+                    int64_t ldy, const char *stage, cudaStream_t stream);
+// CUDA-core GEMM with independent types for X, W (and bias) and Y.
+pmha_status gemm_simt(TcType tx, TcType tw, TcType ty, const void *X, int64_t M, int64_t E,
+                      const GemmSegments &seg, void *Y, int64_t ldy, const char *stage, cudaStream_t stream);
+// dst[i] = fp16(src[i]) for n bf16 values (the out_proj weight of a bf16 layer).
+pmha_status convert_bf16_to_f16(const void *src, void *dst, int64_t n, cudaStream_t stream);
+
+// ---------------------------------------------------------------- edge attention
+struct EdgeArgs {
+    const void *q;        // (B, L) rows, row stride q_ld elements, head h at columns h*d..
+    int64_t q_ld;
+    const void *kv;       // (B, S) rows: K at columns [0, E), V at [v_off, v_off + E)
+    int64_t kv_ld;
+    int64_t v_off;
+    void *mixed;          // (B, L, E) output of the mix (light targets written directly)
+    float *part;          // (B, n_parts, 2H + E) partial state of split targets
+    float *ml;            // (B, L, H, 2): running max (log2 units) and sum per target/head
+    float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
+    int64_t B, L, S, E, H, nnz, n_items, n_parts;
+    float score_scale;    // log2(e) / sqrt(d)
+    bool with_values;     // false: scores and (m, l) only
+};
+// `t` is the intermediate type (F16 or F32) of q, k, v and mixed.
+bool edge_supported(int64_t E, int64_t H, TcType t);
+pmha_status edge_attention(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
+pmha_status split_merge(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
+// weights[b, e(, h)] from raw scores and (m, l); in place when out == scores.
+pmha_status weights_finalize(const pmha_graph *g, const EdgeArgs &a, pmha_wmode mode, float *out,
+                             cudaStream_t s);
+
+}  // namespace pmha

@@ -1,0 +1,104 @@
+"""Shared helpers of the GPU tests: run the CUDA path through the binding and
+the oracle on the same seeded synthetic inputs, and compare."""
+from __future__ import annotations
+
+import numpy as np
+
+import synth
+
+# Outputs: max-abs error relative to the RMS of the oracle's output (the
+# stated bar), after allowing every element the half unit in the last place
+# of its own rounding to the output type: that rounding alone reaches 2.1 % of
+# RMS on workload 2 in bf16 (the oracle's output, correctly rounded to bf16,
+# misses the bare bar), so no bf16 result could pass without it.
+# Weights are probabilities, so their bar is the same number on the
+# probability scale: max-abs error <= TOL.
+TOL = {"bf16": 2e-2, "f32": 1e-5}
+MANTISSA_BITS = {"bf16": 8, "f32": 24}  # significand bits, implicit bit included
+
+
+def half_ulp(x, dt):
+    """Half the spacing of the output type's values at |x| (0 at 0)."""
+    _, e = np.frexp(np.abs(np.asarray(x, np.float64)))  # |x| = f 2^e, f in [0.5, 1)
+    return np.where(x == 0, 0.0, np.ldexp(1.0, e - MANTISSA_BITS[dt] - 1))
+
+
+def torch_dtype(dt):
+    import torch
+    return torch.float32 if dt == "f32" else torch.bfloat16
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = float(np.abs(got - ref).max()) if ref.size else 0.0
+    rms = float(np.sqrt((ref ** 2).mean())) if ref.size else 1.0
+    return err, rms
+
+
+def assert_close(name, got, ref, dt):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err, rms = rel_err(got, ref)
+    excess = float((np.abs(got - ref) - half_ulp(np.maximum(np.abs(got), np.abs(ref)), dt)).max()) if ref.size else 0
+    assert excess <= TOL[dt] * rms, (f"{name}: max-abs error beyond the output rounding {excess:.4e} > {TOL[dt]} x "
+                                     f"RMS {rms:.4e} (raw max-abs {err:.4e})")
+    return excess / rms
+
+
+def assert_close_weights(name, got, ref, dt):
+    err, _ = rel_err(got, ref)
+    assert err <= TOL[dt], f"{name}: max-abs error {err:.4e} > {TOL[dt]}"
+    return err
+
+
+class Case:
+    """One seeded problem: graph, tokens and parameters (numpy, rounded to dt)."""
+
+    def __init__(self, src, tgt, L, S, E, H, B, dt, seed, bipartite=False, bias=True, xq=None, xkv=None,
+                 params=None):
+        self.src, self.tgt = np.asarray(src, np.int64), np.asarray(tgt, np.int64)
+        self.L, self.S, self.E, self.H, self.B, self.dt = L, S, E, H, B, dt
+        rng = np.random.default_rng(seed)
+        self.params = params if params is not None else synth.make_params(rng, E, dt, bias=bias)
+        self.xq = xq if xq is not None else synth.make_tokens(rng, B, L, E, dt)
+        if bipartite or L != S:
+            self.xkv = xkv if xkv is not None else synth.make_tokens(rng, B, S, E, dt)
+        else:
+            self.xkv = self.xq
+
+    @staticmethod
+    def workload(wid, batch=None):
+        w = synth.workload(wid)
+        src, tgt = synth.make_graph(wid)
+        xq, xkv, params = synth.make_inputs(wid, batch)
+        B = xq.shape[0]
+        return Case(src, tgt, w.query_features, w.key_features, w.embed_dim, w.num_heads, B, w.dtype, 0,
+                    bipartite=w.bipartite, xq=xq, xkv=xkv if xkv is not None else xq, params=params)
+
+    # ------------------------------------------------------------ CUDA path
+    def device_inputs(self, dev):
+        import torch
+        tdt = torch_dtype(self.dt)
+        xq = torch.from_numpy(self.xq).to(dev).to(tdt)
+        xkv = xq if self.xkv is self.xq else torch.from_numpy(self.xkv).to(dev).to(tdt)
+        return xq, xkv
+
+    def run(self, dev, wmode="none", add_self_loops=False, graph=None):
+        import torch
+        import graph_sparse_head_gb300 as pmha
+        params = pmha.Params.from_arrays(self.params, self.H, torch_dtype(self.dt), dev)
+        if graph is None:
+            graph = pmha.pmha_build_csr(torch.from_numpy(self.src).to(dev), torch.from_numpy(self.tgt).to(dev),
+                                        self.L, self.S, add_self_loops)
+        xq, xkv = self.device_inputs(dev)
+        out, w = pmha.pmha_forward(graph, params, xq, xkv, xkv, wmode)
+        pmha.pmha_device_status()
+        return graph, params, out, w
+
+    # ------------------------------------------------------------ oracle
+    def oracle(self, need_weights=True, src=None, tgt=None):
+        import oracle
+        src = self.src if src is None else src
+        tgt = self.tgt if tgt is None else tgt
+        return oracle.forward(self.xq, self.xkv, self.xkv, self.params, src, tgt, self.H, need_weights)
