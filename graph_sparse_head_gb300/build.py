@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpmha.so")
-SOURCES = ["api.cu", "csr.cu", "gemm_simt.cu", "gemm_tc.cu", "edge_attn.cu"]
+SOURCES = ["api.cu", "csr.cu", "gemm_simt.cu", "gemm_tc.cu", "edge_attn.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "pmha_internal.h"), os.path.join(ROOT, "include", "pmha.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

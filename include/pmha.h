@@ -209,6 +209,27 @@ pmha_status pmha_edge_weights(const pmha_graph *graph, const pmha_params *params
  */
 pmha_status pmha_device_status(pmha_stream stream);
 
+/*
+ * pmha_forward_noalloc - pmha_forward for callers that cannot allocate device
+ * memory when they call the layer (a host whose allocator owns all device
+ * memory, or a call site where cudaMalloc / cudaFree may not run). The pages
+ * have no counterpart: it is a property of this library, not of the method.
+ *
+ * The caller passes inputs and outputs exactly as for pmha_forward; the
+ * workspace comes from a scratch array of PMHA_NOALLOC_SCRATCH_BYTES built
+ * into the library, which every GPU that loads this code keeps until the
+ * process exits. Problems whose pmha_forward_workspace_size exceeds it are
+ * rejected with PMHA_ERR_WORKSPACE and a message. The call allocates nothing.
+ * Its first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. All calls
+ * share the array: calls whose GPU work overlaps (other streams, unordered
+ * threads) race on it; calls queued on one stream are safe.
+ */
+#define PMHA_NOALLOC_SCRATCH_BYTES (64u << 20)
+pmha_status pmha_forward_noalloc(const pmha_graph *graph, const pmha_params *params, const void *query,
+                                 const void *key, const void *value, int64_t batch, void *output,
+                                 pmha_wmode wmode, float *weights, pmha_stream stream);
+
 /* Message describing the last failure of a call made by this thread ("" if none). */
 const char *pmha_last_error(void);
 
