@@ -18,8 +18,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpmha.so")
-SOURCES = ["api.cu", "csr.cu", "gemm_simt.cu", "gemm_tc.cu", "edge_attn.cu", "noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "pmha_internal.h"), os.path.join(ROOT, "include", "pmha.h")]
+SOURCES = ["api.cu", "csr.cu", "gemm_simt.cu", "gemm_tc.cu", "edge_attn.cu", "edge_attn_f16.cu", "edge_attn_f32.cu",
+           "noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "pmha_internal.h"), os.path.join(CSRC, "edge_stream.cuh"), os.path.join(ROOT, "include", "pmha.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                 "-Xptxas", "-warn-spills", "-I" + os.path.join(ROOT, "include")]
@@ -39,14 +40,16 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), build_dir: str = BUILD,
+          out_lib: str = LIB) -> str:
+    """Compile the sources (only those older than their output) and link the library."""
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     jobs = []
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + HEADERS):
             jobs.append([cc, *FLAGS, *extra_flags, "-c", s, "-o", o])
@@ -62,11 +65,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             for out in ex.map(run, jobs):
                 if verbose and out.strip():
                     print(out, file=sys.stderr)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(out_lib, objs):
+        tmp = out_lib + f".tmp{os.getpid()}"
         run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, out_lib)
+    return out_lib
 
 
 if __name__ == "__main__":

@@ -206,7 +206,7 @@ Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode w
     l.mixed = o;
     if (with_values) o += align256((size_t)(B * g->L * E) * es);
     l.part = o;
-    o += align256((size_t)(B * g->n_parts * (2 * H + E)) * 4);
+    o += align256((size_t)(B * 2 * g->n_units * (2 * H + E)) * 4);
     l.ml = o;
     if (wmode != PMHA_WEIGHTS_NONE) o += align256((size_t)(B * g->L * H * 2) * 4);
     l.scores = o;
@@ -295,8 +295,6 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.E = E;
     a.H = H;
     a.nnz = g->nnz;
-    a.n_items = g->n_items;
-    a.n_parts = g->n_parts;
     a.score_scale = (float)(1.4426950408889634 / sqrt((double)(E / H)));
     a.with_values = with_values;
     if ((st = edge_attention(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;

@@ -15,7 +15,9 @@
 //   sort      LSD radix sort, 8-bit digits, stable scatter per tile
 //   checks    adjacent equal keys -> duplicate
 //   view      row_ptr by binary search; col, perm, target of each edge id
-//   plan      per-target item counts, scans, item and split-target lists
+//   plan      first target of every unit of kUnitEdges positions; list of
+//             targets the merge kernel finishes (crossing a unit boundary,
+//             or without edges)
 // followed by a single device-to-host copy of a summary and one synchronize.
 #include <algorithm>
 #include <vector>
@@ -41,9 +43,7 @@ enum : int { kFlagRange = 1, kFlagDuplicate = 2 };
 struct Summary {
     int flags;
     int nnz_total;
-    int n_chunks;   // partial slots per sample
-    int n_light;
-    int n_heavy;
+    int n_merge;
     int max_deg;
 };
 
@@ -338,53 +338,39 @@ __global__ void k_row_ptr(const K *__restrict__ keys, const Summary *__restrict_
     row_ptr[t] = lo;
 }
 
-__global__ void k_plan_counts(const int32_t *__restrict__ row_ptr, int L, int *__restrict__ chunks,
-                              int *__restrict__ light, int *__restrict__ heavy,
+// Target of the first position of every unit: the largest t with
+// row_ptr[t] <= u * kUnitEdges (it has an edge there, since positions are < nnz).
+__global__ void k_unit_first(const int32_t *__restrict__ row_ptr, int L, const Summary *__restrict__ sum,
+                             int32_t *__restrict__ unit_first_t)
+{
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    const int n_units = (sum->nnz_total + kUnitEdges - 1) / kUnitEdges;
+    if (u >= n_units) return;
+    const int pos = u * kUnitEdges;
+    int lo = 0, hi = L;  // invariant: row_ptr[lo] <= pos < row_ptr[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (row_ptr[mid] <= pos) lo = mid;
+        else hi = mid;
+    }
+    unit_first_t[u] = lo;
+}
+
+__global__ void k_merge_flags(const int32_t *__restrict__ row_ptr, int L, int *__restrict__ flag,
                               Summary *__restrict__ sum)
 {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= L) return;
-    const int deg = row_ptr[t + 1] - row_ptr[t];
-    const bool split = deg > kChunkEdges;
-    chunks[t] = split ? (deg + kChunkEdges - 1) / kChunkEdges : 0;
-    light[t] = split ? 0 : 1;
-    heavy[t] = split ? 1 : 0;
+    const int b = row_ptr[t], e = row_ptr[t + 1], deg = e - b;
+    flag[t] = (deg == 0 || b / kUnitEdges != (e - 1) / kUnitEdges) ? 1 : 0;
     atomicMax(&sum->max_deg, deg);
 }
 
-__global__ void k_plan_write(const int32_t *__restrict__ row_ptr, int L,
-                             const int *__restrict__ chunk_off, const int *__restrict__ light_off,
-                             const int *__restrict__ heavy_off, const Summary *__restrict__ sum,
-                             Item *__restrict__ items, Heavy *__restrict__ heavy)
+__global__ void k_merge_write(const int *__restrict__ flag, const int *__restrict__ off, int L,
+                              int32_t *__restrict__ merge_t)
 {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= L) return;
-    const int b = row_ptr[t], e = row_ptr[t + 1], deg = e - b;
-    if (deg > kChunkEdges) {
-        const int n_chunks = (deg + kChunkEdges - 1) / kChunkEdges;
-        const int first = chunk_off[t];
-        for (int c = 0; c < n_chunks; ++c) {
-            Item it;
-            it.t = t;
-            it.begin = b + c * kChunkEdges;
-            it.end = min(e, it.begin + kChunkEdges);
-            it.slot = first + c;
-            items[first + c] = it;
-        }
-        Heavy h;
-        h.t = t;
-        h.first_slot = first;
-        h.n_chunks = n_chunks;
-        h.pad = 0;
-        heavy[heavy_off[t]] = h;
-    } else {
-        Item it;
-        it.t = t;
-        it.begin = b;
-        it.end = e;
-        it.slot = -1;
-        items[sum->n_chunks + light_off[t]] = it;
-    }
+    if (t < L && flag[t]) merge_t[off[t]] = t;
 }
 
 inline int blocks_for(int64_t n, int threads) { return (int)std::max<int64_t>(1, (n + threads - 1) / threads); }
@@ -395,8 +381,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
 {
     const int nnz = (int)nnz64;
     const int cap = (int)(nnz64 + (self_loops ? L : 0));
-    const int max_items = (int)(L + 2 * ((int64_t)cap / kChunkEdges) + 2);
-    const int max_heavy = cap / kChunkEdges + 1;
+    const int max_units = cap / kUnitEdges + 1;
     int bits = 0;
     {
         const unsigned long long ls = (unsigned long long)L * (unsigned long long)S;
@@ -417,9 +402,9 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     size_t off_col = off_row + align((size_t)(L + 1) * 4);
     size_t off_perm = off_col + align((size_t)cap * 4);
     size_t off_tge = off_perm + align((size_t)cap * 4);
-    size_t off_items = off_tge + align((size_t)cap * 4);
-    size_t off_heavy = off_items + align((size_t)max_items * sizeof(Item));
-    size_t graph_bytes = off_heavy + align((size_t)max_heavy * sizeof(Heavy));
+    size_t off_units = off_tge + align((size_t)cap * 4);
+    size_t off_merge = off_units + align((size_t)max_units * 4);
+    size_t graph_bytes = off_merge + align((size_t)L * 4);
 
     // temporaries
     const int n_tiles = std::max(1, (cap + kSortTile - 1) / kSortTile);
@@ -460,14 +445,14 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     g->col = (int32_t *)(gm + off_col);
     g->perm = (int32_t *)(gm + off_perm);
     g->tgt_of_edge = (int32_t *)(gm + off_tge);
-    g->items = (Item *)(gm + off_items);
-    g->heavy = (Heavy *)(gm + off_heavy);
+    g->unit_first_t = (int32_t *)(gm + off_units);
+    g->merge_t = (int32_t *)(gm + off_merge);
 
     K *keys_a = (K *)(tm + t_keys_a), *keys_b = (K *)(tm + t_keys_b);
     int *vals_a = (int *)(tm + t_vals_a), *vals_b = (int *)(tm + t_vals_b);
     int *hist = (int *)(tm + t_hist), *scan_tmp = (int *)(tm + t_scan);
     int *has_loop = (int *)(tm + t_loop), *miss = (int *)(tm + t_miss);
-    int *c1 = (int *)(tm + t_c1), *c2 = (int *)(tm + t_c2), *c3 = (int *)(tm + t_c3);
+    int *c1 = (int *)(tm + t_c1), *c2 = (int *)(tm + t_c2);
     int *tot = (int *)(tm + t_tot);
     Summary *dsum = (Summary *)(tm + t_sum);
 
@@ -497,13 +482,11 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         k_check_and_view<K><<<blocks_for(cap, TB), TB, 0, stream>>>(keys_s, vals_s, S, dsum, g->col, g->perm,
                                                                     g->tgt_of_edge);
         k_row_ptr<K><<<blocks_for(L + 1, TB), TB, 0, stream>>>(keys_s, dsum, L, S, g->row_ptr);
-        k_plan_counts<<<blocks_for(L, TB), TB, 0, stream>>>(g->row_ptr, (int)L, c1, c2, c3, dsum);
-        count_launch(3);
-        exclusive_scan(c1, c1, (int)L, &dsum->n_chunks, scan_tmp, stream);
-        exclusive_scan(c2, c2, (int)L, &dsum->n_light, scan_tmp, stream);
-        exclusive_scan(c3, c3, (int)L, &dsum->n_heavy, scan_tmp, stream);
-        k_plan_write<<<blocks_for(L, TB), TB, 0, stream>>>(g->row_ptr, (int)L, c1, c2, c3, dsum, g->items,
-                                                           g->heavy);
+        k_unit_first<<<blocks_for(max_units, TB), TB, 0, stream>>>(g->row_ptr, (int)L, dsum, g->unit_first_t);
+        k_merge_flags<<<blocks_for(L, TB), TB, 0, stream>>>(g->row_ptr, (int)L, c1, dsum);
+        count_launch(4);
+        exclusive_scan(c1, c2, (int)L, &dsum->n_merge, scan_tmp, stream);
+        k_merge_write<<<blocks_for(L, TB), TB, 0, stream>>>(c1, c2, (int)L, g->merge_t);
         count_launch();
         if ((ce = cudaGetLastError()) != cudaSuccess) break;
         if ((ce = cudaMemcpyAsync(host_sum, dsum, sizeof(Summary), cudaMemcpyDeviceToHost, stream)) !=
@@ -524,9 +507,8 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     if (st == PMHA_OK) {
         g->nnz = host_sum->nnz_total;
         g->max_deg = host_sum->max_deg;
-        g->n_parts = host_sum->n_chunks;
-        g->n_heavy = host_sum->n_heavy;
-        g->n_items = (int64_t)host_sum->n_chunks + host_sum->n_light;
+        g->n_units = (g->nnz + kUnitEdges - 1) / kUnitEdges;
+        g->n_merge = host_sum->n_merge;
     }
     cudaFree(tm);
     cudaFreeHost(host_sum);

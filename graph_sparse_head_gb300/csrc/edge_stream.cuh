@@ -1,0 +1,501 @@
+// The streaming edge-attention kernel (kpnn2 PackedMultiheadAttention,
+// Notes steps 2-4), templated on its lane shape. Included by the
+// translation units that instantiate it for fp16 and float32 intermediates.
+//
+// Work decomposition. The CSR positions of one sample are cut into units of
+// kUnitEdges consecutive positions (edges of consecutive targets, each
+// target's edges ordered by source). A unit is walked by one "slot": the LPE
+// lanes that own one row of channels, a lane owning CPL consecutive channels
+// (one whole head when the head has at most 16 channels). A warp runs
+// 32 / LPE units side by side. Every slot does the same gather work whatever
+// the in-degrees, and no target needs atomics: a target inside one unit is
+// finished there, a target crossing a unit boundary leaves partial softmax
+// states that the merge kernel combines.
+//
+// Per edge, a lane gathers its chunks of the source's k and v rows through
+// cp.async into a per-lane ring of shared-memory stages, kDepth edges ahead
+// of use, so the loads in flight hold no registers. Edges go two per step:
+// when both belong to the current target their scores are independent and
+// share one rescale; at a target boundary they go one at a time. Source
+// indices (three windows of LPE positions), target bounds (row_ptr) and the
+// next target's q row are prefetched in registers. When a head spans several lanes, its dot
+// product is a butterfly sum over them, so those lanes hold the same score.
+//
+// The softmax is online, in log2 units: s = (q . k) * log2(e)/sqrt(d) with q
+// pre-scaled in fp32; m = running max, l = running sum of 2^(s - m), acc =
+// running sum of 2^(s - m) v, updated with paired fp32 FMAs. The (m, l)
+// arithmetic uses explicit round-to-nearest operations so that it is identical in the variants with and without values; that makes
+// pmha_edge_weights bit-identical to the weights of pmha_forward.
+#pragma once
+
+#include <math.h>
+
+#include "pmha_internal.h"
+
+namespace pmha {
+namespace stream {
+
+#ifndef PMHA_STREAM_DEPTH
+#define PMHA_STREAM_DEPTH 6
+#endif
+#ifndef PMHA_STREAM_WARPS
+#define PMHA_STREAM_WARPS 4
+#endif
+constexpr int kWarps = PMHA_STREAM_WARPS;  // warps per block
+constexpr int kDepth = PMHA_STREAM_DEPTH;  // edges in flight per slot (even: two per step)
+constexpr int kRing = kDepth + 2;          // stages: a stage is refilled one step after it was read
+
+struct Args {
+    const void *q;
+    long long q_ld;
+    const void *kv;
+    long long kv_ld, v_off;
+    void *mixed;
+    float *part;
+    float *ml;
+    float *scores;
+    const int32_t *row_ptr;
+    const int32_t *col;
+    const int32_t *perm;
+    const int32_t *unit_first_t;
+    long long n_units, nnz;
+    int B, L, S, E, H, d;
+    float score_scale;
+};
+
+template <typename T, int CPL, bool WV>
+constexpr int smem_bytes()
+{
+    return kWarps * kRing * (WV ? 2 : 1) * 32 * CPL * (int)sizeof(T);
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+template <int CB>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void *src)
+{
+    if constexpr (CB >= 16) {
+#pragma unroll
+        for (int i = 0; i < CB / 16; ++i)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * i),
+                         "l"((const char *)src + 16 * i)
+                         : "memory");
+    } else {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(CB) : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int CB>
+struct Raw {
+    uint32_t w[CB / 4];
+};
+
+template <int CB>
+__device__ __forceinline__ Raw<CB> lds_raw(uint32_t addr)
+{
+    Raw<CB> r;
+    if constexpr (CB % 16 == 0) {
+#pragma unroll
+        for (int i = 0; i < CB / 16; ++i)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(r.w[4 * i]), "=r"(r.w[4 * i + 1]), "=r"(r.w[4 * i + 2]), "=r"(r.w[4 * i + 3])
+                         : "r"(addr + 16 * i));
+    } else if constexpr (CB == 8) {
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "r"(addr));
+    } else {
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r.w[0]) : "r"(addr));
+    }
+    return r;
+}
+
+template <int CB>
+__device__ __forceinline__ Raw<CB> ldg_raw(const void *p)
+{
+    Raw<CB> r;
+    if constexpr (CB % 16 == 0) {
+#pragma unroll
+        for (int i = 0; i < CB / 16; ++i) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p) + i);
+            r.w[4 * i] = u.x;
+            r.w[4 * i + 1] = u.y;
+            r.w[4 * i + 2] = u.z;
+            r.w[4 * i + 3] = u.w;
+        }
+    } else if constexpr (CB == 8) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        r.w[0] = u.x;
+        r.w[1] = u.y;
+    } else {
+        r.w[0] = __ldg(reinterpret_cast<const unsigned int *>(p));
+    }
+    return r;
+}
+
+// ---- paired fp32 arithmetic (each half rounds exactly like its scalar op)
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk(float x, float y)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 upk(f2 r)
+{
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+__device__ __forceinline__ f2 ffma2(f2 a, f2 b, f2 c)
+{
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2 fmul2(f2 a, f2 b)
+{
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// CPL channels of type T in `r`, widened to CPL / 2 fp32 pairs.
+template <typename T, int CPL>
+__device__ __forceinline__ void widen2(const Raw<CPL * (int)sizeof(T)> &r, f2 (&f)[CPL / 2])
+{
+    if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int j = 0; j < CPL / 2; ++j) {
+            const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&r.w[j]));
+            f[j] = pk(x.x, x.y);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CPL / 2; ++j) f[j] = pk(__uint_as_float(r.w[2 * j]), __uint_as_float(r.w[2 * j + 1]));
+    }
+}
+
+template <typename T, int CPL>
+__device__ __forceinline__ void store_row(T *p, const f2 (&v)[CPL / 2])
+{
+    if constexpr (sizeof(T) == 2) {
+        uint32_t w[CPL / 2];
+#pragma unroll
+        for (int j = 0; j < CPL / 2; ++j) {
+            const float2 x = upk(v[j]);
+            __half2 h = __floats2half2_rn(x.x, x.y);
+            w[j] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        if constexpr (CPL * 2 >= 16) {
+#pragma unroll
+            for (int i = 0; i < CPL * 2 / 16; ++i)
+                reinterpret_cast<uint4 *>(p)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        } else if constexpr (CPL * 2 == 8) {
+            *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+        } else {
+            *reinterpret_cast<uint32_t *>(p) = w[0];
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CPL / 2; ++j) reinterpret_cast<float2 *>(p)[j] = upk(v[j]);
+    }
+}
+
+template <typename T, int CPL, int LPE, bool WV, bool WS>
+__global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
+{
+    constexpr int P = 32 / LPE;               // slots per warp
+    constexpr int CB = CPL * (int)sizeof(T);  // bytes per lane per row
+    constexpr int NR = WV ? 2 : 1;            // rows staged per edge: k (and v)
+    constexpr int NP = CPL / 2;               // fp32 pairs per lane
+    constexpr int STAGE = NR * 32 * CB;       // bytes of one stage of one warp
+    extern __shared__ __align__(16) unsigned char smem_dyn[];
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int slot = lane / LPE, grp = lane % LPE;
+    const unsigned smask = LPE == 32 ? 0xffffffffu : (((1u << LPE) - 1u) << (slot * LPE));
+    const long long gu = ((long long)blockIdx.x * kWarps + warp) * P + slot;
+    if (gu >= (long long)a.B * a.n_units) return;  // the whole slot leaves together
+    const int b = (int)(gu / a.n_units);
+    const int u = (int)(gu - (long long)b * a.n_units);
+    const int e0 = u * kUnitEdges;
+    const int n = (int)min((long long)kUnitEdges, a.nnz - e0);
+    const int e1 = e0 + n;
+
+    const int c0 = grp * CPL;
+    const int head = c0 / a.d;
+    const int lph = a.d / CPL;  // lanes per head (1 when a lane owns a whole head)
+    const bool head_leader = (grp & (lph - 1)) == 0;
+
+    const uint32_t sbase = smem_u32(smem_dyn) + (uint32_t)(warp * kRing * STAGE + lane * CB);
+    const char *KVb = (const char *)a.kv + ((long long)b * a.S * a.kv_ld + c0) * (long long)sizeof(T);
+    const long long row_bytes = a.kv_ld * (long long)sizeof(T);
+    const long long v_bytes = a.v_off * (long long)sizeof(T);
+    const T *Qb = (const T *)a.q + (long long)b * a.L * a.q_ld + c0;
+    float *scores_b = WS ? a.scores + (long long)b * a.nnz * a.H : nullptr;
+    const int32_t *colu = a.col + e0;
+
+    // ---- gathers: windows w, w + 1, w + 2 of source indices (lane grp holds position w * LPE + grp)
+    auto ldcol = [&](int w) -> int {
+        const int p = w * LPE + grp;
+        return p < n ? colu[p] : 0;
+    };
+    int iw = 0;
+    int cw0 = ldcol(0), cw1 = ldcol(1), cw2 = ldcol(2);
+    // edges j and j + 1 (j even) in one commit group; both lie in one window
+    auto issue2 = [&](int j) {
+        if (j >= (iw + 1) * LPE) {
+            ++iw;
+            cw0 = cw1;
+            cw1 = cw2;
+            cw2 = ldcol(iw + 2);
+        }
+        const int s0 = __shfl_sync(smask, cw0, j & (LPE - 1), LPE);
+        const int s1 = __shfl_sync(smask, cw0, (j + 1) & (LPE - 1), LPE);
+        if (j < n) {
+            const char *row = KVb + (long long)s0 * row_bytes;
+            const uint32_t dst = sbase + (uint32_t)((j % kRing) * STAGE);
+            cp_async<CB>(dst, row);
+            if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
+        }
+        if (j + 1 < n) {
+            const char *row = KVb + (long long)s1 * row_bytes;
+            const uint32_t dst = sbase + (uint32_t)(((j + 1) % kRing) * STAGE);
+            cp_async<CB>(dst, row);
+            if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kDepth; j += 2) issue2(j);
+
+    // ---- given-order edge ids for the score write-out
+    int pw = 0, perm_cur = 0, perm_nxt = 0;
+    if constexpr (WS) {
+        perm_cur = grp < n ? a.perm[e0 + grp] : 0;
+        perm_nxt = LPE + grp < n ? a.perm[e0 + LPE + grp] : 0;
+    }
+    auto edge_id = [&](int j) -> int {  // j never decreases
+        if (j >= (pw + 1) * LPE) {
+            ++pw;
+            perm_cur = perm_nxt;
+            const int p = (pw + 1) * LPE + grp;
+            perm_nxt = p < n ? a.perm[e0 + p] : 0;
+        }
+        return __shfl_sync(smask, perm_cur, j & (LPE - 1), LPE);
+    };
+
+    // ---- target bounds: lane grp holds row_ptr[tw + grp + 1], the end of target tw + grp
+    int t = a.unit_first_t[u];
+    int tw = t;
+    int rp_cur = tw + grp < a.L ? a.row_ptr[tw + grp + 1] : (int)a.nnz;
+    int rp_nxt = tw + LPE + grp < a.L ? a.row_ptr[tw + LPE + grp + 1] : (int)a.nnz;
+    auto end_of = [&](int tt) -> int {  // row_ptr[tt + 1]; tt never decreases
+        while (tt - tw >= LPE) {
+            tw += LPE;
+            rp_cur = rp_nxt;
+            rp_nxt = tw + LPE + grp < a.L ? a.row_ptr[tw + LPE + grp + 1] : (int)a.nnz;
+        }
+        return __shfl_sync(smask, rp_cur, tt - tw, LPE);
+    };
+    int bound = end_of(t);
+    const bool first_started_here = a.row_ptr[t] == e0;
+    bool is_first = true;
+
+    f2 q2[NP];
+    const f2 sc2 = pk(a.score_scale, a.score_scale);
+    auto set_q = [&](const Raw<CB> &r) {
+        widen2<T, CPL>(r, q2);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) q2[j] = fmul2(q2[j], sc2);
+    };
+    set_q(ldg_raw<CB>(Qb + (long long)t * a.q_ld));
+    Raw<CB> qnext = ldg_raw<CB>(Qb + (long long)min(t + 1, a.L - 1) * a.q_ld);
+
+    float m = -INFINITY, l = 0.f;
+    f2 acc2[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) acc2[j] = 0ull;
+
+    // finish target t in this unit: a complete target writes its result, a
+    // target crossing a unit boundary its partial state
+    auto finish = [&]() {
+        const bool complete = (is_first ? first_started_here : true) && bound <= e1;
+        if (complete) {
+            if constexpr (WV) {
+                const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
+                const f2 inv2 = pk(inv, inv);
+                f2 o[NP];
+#pragma unroll
+                for (int j = 0; j < NP; ++j) o[j] = fmul2(acc2[j], inv2);
+                store_row<T, CPL>((T *)a.mixed + ((long long)b * a.L + t) * a.E + c0, o);
+            }
+            if (a.ml && head_leader) {
+                float *p = a.ml + (((long long)b * a.L + t) * a.H + head) * 2;
+                p[0] = m;
+                p[1] = l;
+            }
+        } else {
+            const int slot_id = 2 * u + (is_first ? 0 : 1);
+            float *p = a.part + ((long long)b * 2 * a.n_units + slot_id) * (2 * a.H + a.E);
+            if (head_leader) {
+                p[head] = m;
+                p[a.H + head] = l;
+            }
+            if constexpr (WV) {
+#pragma unroll
+                for (int j = 0; j < NP; ++j) reinterpret_cast<float2 *>(p + 2 * a.H + c0)[j] = upk(acc2[j]);
+            }
+        }
+    };
+    // move from t to the target of position pos (> the end of t)
+    auto advance = [&](int pos) {
+        finish();
+        is_first = false;
+        const int t_prev = t;
+        do {
+            ++t;
+            bound = end_of(t);
+        } while (bound <= pos);
+        set_q(t == t_prev + 1 ? qnext : ldg_raw<CB>(Qb + (long long)t * a.q_ld));
+        qnext = ldg_raw<CB>(Qb + (long long)min(t + 1, a.L - 1) * a.q_ld);
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) acc2[i] = 0ull;
+    };
+    // the head's score of one staged k row (two independent partial sums)
+    auto score = [&](const Raw<CB> &kr) -> float {
+        f2 k2[NP];
+        widen2<T, CPL>(kr, k2);
+        f2 da = 0ull, db = 0ull;
+#pragma unroll
+        for (int i = 0; i < NP; i += 2) {
+            da = ffma2(q2[i], k2[i], da);
+            if (i + 1 < NP) db = ffma2(q2[i + 1], k2[i + 1], db);
+        }
+        const float2 fa = upk(da), fb = upk(db);
+        float dot = __fadd_rn(__fadd_rn(fa.x, fb.x), __fadd_rn(fa.y, fb.y));
+        for (int o = 1; o < lph; o <<= 1) dot = __fadd_rn(dot, __shfl_xor_sync(smask, dot, o, LPE));
+        return dot;
+    };
+    auto mix = [&](const Raw<CB> &vr, float p) {
+        f2 v2[NP];
+        widen2<T, CPL>(vr, v2);
+        const f2 p2 = pk(p, p);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) acc2[i] = ffma2(p2, v2[i], acc2[i]);
+    };
+    auto rescale = [&](float scale) {
+        const f2 s2 = pk(scale, scale);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) acc2[i] = fmul2(acc2[i], s2);
+    };
+    // one edge through the online softmax (used at target boundaries)
+    auto one = [&](int j, const Raw<CB> &kr, const Raw<CB> &vr) {
+        const int pos = e0 + j;
+        if (pos >= bound) advance(pos);
+        const float dot = score(kr);
+        if constexpr (WS) {
+            const int e = edge_id(j);
+            if (head_leader) scores_b[(long long)e * a.H + head] = dot;
+        }
+        const float m_new = fmaxf(m, dot);
+        const float scale = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, m_new));
+        const float p = ex2(__fsub_rn(dot, m_new));
+        l = __fadd_rn(__fmul_rn(l, scale), p);
+        if constexpr (WV) {
+            rescale(scale);
+            mix(vr, p);
+        }
+        m = m_new;
+    };
+
+    for (int j = 0; j < n; j += 2) {
+        cp_async_wait<kDepth / 2 - 1>();
+        const uint32_t st0 = sbase + (uint32_t)((j % kRing) * STAGE);
+        const uint32_t st1 = sbase + (uint32_t)(((j + 1) % kRing) * STAGE);
+        const Raw<CB> kr0 = lds_raw<CB>(st0);
+        const Raw<CB> kr1 = lds_raw<CB>(st1);
+        Raw<CB> vr0, vr1;
+        if constexpr (WV) {
+            vr0 = lds_raw<CB>(st0 + 32 * CB);
+            vr1 = lds_raw<CB>(st1 + 32 * CB);
+        }
+        issue2(j + kDepth);
+
+        const int pos = e0 + j;
+        if (j + 1 < n && pos + 1 < bound) {
+            // both edges belong to t: two independent scores, one rescale
+            const float d0 = score(kr0), d1 = score(kr1);
+            if constexpr (WS) {
+                const int i0 = edge_id(j), i1 = edge_id(j + 1);
+                if (head_leader) {
+                    scores_b[(long long)i0 * a.H + head] = d0;
+                    scores_b[(long long)i1 * a.H + head] = d1;
+                }
+            }
+            const float m_new = fmaxf(m, fmaxf(d0, d1));
+            const float scale = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, m_new));
+            const float p0 = ex2(__fsub_rn(d0, m_new));
+            const float p1 = ex2(__fsub_rn(d1, m_new));
+            l = __fadd_rn(__fadd_rn(__fmul_rn(l, scale), p0), p1);
+            if constexpr (WV) {
+                rescale(scale);
+                mix(vr0, p0);
+                mix(vr1, p1);
+            }
+            m = m_new;
+        } else {
+            one(j, kr0, vr0);
+            if (j + 1 < n) one(j + 1, kr1, vr1);
+        }
+    }
+    cp_async_wait<0>();
+    finish();
+}
+
+// Instantiated in edge_attn_f16.cu / edge_attn_f32.cu.
+template <typename T, int CPL, int LPE, bool WV>
+pmha_status launch(const Args &k, long long slots, cudaStream_t s)
+{
+    constexpr int smem = smem_bytes<T, CPL, WV>();
+    constexpr int P = 32 / LPE;
+    const long long warps = (slots + P - 1) / P;
+    const long long blocks = (warps + kWarps - 1) / kWarps;
+    auto kern = k.scores ? k_edge_stream<T, CPL, LPE, WV, true> : k_edge_stream<T, CPL, LPE, WV, false>;
+    if constexpr (smem > 48 * 1024) {
+        PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    }
+    kern<<<(unsigned)blocks, kWarps * 32, smem, s>>>(k);
+    return PMHA_OK;
+}
+
+template <typename T, int CPL, bool WV>
+pmha_status launch_lpe(int lpe, const Args &k, long long slots, cudaStream_t s)
+{
+    switch (lpe) {
+    case 2: return launch<T, CPL, 2, WV>(k, slots, s);
+    case 4: return launch<T, CPL, 4, WV>(k, slots, s);
+    case 8: return launch<T, CPL, 8, WV>(k, slots, s);
+    case 16: return launch<T, CPL, 16, WV>(k, slots, s);
+    case 32: return launch<T, CPL, 32, WV>(k, slots, s);
+    default: return PMHA_ERR_UNSUPPORTED;
+    }
+}
+
+// Entry points of the two instantiating translation units.
+pmha_status launch_f16(int cpl, int lpe, bool wv, const Args &k, long long slots, cudaStream_t s);
+pmha_status launch_f32(int cpl, int lpe, bool wv, const Args &k, long long slots, cudaStream_t s);
+
+}  // namespace stream
+}  // namespace pmha

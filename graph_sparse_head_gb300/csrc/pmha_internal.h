@@ -13,23 +13,17 @@ namespace pmha {
 // --------------------------------------------------------------------------
 // Graph: the live edges grouped by target, plus the work plan of the edge
 // kernel. Everything lives in one device allocation owned by the graph.
+//
+// Work plan: the CSR positions [0, nnz) of one sample are cut into units of
+// kUnitEdges consecutive positions. A unit walks the targets its positions
+// belong to, in order. A target whose edges all lie in one unit is finished
+// there; a target that crosses a unit boundary (and a target with no edge)
+// is finished by the merge kernel, from partial softmax states that the
+// units write to two slots per unit: slot 2u for the unit's first target,
+// slot 2u + 1 for its last.
 // --------------------------------------------------------------------------
 
-// One unit of edge-kernel work: the edges [begin, end) (CSR positions) of
-// target t. slot < 0: the item covers every edge of t and writes t's result
-// directly; slot >= 0: t is split and this item writes partial softmax state
-// to partial slot `slot`, merged later.
-struct Item {
-    int32_t t, begin, end, slot;
-};
-
-// A split target: partial slots [first_slot, first_slot + n_chunks).
-struct Heavy {
-    int32_t t, first_slot, n_chunks, pad;
-};
-
-// Edges per item of a split target; targets with more edges are split.
-constexpr int kChunkEdges = 128;
+constexpr int kUnitEdges = 256;
 
 }  // namespace pmha
 
@@ -37,16 +31,15 @@ struct pmha_graph {
     int64_t L = 0, S = 0;
     int64_t nnz_given = 0, nnz = 0;   // nnz counts appended self-loops
     int64_t max_deg = 0;
-    int64_t n_items = 0;              // items per sample
-    int64_t n_parts = 0;              // partial slots per sample
-    int64_t n_heavy = 0;              // split targets
+    int64_t n_units = 0;              // units per sample, ceil(nnz / kUnitEdges)
+    int64_t n_merge = 0;              // targets finished by the merge kernel
     int device = 0;
     int32_t *row_ptr = nullptr;       // L + 1
     int32_t *col = nullptr;           // nnz, source per CSR position
     int32_t *perm = nullptr;          // nnz, given-order edge id per CSR position
     int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
-    pmha::Item *items = nullptr;      // n_items
-    pmha::Heavy *heavy = nullptr;     // n_heavy
+    int32_t *unit_first_t = nullptr;  // n_units, target of each unit's first position
+    int32_t *merge_t = nullptr;       // n_merge, targets to merge (crossing a unit boundary, or without edges)
     void *mem = nullptr;              // the single allocation behind the arrays above
 };
 
@@ -116,10 +109,10 @@ struct EdgeArgs {
     int64_t kv_ld;
     int64_t v_off;
     void *mixed;          // (B, L, E) output of the mix (light targets written directly)
-    float *part;          // (B, n_parts, 2H + E) partial state of split targets
+    float *part;          // (B, 2 n_units, 2H + E): per slot m[H], l[H], acc[E] of a crossing target
     float *ml;            // (B, L, H, 2): running max (log2 units) and sum per target/head
     float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
-    int64_t B, L, S, E, H, nnz, n_items, n_parts;
+    int64_t B, L, S, E, H, nnz;
     float score_scale;    // log2(e) / sqrt(d)
     bool with_values;     // false: scores and (m, l) only
 };
