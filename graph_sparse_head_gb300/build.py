@@ -20,7 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpmha.so")
 SOURCES = ["api.cu", "csr.cu", "gemm_simt.cu", "gemm_tc.cu", "edge_attn.cu", "edge_attn_f16.cu", "edge_attn_f32.cu",
            "noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "pmha_internal.h"), os.path.join(CSRC, "edge_stream.cuh"), os.path.join(ROOT, "include", "pmha.h")]
+HEADERS = [os.path.join(CSRC, "pmha_internal.h"), os.path.join(CSRC, "edge_stream.cuh"),
+           os.path.join(ROOT, "include", "pmha.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
                 "-Xptxas", "-warn-spills", "-I" + os.path.join(ROOT, "include")]

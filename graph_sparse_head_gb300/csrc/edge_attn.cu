@@ -20,20 +20,26 @@ __device__ __forceinline__ float ex2(float x)
 // One warp per (sample, merge-list target). Targets without edges get zeros
 // and (m, l) = (-inf, 0); others combine their partial states:
 // M = max m_i, L = sum l_i 2^(m_i - M), acc = sum acc_i 2^(m_i - M).
-template <typename T, bool WV>
+// Pass 1: lane h owns head h and walks the pieces in order. Pass 2: lane l
+// owns channels l, l + 32, ... (CH of them) and walks the pieces in order.
+// Both orders are fixed, so results are deterministic, and pass 1 is the
+// same code with and without values.
+template <typename T, bool WV, int CH>
 __global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge_t, long long n_merge,
                                                const int32_t *__restrict__ row_ptr, const float *__restrict__ part,
                                                long long n_units, int B, int L, int E, int H, int d, void *mixed,
                                                float *ml)
 {
-    const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    __shared__ float sm_m[8][32], sm_l[8][32];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long long gw = (long long)blockIdx.x * 8 + wib;
     if (gw >= (long long)B * n_merge) return;
     const int b = (int)(gw / n_merge);
     const int t = merge_t[gw - (long long)b * n_merge];
     const int beg = row_ptr[t], end = row_ptr[t + 1];
     const int stride = 2 * H + E;
     T *mrow = WV ? (T *)mixed + ((long long)b * L + t) * E : nullptr;
+    float *mlrow = ml ? ml + ((long long)b * L + t) * H * 2 : nullptr;
     if (beg == end) {
         if constexpr (WV) {
             for (int c = lane; c < E; c += 32) {
@@ -41,49 +47,65 @@ __global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge
                 else reinterpret_cast<float *>(mrow)[c] = 0.f;
             }
         }
-        if (ml)
+        if (mlrow)
             for (int h = lane; h < H; h += 32) {
-                ml[(((long long)b * L + t) * H + h) * 2] = -INFINITY;
-                ml[(((long long)b * L + t) * H + h) * 2 + 1] = 0.f;
+                mlrow[2 * h] = -INFINITY;
+                mlrow[2 * h + 1] = 0.f;
             }
         return;
     }
     const int u0 = beg / kUnitEdges, u1 = (end - 1) / kUnitEdges;
     const int n_pieces = u1 - u0 + 1;
     // piece i lives in unit u0 + i: slot 2u for the unit's first target, else 2u + 1
+    const float *base = part + (long long)b * 2 * n_units * stride;
     auto piece = [&](int i) -> const float * {
-        const int uu = u0 + i;
-        const int slot_id = 2 * uu + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
-        return part + ((long long)b * 2 * n_units + slot_id) * stride;
+        const int slot_id = 2 * (u0 + i) + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
+        return base + (long long)slot_id * stride;
     };
-    for (int h = 0; h < H; ++h) {
-        // over pieces, lane-parallel, with a fixed reduction order
-        float mx = -INFINITY;
-        for (int i = lane; i < n_pieces; i += 32) mx = fmaxf(mx, piece(i)[h]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float sum = 0.f;
-        for (int i = lane; i < n_pieces; i += 32) {
+    if (lane < H) {
+        float mh = -INFINITY;
+        for (int i = 0; i < n_pieces; ++i) mh = fmaxf(mh, piece(i)[lane]);
+        float lh = 0.f;
+        for (int i = 0; i < n_pieces; ++i) {
             const float *p = piece(i);
-            sum = __fadd_rn(sum, __fmul_rn(p[H + h], ex2(__fsub_rn(p[h], mx))));
+            lh = __fadd_rn(lh, __fmul_rn(p[H + lane], ex2(__fsub_rn(p[lane], mh))));
+        }
+        sm_m[wib][lane] = mh;
+        sm_l[wib][lane] = lh;
+        if (mlrow) {
+            mlrow[2 * lane] = mh;
+            mlrow[2 * lane + 1] = lh;
+        }
+    }
+    __syncwarp();
+    if constexpr (WV) {
+        float acc[CH];
+        int hd[CH];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            acc[k] = 0.f;
+            const int ch = lane + 32 * k;
+            hd[k] = ch < E ? ch / d : 0;
+        }
+        for (int i = 0; i < n_pieces; ++i) {
+            const float *p = piece(i);
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const int ch = lane + 32 * k;
+                if (ch < E) {
+                    const float w = ex2(__fsub_rn(p[hd[k]], sm_m[wib][hd[k]]));
+                    acc[k] = __fmaf_rn(p[2 * H + ch], w, acc[k]);
+                }
+            }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
-        if (ml && lane == 0) {
-            ml[(((long long)b * L + t) * H + h) * 2] = mx;
-            ml[(((long long)b * L + t) * H + h) * 2 + 1] = sum;
-        }
-        if constexpr (WV) {
-            const float inv = sum > 0.f ? __frcp_rn(sum) : 0.f;
-            for (int c = h * d + lane; c < (h + 1) * d; c += 32) {
-                float acc = 0.f;
-                for (int i = 0; i < n_pieces; ++i) {
-                    const float *p = piece(i);
-                    acc = __fmaf_rn(p[2 * H + c], ex2(__fsub_rn(p[h], mx)), acc);
-                }
-                const float v = __fmul_rn(acc, inv);
-                if constexpr (sizeof(T) == 2) reinterpret_cast<__half *>(mrow)[c] = __float2half_rn(v);
-                else reinterpret_cast<float *>(mrow)[c] = v;
+        for (int k = 0; k < CH; ++k) {
+            const int ch = lane + 32 * k;
+            if (ch < E) {
+                const float lh = sm_l[wib][hd[k]];
+                const float v = __fmul_rn(acc[k], lh > 0.f ? __frcp_rn(lh) : 0.f);
+                if constexpr (sizeof(T) == 2) reinterpret_cast<__half *>(mrow)[ch] = __float2half_rn(v);
+                else reinterpret_cast<float *>(mrow)[ch] = v;
             }
         }
     }
@@ -180,27 +202,47 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     return PMHA_OK;
 }
 
+namespace {
+template <typename T, bool WV, int CH>
+void launch_merge(const pmha_graph *g, const EdgeArgs &a, unsigned blocks, cudaStream_t s)
+{
+    k_merge<T, WV, CH><<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, a.part, g->n_units, (int)a.B,
+                                              (int)g->L, (int)a.E, (int)a.H, (int)(a.E / a.H), a.mixed, a.ml);
+}
+template <typename T, bool WV>
+bool launch_merge_ch(int E, const pmha_graph *g, const EdgeArgs &a, unsigned blocks, cudaStream_t s)
+{
+    const int ch = (E + 31) / 32;
+    if (ch <= 1) launch_merge<T, WV, 1>(g, a, blocks, s);
+    else if (ch <= 2) launch_merge<T, WV, 2>(g, a, blocks, s);
+    else if (ch <= 4) launch_merge<T, WV, 4>(g, a, blocks, s);
+    else if (ch <= 8) launch_merge<T, WV, 8>(g, a, blocks, s);
+    else if (ch <= 16) launch_merge<T, WV, 16>(g, a, blocks, s);
+    else return false;
+    return true;
+}
+}  // namespace
+
 pmha_status split_merge(TcType dt, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s)
 {
     if (g->n_merge == 0) return PMHA_OK;
     const long long warps = a.B * g->n_merge;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
-    const int d = (int)(a.E / a.H);
     StageTimer timer("split_merge", s);
-    if (dt == TcType::F16) {
-        if (a.with_values)
-            k_merge<__half, true><<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, a.part, g->n_units,
-                                                        (int)a.B, (int)g->L, (int)a.E, (int)a.H, d, a.mixed, a.ml);
-        else
-            k_merge<__half, false><<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, a.part, g->n_units,
-                                                         (int)a.B, (int)g->L, (int)a.E, (int)a.H, d, a.mixed, a.ml);
-    } else {
-        if (a.with_values)
-            k_merge<float, true><<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, a.part, g->n_units,
-                                                       (int)a.B, (int)g->L, (int)a.E, (int)a.H, d, a.mixed, a.ml);
-        else
-            k_merge<float, false><<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, a.part, g->n_units,
-                                                        (int)a.B, (int)g->L, (int)a.E, (int)a.H, d, a.mixed, a.ml);
+    if (a.H > 32) {
+        set_error("split_merge: at most 32 heads");
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    bool ok;
+    if (dt == TcType::F16)
+        ok = a.with_values ? launch_merge_ch<__half, true>((int)a.E, g, a, blocks, s)
+                           : launch_merge_ch<__half, false>((int)a.E, g, a, blocks, s);
+    else
+        ok = a.with_values ? launch_merge_ch<float, true>((int)a.E, g, a, blocks, s)
+                           : launch_merge_ch<float, false>((int)a.E, g, a, blocks, s);
+    if (!ok) {
+        set_error("split_merge: embed_dim %lld is wider than 512", (long long)a.E);
+        return PMHA_ERR_UNSUPPORTED;
     }
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());

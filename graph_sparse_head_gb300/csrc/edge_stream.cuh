@@ -36,10 +36,10 @@ namespace pmha {
 namespace stream {
 
 #ifndef PMHA_STREAM_DEPTH
-#define PMHA_STREAM_DEPTH 6
+#define PMHA_STREAM_DEPTH 4
 #endif
 #ifndef PMHA_STREAM_WARPS
-#define PMHA_STREAM_WARPS 4
+#define PMHA_STREAM_WARPS 2
 #endif
 constexpr int kWarps = PMHA_STREAM_WARPS;  // warps per block
 constexpr int kDepth = PMHA_STREAM_DEPTH;  // edges in flight per slot (even: two per step)

@@ -12,11 +12,13 @@
 //
 // Persistent kernel, one CTA per SM, 6 warps:
 //   warp 0    TMA producer: X tile 128 x 64 and W tile 128 x 64 per stage,
-//             128-byte swizzle, into a 6-stage shared-memory ring
+//             128-byte swizzle, into a 4-stage shared-memory ring
 //   warp 1    allocates 256 TMEM columns (two 128 x 128 fp32 accumulators)
 //             and issues tcgen05.mma (M=128, N=128, K=16) from one thread
-//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time, + bias, -> bf16,
-//             16-byte stores; warp w reads TMEM lanes 32*(w%4) .. +31
+//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM
+//             lanes 32*(w%4) .. +31), + bias, rounded to the output type,
+//             written to a 128-byte-swizzled shared tile that one thread
+//             stores with TMA (two tiles in flight)
 // Tiles are visited m-major with the N tiles of one row block adjacent, so
 // CTAs that share an X tile run together and the re-reads hit L2.
 //
@@ -36,14 +38,16 @@ namespace pmha {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kTileABytes = BM * BK * 2;
 constexpr int kTileBBytes = BN * BK * 2;
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 2 * BN;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kOutBoxBytes = BM * 128;             // 128 rows x 64 16-bit columns, 128-byte swizzle
+constexpr int kOutTileBytes = 2 * kOutBoxBytes;     // one 128 x 128 output tile
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kOutTileBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B of one 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), both
@@ -178,6 +182,34 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// barrier 1 over the 128 epilogue threads
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// same barrier, returning whether any of the 128 threads passed `pred`
+__device__ __forceinline__ bool epi_sync_or(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -201,12 +233,13 @@ template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(kThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
           const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
-          TcArgs a)
+          const __grid_constant__ CUtensorMap tm_y, TcArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *tiles = smem;
-    uint64_t *bars = (uint64_t *)(smem + kStages * kStageBytes);
+    uint8_t *staging = smem + kStages * kStageBytes;  // two output tiles
+    uint64_t *bars = (uint64_t *)(staging + 2 * kOutTileBytes);
     uint64_t *full = bars;                    // [kStages]
     uint64_t *empty = bars + kStages;         // [kStages]
     uint64_t *acc_full = bars + 2 * kStages;  // [2]
@@ -321,50 +354,71 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             mbar_wait(smem_u32(mma_done), 0, (volatile int *)&dummy, a.err);
         }
     } else {
-        // ---------------- epilogue, 128 threads
+        // ---------------- epilogue, 128 threads: TMEM -> registers (+ bias, rounding)
+        // -> swizzled shared tile -> TMA tensor store, double-buffered
         const int quarter = warp & 3;
+        const int et = threadIdx.x - 64;  // 0..127
+        const int r = quarter * 32 + lane;  // tile row of this thread
         int acc = 0;
         uint32_t acc_phase = 0;
+        int buf = 0;
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-            if (!mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err)) break;
+            const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err);
+            if (et == 0) bulk_wait_read1();  // the store that last read this buffer is done
+            if (epi_sync_or(!ok)) break;     // one decision for all 128 threads
             tc_fence_after();
             const int m_blk = tile / n_tiles_n, n_blk = tile % n_tiles_n;
             const int n_glob = n_blk * BN;
             const int seg = n_glob / a.E;
             const int n_loc = n_glob - seg * a.E;
             const __nv_bfloat16 *bias = a.bias[seg];
-            const int row = m_blk * BM + quarter * 32 + lane;
-            TOut *orow = (TOut *)a.out + (long long)row * a.ldy + n_glob;
+            const bool live = m_blk * BM + r < a.M;
+            uint8_t *sb = staging + buf * kOutTileBytes;
             bool range_bad = false;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
-                if (row < a.M) {
-                    uint32_t packed[16];
+                uint32_t v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), v);
+                uint32_t packed[16];
+                bool bad = false;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float v0 = __uint_as_float(r[2 * j]), v1 = __uint_as_float(r[2 * j + 1]);
-                        if (bias) {
-                            v0 = __fadd_rn(v0, __bfloat162float(bias[n_loc + c * 32 + 2 * j]));
-                            v1 = __fadd_rn(v1, __bfloat162float(bias[n_loc + c * 32 + 2 * j + 1]));
-                        }
-                        packed[j] = pack2<TOut>(v0, v1, range_bad);
+                for (int j = 0; j < 16; ++j) {
+                    float v0 = __uint_as_float(v[2 * j]), v1 = __uint_as_float(v[2 * j + 1]);
+                    if (bias) {
+                        v0 = __fadd_rn(v0, __bfloat162float(bias[n_loc + c * 32 + 2 * j]));
+                        v1 = __fadd_rn(v1, __bfloat162float(bias[n_loc + c * 32 + 2 * j + 1]));
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    packed[j] = pack2<TOut>(v0, v1, bad);
+                }
+                range_bad |= bad && live;
+                // 16-byte unit u of the 128-byte row of box c / 2 sits at u ^ (r % 8)
+                uint8_t *rowp = sb + (c >> 1) * kOutBoxBytes + r * 128;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) {
+                    const int u = (c & 1) * 4 + q;
+                    *reinterpret_cast<uint4 *>(rowp + ((u ^ (r & 7)) << 4)) =
+                        make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 }
             }
             if (range_bad) atomicOr(a.err, kErrRangeBit);
+            // the accumulator has been read: hand it back to the MMA warp
             tc_fence_before();
             mbar_arrive(smem_u32(&acc_empty[acc]));
+            // staged tile -> global (rows past M are clipped by the tensor map)
+            fence_async_shared();
+            epi_sync();
+            if (et == 0) {
+                tma_store_2d(&tm_y, smem_u32(sb), n_glob, m_blk * BM);
+                tma_store_2d(&tm_y, smem_u32(sb + kOutBoxBytes), n_glob + 64, m_blk * BM);
+                bulk_commit();
+            }
+            buf ^= 1;
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
         }
+        if (et == 0) bulk_wait_all();  // the CTA's shared memory must outlive its stores
     }
 
     __syncthreads();
@@ -405,13 +459,14 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D 16-bit row-major tensor (rows x cols, row stride cols), box 128 rows x 64 columns.
-bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, bool bf16)
+// 2-D 16-bit row-major tensor (rows x cols, row pitch `pitch` elements),
+// box 128 rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, bool bf16, int64_t pitch = 0)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)(pitch ? pitch : cols) * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
@@ -452,6 +507,11 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
             return PMHA_ERR_CUDA;
         }
     }
+    CUtensorMap my;
+    if (!make_map(&my, Y, M, E * seg.n_seg, out == TcType::BF16, ldy)) {
+        set_error("gemm_tc: cuTensorMapEncodeTiled failed for Y (pointer %p, pitch %lld)", Y, (long long)ldy);
+        return PMHA_ERR_CUDA;
+    }
     TcArgs a;
     a.M = (int)M;
     a.N = (int)(E * seg.n_seg);
@@ -463,7 +523,7 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     a.err = device_error_word();
     if (!a.err) return PMHA_ERR_CUDA;
 
-    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
     if (in_bf16 && out == TcType::F16) kern = k_gemm_tc<__nv_bfloat16, __half>;
     else if (in_bf16) kern = k_gemm_tc<__nv_bfloat16, __nv_bfloat16>;
     else if (out == TcType::BF16) kern = k_gemm_tc<__half, __nv_bfloat16>;
@@ -482,7 +542,7 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     const int n_tiles = (int)(((M + BM - 1) / BM) * (a.N / BN));
     const int grid = std::min(n_tiles, num_sms());
     StageTimer timer(stage, stream);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw[0], mw[1], mw[2], a);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw[0], mw[1], mw[2], my, a);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;
