@@ -87,7 +87,7 @@ def source_digest(paths) -> str:
 
 
 KERNEL_SOURCES = {
-    "edge_attn": ["graph_sparse_head_gb300/csrc/edge_attn.cu"],
+    "edge_attn": ["graph_sparse_head_gb300/csrc/edge_stream.cuh", "graph_sparse_head_gb300/csrc/edge_attn_f16.cu"],
     "proj_qkv": ["graph_sparse_head_gb300/csrc/gemm_tc.cu"],
     "out_proj": ["graph_sparse_head_gb300/csrc/gemm_tc.cu"],
 }
@@ -184,12 +184,14 @@ def make_rank_inputs(rank: int, batch: int):
     return xq, params
 
 
-def max_over_ranks(x: float, world: int, device) -> float:
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's value (the job finishes when every rank has)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
+    on_cpu = dist.get_backend() == "gloo" or device is None
+    t = torch.tensor([x], dtype=torch.float64, device="cpu" if on_cpu else device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

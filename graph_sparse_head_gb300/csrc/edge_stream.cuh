@@ -6,11 +6,12 @@
 // kUnitEdges consecutive positions (edges of consecutive targets, each
 // target's edges ordered by source). A unit is walked by one "slot": the LPE
 // lanes that own one row of channels, a lane owning CPL consecutive channels
-// (one whole head when the head has at most 16 channels). A warp runs
-// 32 / LPE units side by side. Every slot does the same gather work whatever
-// the in-degrees, and no target needs atomics: a target inside one unit is
-// finished there, a target crossing a unit boundary leaves partial softmax
-// states that the merge kernel combines.
+// (one whole head when the head has at most 16 channels). A warp runs the
+// same unit for 32 / LPE samples side by side, so its slots never diverge.
+// Every slot does the same gather work whatever the in-degrees, and no
+// target needs atomics: a target inside one unit is finished there, a target
+// crossing a unit boundary leaves partial softmax states that the merge
+// kernel combines.
 //
 // Per edge, a lane gathers its chunks of the source's k and v rows through
 // cp.async into a per-lane ring of shared-memory stages, kDepth edges ahead
@@ -223,10 +224,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int slot = lane / LPE, grp = lane % LPE;
     const unsigned smask = LPE == 32 ? 0xffffffffu : (((1u << LPE) - 1u) << (slot * LPE));
-    const long long gu = ((long long)blockIdx.x * kWarps + warp) * P + slot;
-    if (gu >= (long long)a.B * a.n_units) return;  // the whole slot leaves together
-    const int b = (int)(gu / a.n_units);
-    const int u = (int)(gu - (long long)b * a.n_units);
+    // the P slots of a warp walk the same unit for P consecutive samples: the
+    // graph is shared by all samples, so their control flow is identical
+    const long long gw = (long long)blockIdx.x * kWarps + warp;
+    const long long groups = (a.B + P - 1) / P;
+    if (gw >= groups * a.n_units) return;
+    const int u = (int)(gw % a.n_units);
+    const int b = (int)(gw / a.n_units) * P + slot;
+    if (b >= a.B) return;  // the whole slot leaves together
     const int e0 = u * kUnitEdges;
     const int n = (int)min((long long)kUnitEdges, a.nnz - e0);
     const int e1 = e0 + n;
@@ -470,8 +475,9 @@ pmha_status launch(const Args &k, long long slots, cudaStream_t s)
 {
     constexpr int smem = smem_bytes<T, CPL, WV>();
     constexpr int P = 32 / LPE;
-    const long long warps = (slots + P - 1) / P;
+    const long long warps = (k.B + P - 1) / P * k.n_units;
     const long long blocks = (warps + kWarps - 1) / kWarps;
+    (void)slots;
     auto kern = k.scores ? k_edge_stream<T, CPL, LPE, WV, true> : k_edge_stream<T, CPL, LPE, WV, false>;
     if constexpr (smem > 48 * 1024) {
         PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
