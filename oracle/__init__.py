@@ -63,6 +63,11 @@ def _load():
         lib.oracle_attend.restype = ctypes.c_int
         lib.oracle_forward.argtypes = [_i64] * 5 + [_D] * 11 + [_i64, _I64, _I64, _D, _D]
         lib.oracle_forward.restype = ctypes.c_int
+        _U8 = ctypes.POINTER(ctypes.c_ubyte)
+        lib.oracle_forward_masked.argtypes = [_i64] * 5 + [_D] * 11 + [_i64, _I64, _I64, _U8, _D, _D]
+        lib.oracle_forward_masked.restype = ctypes.c_int
+        lib.oracle_attend_masked.argtypes = [_i64, _i64, _D, _i64, _D, _D, _U8, _D, _D]
+        lib.oracle_attend_masked.restype = ctypes.c_int
         lib.oracle_average_heads.argtypes = [_i64, _i64, _D, _D]
         lib.oracle_average_heads.restype = None
         lib.oracle_num_threads.argtypes = []
@@ -138,24 +143,35 @@ def linear(x, w, b=None) -> np.ndarray:
     return y
 
 
-def attend(q, k_rows, v_rows, num_heads: int):
-    """Per-target attention: returns (mixed (E,), weights (n_edges, H))."""
+def _mask(m):
+    return None if m is None else np.ascontiguousarray(np.asarray(m).astype(np.uint8))
+
+
+def _mp(m):
+    return None if m is None else m.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
+
+
+def attend(q, k_rows, v_rows, num_heads: int, masked=None):
+    """Per-target attention: returns (mixed (E,), weights (n_edges, H)).
+    masked (n_edges,) bool drops those edges (key_padding_mask)."""
     q, k_rows, v_rows = _f64(q), _f64(k_rows), _f64(v_rows)
     E = q.shape[-1]
     n = k_rows.shape[0]
     mixed = np.empty(E, np.float64)
     w = np.empty((n, num_heads), np.float64)
-    st = _load().oracle_attend(E, num_heads, _dp(q), n, _dp(k_rows), _dp(v_rows), _dp(mixed), _dp(w))
+    mk = _mask(masked)
+    st = _load().oracle_attend_masked(E, num_heads, _dp(q), n, _dp(k_rows), _dp(v_rows), _mp(mk), _dp(mixed),
+                                      _dp(w))
     if st != OK:
         raise ValueError(f"oracle_attend status {st}")
     return mixed, w
 
 
 def forward(query, key, value, params: dict, source_index, target_index, num_heads: int,
-            need_weights: bool = True):
+            need_weights: bool = True, key_padding_mask=None):
     """Full forward. query (B, L, E), key/value (B, S, E); params holds wq, wk, wv, wo
-    (E, E) and bq, bk, bv, bo (E,) or None. Returns (output (B, L, E),
-    weights (B, nnz, H) or None)."""
+    (E, E) and bq, bk, bv, bo (E,) or None; key_padding_mask (B, S) bool or None.
+    Returns (output (B, L, E), weights (B, nnz, H) or None)."""
     q, k, v = _f64(query), _f64(key), _f64(value)
     B, L, E = q.shape
     S = k.shape[1]
@@ -164,17 +180,20 @@ def forward(query, key, value, params: dict, source_index, target_index, num_hea
          for n in ("wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo")}
     out = np.empty((B, L, E), np.float64)
     w = np.empty((B, s.size, num_heads), np.float64) if need_weights else None
-    st = _load().oracle_forward(B, L, S, E, num_heads, _dp(q), _dp(k), _dp(v),
-                                _dp(p["wq"]), _dp(p["bq"]), _dp(p["wk"]), _dp(p["bk"]),
-                                _dp(p["wv"]), _dp(p["bv"]), _dp(p["wo"]), _dp(p["bo"]),
-                                s.size, _ip(s), _ip(t), _dp(out), _dp(w))
+    mk = _mask(key_padding_mask)
+    if mk is not None and mk.shape != (B, S):
+        raise ValueError(f"key_padding_mask must be ({B}, {S})")
+    st = _load().oracle_forward_masked(B, L, S, E, num_heads, _dp(q), _dp(k), _dp(v),
+                                       _dp(p["wq"]), _dp(p["bq"]), _dp(p["wk"]), _dp(p["bk"]),
+                                       _dp(p["wv"]), _dp(p["bv"]), _dp(p["wo"]), _dp(p["bo"]),
+                                       s.size, _ip(s), _ip(t), _mp(mk), _dp(out), _dp(w))
     if st != OK:
         raise ValueError(f"oracle_forward status {st}")
     return out, w
 
 
 def forward_rows(query, key, value, params: dict, source_index, target_index, num_heads: int,
-                 rows):
+                 rows, key_padding_mask=None):
     """Output rows and edge weights of selected (sample, target) pairs only.
 
     rows: iterable of (b, t). Projects only the tokens those rows read, in the
@@ -189,7 +208,8 @@ def forward_rows(query, key, value, params: dict, source_index, target_index, nu
         q_t = linear(np.asarray(query[b, t]), params["wq"], params.get("bq"))
         k_r = linear(np.asarray(key[b][srcs]), params["wk"], params.get("bk")).reshape(len(srcs), -1)
         v_r = linear(np.asarray(value[b][srcs]), params["wv"], params.get("bv")).reshape(len(srcs), -1)
-        mixed, w = attend(q_t, k_r, v_r, num_heads)
+        masked = None if key_padding_mask is None else np.asarray(key_padding_mask)[b][srcs]
+        mixed, w = attend(q_t, k_r, v_r, num_heads, masked)
         out = linear(mixed, params["wo"], params.get("bo"))
         res.append((out, e_ids, w))
     return res

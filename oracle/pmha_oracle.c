@@ -165,6 +165,9 @@ void oracle_linear(int64_t rows, int64_t in_dim, int64_t out_dim, const double *
 /* ------------------------------------------------------------------------ */
 /* Attention of one target over its live keys, all heads.                    */
 /* kpnn2 PackedMultiheadAttention, Notes steps 2-4:                          */
+/* (forward() parameter key_padding_mask: a masked key's edges take no part  */
+/*  in the softmax; masked[j] != 0 marks edge j of this target as dropped,   */
+/*  masked may be NULL)                                                      */
 /*   score[e] = dot(q[t], k[s]) / sqrt(d)       per head, d = E / H channels */
 /*   weight   = softmax of the scores over the edges into t only             */
 /*   mixed[t] = sum_e weight[e] * v[s]                                       */
@@ -177,14 +180,20 @@ void oracle_linear(int64_t rows, int64_t in_dim, int64_t out_dim, const double *
 /* function and keeps exp() finite.                                          */
 /* ------------------------------------------------------------------------ */
 
-int oracle_attend(int64_t embed_dim, int64_t num_heads, const double *q, int64_t n_edges,
-                  const double *k_rows, const double *v_rows, double *mixed, double *weight)
+int oracle_attend_masked(int64_t embed_dim, int64_t num_heads, const double *q, int64_t n_edges,
+                         const double *k_rows, const double *v_rows, const unsigned char *masked,
+                         double *mixed, double *weight)
 {
     if (num_heads < 1 || embed_dim % num_heads != 0) return ORACLE_ERR_ARG;
     const int64_t E = embed_dim, H = num_heads, d = E / H;
     const double inv_sqrt_d = 1.0 / sqrt((double)d);
     for (int64_t c = 0; c < E; ++c) mixed[c] = 0.0;
-    if (n_edges == 0) return ORACLE_OK;
+    if (weight)
+        for (int64_t j = 0; j < n_edges * H; ++j) weight[j] = 0.0;
+    int64_t live = 0;
+    for (int64_t j = 0; j < n_edges; ++j)
+        if (!masked || !masked[j]) ++live;
+    if (live == 0) return ORACLE_OK; /* no live key: mixes to zeros, weights 0 */
     double *score = (double *)malloc((size_t)n_edges * sizeof(double));
     if (!score) return ORACLE_ERR_NOMEM;
     for (int64_t h = 0; h < H; ++h) {
@@ -194,14 +203,16 @@ int oracle_attend(int64_t embed_dim, int64_t num_heads, const double *q, int64_t
             for (int64_t c = 0; c < d; ++c) dot += q[h * d + c] * k_rows[j * E + h * d + c];
             score[j] = dot * inv_sqrt_d;
         }
-        /* step 3: softmax over the edges into this target */
-        double m = score[0];
-        for (int64_t j = 1; j < n_edges; ++j)
-            if (score[j] > m) m = score[j];
+        /* step 3: softmax over the live edges into this target */
+        double m = -INFINITY;
+        for (int64_t j = 0; j < n_edges; ++j)
+            if ((!masked || !masked[j]) && score[j] > m) m = score[j];
         double denom = 0.0;
-        for (int64_t j = 0; j < n_edges; ++j) denom += exp(score[j] - m);
+        for (int64_t j = 0; j < n_edges; ++j)
+            if (!masked || !masked[j]) denom += exp(score[j] - m);
         /* step 4: weighted sum of the value rows */
         for (int64_t j = 0; j < n_edges; ++j) {
+            if (masked && masked[j]) continue;
             double w = exp(score[j] - m) / denom;
             if (weight) weight[j * H + h] = w;
             for (int64_t c = 0; c < d; ++c) mixed[h * d + c] += w * v_rows[j * E + h * d + c];
@@ -211,9 +222,17 @@ int oracle_attend(int64_t embed_dim, int64_t num_heads, const double *q, int64_t
     return ORACLE_OK;
 }
 
+int oracle_attend(int64_t embed_dim, int64_t num_heads, const double *q, int64_t n_edges,
+                  const double *k_rows, const double *v_rows, double *mixed, double *weight)
+{
+    return oracle_attend_masked(embed_dim, num_heads, q, n_edges, k_rows, v_rows, NULL, mixed, weight);
+}
+
 /* ------------------------------------------------------------------------ */
 /* One full forward pass, batch-first.                                       */
-/* kpnn2 PackedMultiheadAttention, Notes steps 1-5 and forward() Returns:    */
+/* kpnn2 PackedMultiheadAttention, Notes steps 1-5 and forward() Returns;    */
+/* key_padding_mask (nullable) is (B, S) bytes, nonzero = key ignored in     */
+/* that sample (forward() parameter key_padding_mask).                       */
 /*   query (B, L, E), key and value (B, S, E); output (B, L, E);             */
 /*   weight (B, nnz, H), one entry per live edge in the order of the index   */
 /*   arrays (nullable).                                                      */
@@ -223,13 +242,13 @@ int oracle_attend(int64_t embed_dim, int64_t num_heads, const double *q, int64_t
 /* in their given order; no CSR from elsewhere is used.                      */
 /* ------------------------------------------------------------------------ */
 
-int oracle_forward(int64_t batch, int64_t query_features, int64_t key_features,
-                   int64_t embed_dim, int64_t num_heads,
-                   const double *query, const double *key, const double *value,
-                   const double *wq, const double *bq, const double *wk, const double *bk,
-                   const double *wv, const double *bv, const double *wo, const double *bo,
-                   int64_t nnz, const int64_t *source_index, const int64_t *target_index,
-                   double *output, double *weight)
+int oracle_forward_masked(int64_t batch, int64_t query_features, int64_t key_features,
+                          int64_t embed_dim, int64_t num_heads,
+                          const double *query, const double *key, const double *value,
+                          const double *wq, const double *bq, const double *wk, const double *bk,
+                          const double *wv, const double *bv, const double *wo, const double *bo,
+                          int64_t nnz, const int64_t *source_index, const int64_t *target_index,
+                          const unsigned char *key_padding_mask, double *output, double *weight)
 {
     const int64_t B = batch, L = query_features, S = key_features, E = embed_dim, H = num_heads;
     if (B < 1 || L < 1 || S < 1 || E < 1 || H < 1 || E % H != 0) return ORACLE_ERR_ARG;
@@ -265,7 +284,8 @@ int oracle_forward(int64_t batch, int64_t query_features, int64_t key_features,
         double *kr = (double *)malloc((size_t)(max_deg > 0 ? max_deg : 1) * E * sizeof(double));
         double *vr = (double *)malloc((size_t)(max_deg > 0 ? max_deg : 1) * E * sizeof(double));
         double *wr = (double *)malloc((size_t)(max_deg > 0 ? max_deg : 1) * H * sizeof(double));
-        int local_status = (kr && vr && wr) ? ORACLE_OK : ORACLE_ERR_NOMEM;
+        unsigned char *mk = (unsigned char *)malloc((size_t)(max_deg > 0 ? max_deg : 1));
+        int local_status = (kr && vr && wr && mk) ? ORACLE_OK : ORACLE_ERR_NOMEM;
 #pragma omp for schedule(dynamic, 16)
         for (int64_t bt = 0; bt < B * L; ++bt) {
             if (local_status != ORACLE_OK) continue;
@@ -275,8 +295,9 @@ int oracle_forward(int64_t batch, int64_t query_features, int64_t key_features,
                 const int64_t s = source_index[edges_of[first[t] + j]];
                 memcpy(kr + j * E, k + (b * S + s) * E, (size_t)E * sizeof(double));
                 memcpy(vr + j * E, v + (b * S + s) * E, (size_t)E * sizeof(double));
+                mk[j] = key_padding_mask ? key_padding_mask[b * S + s] : 0;
             }
-            oracle_attend(E, H, q + (b * L + t) * E, deg, kr, vr, mixed + (b * L + t) * E, wr);
+            oracle_attend_masked(E, H, q + (b * L + t) * E, deg, kr, vr, mk, mixed + (b * L + t) * E, wr);
             if (weight)
                 for (int64_t j = 0; j < deg; ++j) {
                     const int64_t e = edges_of[first[t] + j];
@@ -287,7 +308,7 @@ int oracle_forward(int64_t batch, int64_t query_features, int64_t key_features,
 #pragma omp atomic write
             status = local_status;
         }
-        free(kr); free(vr); free(wr);
+        free(kr); free(vr); free(wr); free(mk);
     }
     if (status != ORACLE_OK) goto done;
 
@@ -297,6 +318,19 @@ int oracle_forward(int64_t batch, int64_t query_features, int64_t key_features,
 done:
     free(q); free(k); free(v); free(mixed); free(first); free(fill); free(edges_of);
     return status;
+}
+
+int oracle_forward(int64_t batch, int64_t query_features, int64_t key_features,
+                   int64_t embed_dim, int64_t num_heads,
+                   const double *query, const double *key, const double *value,
+                   const double *wq, const double *bq, const double *wk, const double *bk,
+                   const double *wv, const double *bv, const double *wo, const double *bo,
+                   int64_t nnz, const int64_t *source_index, const int64_t *target_index,
+                   double *output, double *weight)
+{
+    return oracle_forward_masked(batch, query_features, key_features, embed_dim, num_heads, query, key, value,
+                                 wq, bq, wk, bk, wv, bv, wo, bo, nnz, source_index, target_index, NULL,
+                                 output, weight);
 }
 
 /* Mean over heads of per-head weights: kpnn2 forward(), average_attn_weights

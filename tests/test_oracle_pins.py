@@ -292,3 +292,43 @@ def test_thread_count_does_not_change_results():
     finally:
         oracle.set_num_threads(n0)
     assert np.array_equal(a, b) and np.array_equal(wa, wb)
+
+
+# ------------------------------------------------------------ key padding mask
+
+@pytest.mark.parametrize("E,H,n,B", [(16, 4, 6, 3), (24, 2, 9, 2)])
+def test_key_padding_mask_equals_torch_mha(E, H, n, B):
+    """kpnn2 forward(), key_padding_mask: True drops that key's edges from the
+    softmax; on the complete graph this is torch's key_padding_mask."""
+    rng = np.random.default_rng(E + n)
+    p = _params(rng, E)
+    x = rng.standard_normal((B, n, E))
+    src, tgt = synth.complete_graph(rng, n)
+    kpm = rng.random((B, n)) < 0.4
+    kpm[:, 0] = False  # every query keeps a live key
+    out, w = oracle.forward(x, x, x, p, src, tgt, H, key_padding_mask=kpm)
+    mha = _torch_mha(p, E, H)
+    with torch.no_grad():
+        ref, ref_w = mha(*(torch.from_numpy(x),) * 3, key_padding_mask=torch.from_numpy(kpm), need_weights=True,
+                         average_attn_weights=False)
+    assert np.abs(out - ref.numpy()).max() < 1e-12
+    assert np.abs(w - ref_w.numpy()[:, :, tgt, src].transpose(0, 2, 1)).max() < 1e-14
+    # masked keys carry weight 0, live ones sum to 1
+    assert np.all(w[kpm[:, src]] == 0.0)
+
+
+def test_key_padding_mask_drops_every_key_of_a_target():
+    """A query whose live keys are all masked mixes to zeros: output = bo."""
+    rng = np.random.default_rng(31)
+    E, H, n = 16, 2, 8
+    p = _params(rng, E)
+    x = rng.standard_normal((2, n, E))
+    src, tgt = synth.uniform_graph(rng, n, n, 30)
+    kpm = np.zeros((2, n), bool)
+    t0 = int(tgt[0])
+    kpm[1, src[tgt == t0]] = True  # sample 1: every source of t0 masked
+    out, w = oracle.forward(x, x, x, p, src, tgt, H, key_padding_mask=kpm)
+    assert np.array_equal(out[1, t0], p["bo"].astype(np.float64))
+    assert np.all(w[1, tgt == t0] == 0.0)
+    out0, _ = oracle.forward(x, x, x, p, src, tgt, H)
+    assert np.array_equal(out[0], out0[0])  # sample 0 has no masked key
