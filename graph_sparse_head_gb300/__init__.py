@@ -188,14 +188,29 @@ def _check_tokens(name, x, batch, seq, E, dtype, device):
         raise ValueError(f"{name} must be a contiguous {dtype} tensor on {device}")
 
 
+def _check_mask(mask, batch, S, on_device, device=None):
+    """key_padding_mask: None, or a contiguous (B, S) bool / uint8 tensor (nonzero = key dropped)."""
+    if mask is None:
+        return None
+    if not isinstance(mask, torch.Tensor) or tuple(mask.shape) != (batch, S) or \
+            mask.dtype not in (torch.bool, torch.uint8) or not mask.is_contiguous():
+        raise ValueError(f"key_padding_mask must be a contiguous ({batch}, {S}) bool or uint8 tensor")
+    if on_device and mask.device != device:
+        raise ValueError(f"key_padding_mask must live on {device}")
+    if not on_device and mask.is_cuda:
+        raise ValueError("key_padding_mask must be a host tensor here")
+    return _ptr(mask)
+
+
 def _weights_shape(graph, batch, H, wmode):
     return (batch, graph.nnz) if wmode == "avg" else (batch, graph.nnz, H)
 
 
 def pmha_forward(graph: Graph, params: Params, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
                  wmode: str = "none", out: torch.Tensor | None = None, weights: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None, stream=None):
-    """One forward pass on device tensors: query (B, L, E), key / value (B, S, E).
+                 workspace: torch.Tensor | None = None, stream=None, key_padding_mask: torch.Tensor | None = None):
+    """One forward pass on device tensors: query (B, L, E), key / value (B, S, E),
+    key_padding_mask (B, S) bool (True = key dropped) or None.
     Returns (output (B, L, E), weights or None)."""
     B = int(query.shape[0])
     E, H = params.embed_dim, int(params.num_heads)
@@ -203,6 +218,7 @@ def pmha_forward(graph: Graph, params: Params, query: torch.Tensor, key: torch.T
     _check_tokens("query", query, B, graph.query_features, E, params.dtype, dev)
     _check_tokens("key", key, B, graph.key_features, E, params.dtype, dev)
     _check_tokens("value", value, B, graph.key_features, E, params.dtype, dev)
+    mp = _check_mask(key_padding_mask, B, graph.key_features, True, dev)
     p = params.as_struct()
     lib = _lib.load()
     wm = WMODES[wmode]
@@ -215,7 +231,7 @@ def pmha_forward(graph: Graph, params: Params, query: torch.Tensor, key: torch.T
         _lib.check(_lib.PMHA_OK + 1, "pmha_forward_workspace_size")
     ws = _workspace(need, dev, workspace)
     with torch.cuda.device(dev):
-        st = lib.pmha_forward(graph.handle, ctypes.byref(p), _ptr(query), _ptr(key), _ptr(value), B, _ptr(out), wm,
+        st = lib.pmha_forward(graph.handle, ctypes.byref(p), _ptr(query), _ptr(key), _ptr(value), mp, B, _ptr(out), wm,
                               _ptr(weights) if wm != PMHA_WEIGHTS_NONE else None, _ptr(ws),
                               ws.numel() * ws.element_size(), _stream_ptr(stream))
     _lib.check(st, "pmha_forward")
@@ -224,7 +240,8 @@ def pmha_forward(graph: Graph, params: Params, query: torch.Tensor, key: torch.T
 
 def pmha_forward_host(graph: Graph, params: Params, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
                       out: torch.Tensor, wmode: str = "none", weights: torch.Tensor | None = None,
-                      workspace: torch.Tensor | None = None, stream=None, device=None):
+                      workspace: torch.Tensor | None = None, stream=None, device=None,
+                      key_padding_mask: torch.Tensor | None = None):
     """Forward pass on HOST tensors (pinned for asynchronous copies): the library
     copies the inputs in, runs the layer and copies out (and weights) back, all
     on the stream. Synchronize the stream before reading `out`."""
@@ -235,13 +252,15 @@ def pmha_forward_host(graph: Graph, params: Params, query: torch.Tensor, key: to
                       ("value", value, graph.key_features), ("out", out, graph.query_features)):
         if x.is_cuda or tuple(x.shape) != (B, seq, E) or x.dtype != params.dtype or not x.is_contiguous():
             raise ValueError(f"{n} must be a contiguous host tensor ({B}, {seq}, {E}) of {params.dtype}")
+    mp = _check_mask(key_padding_mask, B, graph.key_features, False)
     p = params.as_struct()
     lib = _lib.load()
     wm = WMODES[wmode]
     need = lib.pmha_forward_host_workspace_size(graph.handle, ctypes.byref(p), B, wm)
     ws = _workspace(need, dev, workspace)
     with torch.cuda.device(dev):
-        st = lib.pmha_forward_host(graph.handle, ctypes.byref(p), _ptr(query), _ptr(key), _ptr(value), B, _ptr(out),
+        st = lib.pmha_forward_host(graph.handle, ctypes.byref(p), _ptr(query), _ptr(key), _ptr(value), mp, B,
+                                   _ptr(out),
                                    wm, _ptr(weights) if wm != PMHA_WEIGHTS_NONE else None, _ptr(ws),
                                    ws.numel() * ws.element_size(), _stream_ptr(stream))
     _lib.check(st, "pmha_forward_host")
@@ -249,7 +268,8 @@ def pmha_forward_host(graph: Graph, params: Params, query: torch.Tensor, key: to
 
 
 def pmha_edge_weights(graph: Graph, params: Params, query: torch.Tensor, key: torch.Tensor, wmode: str = "avg",
-                      weights: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+                      weights: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None,
+                      key_padding_mask: torch.Tensor | None = None):
     """Per-edge softmax weights only (no value projection, mix or out_proj)."""
     B = int(query.shape[0])
     E, H = params.embed_dim, int(params.num_heads)
@@ -258,6 +278,7 @@ def pmha_edge_weights(graph: Graph, params: Params, query: torch.Tensor, key: to
     _check_tokens("key", key, B, graph.key_features, E, params.dtype, dev)
     if wmode not in ("avg", "per_head"):
         raise ValueError("wmode must be 'avg' or 'per_head'")
+    mp = _check_mask(key_padding_mask, B, graph.key_features, True, dev)
     p = params.as_struct()
     lib = _lib.load()
     wm = WMODES[wmode]
@@ -266,7 +287,7 @@ def pmha_edge_weights(graph: Graph, params: Params, query: torch.Tensor, key: to
     need = lib.pmha_edge_weights_workspace_size(graph.handle, ctypes.byref(p), B, wm)
     ws = _workspace(need, dev, workspace)
     with torch.cuda.device(dev):
-        st = lib.pmha_edge_weights(graph.handle, ctypes.byref(p), _ptr(query), _ptr(key), B, wm, _ptr(weights),
+        st = lib.pmha_edge_weights(graph.handle, ctypes.byref(p), _ptr(query), _ptr(key), mp, B, wm, _ptr(weights),
                                    _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
     _lib.check(st, "pmha_edge_weights")
     return weights
@@ -303,7 +324,8 @@ def pmha_launch_count() -> int:
 class PackedMultiheadAttention:
     """The layer as one object: a built graph plus parameters, called like
     kpnn2's PackedMultiheadAttention.forward on batch-first device tensors:
-    ``out, w = layer(query, key, value, need_weights=False, average_attn_weights=True)``.
+    ``out, w = layer(query, key, value, key_padding_mask=None, need_weights=False,
+    average_attn_weights=True)``.
     Reuses one workspace tensor across calls on the current stream."""
 
     def __init__(self, source_index, target_index, query_features: int, key_features: int, params: Params,
@@ -318,10 +340,12 @@ class PackedMultiheadAttention:
         self.nnz = self.graph.nnz
         self._ws = None
 
-    def __call__(self, query, key, value, need_weights: bool = False, average_attn_weights: bool = True):
+    def __call__(self, query, key, value, key_padding_mask=None, need_weights: bool = False,
+                 average_attn_weights: bool = True):
         wmode = "none" if not need_weights else ("avg" if average_attn_weights else "per_head")
         B = int(query.shape[0])
         need = pmha_forward_workspace_size(self.graph, self.params, B, wmode)
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(need, dtype=torch.uint8, device=query.device)
-        return pmha_forward(self.graph, self.params, query, key, value, wmode, workspace=self._ws)
+        return pmha_forward(self.graph, self.params, query, key, value, wmode, workspace=self._ws,
+                            key_padding_mask=key_padding_mask)

@@ -39,11 +39,11 @@ SIGNATURES = {
     "pmha_graph_destroy": (None, [_vp]),
     "pmha_forward_workspace_size": (_sz, [_vp, _P, _i64, ctypes.c_int]),
     "pmha_edge_weights_workspace_size": (_sz, [_vp, _P, _i64, ctypes.c_int]),
-    "pmha_forward": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _i64, _vp, ctypes.c_int, _vp, _vp, _sz, _vp]),
+    "pmha_forward": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _vp, _i64, _vp, ctypes.c_int, _vp, _vp, _sz, _vp]),
     "pmha_forward_host_workspace_size": (_sz, [_vp, _P, _i64, ctypes.c_int]),
-    "pmha_forward_host": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _i64, _vp, ctypes.c_int, _vp, _vp, _sz, _vp]),
-    "pmha_edge_weights": (ctypes.c_int, [_vp, _P, _vp, _vp, _i64, ctypes.c_int, _vp, _vp, _sz, _vp]),
-    "pmha_forward_noalloc": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
+    "pmha_forward_host": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _vp, _i64, _vp, ctypes.c_int, _vp, _vp, _sz, _vp]),
+    "pmha_edge_weights": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _i64, ctypes.c_int, _vp, _vp, _sz, _vp]),
+    "pmha_forward_noalloc": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _vp, _i64, _vp, ctypes.c_int, _vp, _vp]),
     "pmha_device_status": (ctypes.c_int, [_vp]),
     "pmha_last_error": (ctypes.c_char_p, []),
     "pmha_profile_enable": (ctypes.c_int, [ctypes.c_int]),

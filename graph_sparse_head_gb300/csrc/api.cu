@@ -242,7 +242,7 @@ GemmSegments segs(const void *w0, const void *b0, const void *w1 = nullptr, cons
 
 // Steps 1-4 (and the weights); with_values = false stops after the scores.
 pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
-                   const void *value, int64_t B, pmha_wmode wmode, float *weights, char *ws, const Layout &lay,
+                   const void *value, const uint8_t *kpm, int64_t B, pmha_wmode wmode, float *weights, char *ws, const Layout &lay,
                    bool with_values, cudaStream_t s, const void **mixed_out)
 {
     const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
@@ -297,6 +297,7 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.nnz = g->nnz;
     a.score_scale = (float)(1.4426950408889634 / sqrt((double)(E / H)));
     a.with_values = with_values;
+    a.kpm = kpm;
     if ((st = edge_attention(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
     if ((st = split_merge(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
     if (wmode != PMHA_WEIGHTS_NONE)
@@ -327,7 +328,7 @@ pmha_status check_wmode(pmha_wmode wmode, const float *weights, bool allow_none)
 }
 
 pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
-                           const void *value, int64_t B, void *output, pmha_wmode wmode, float *weights,
+                           const void *value, const uint8_t *kpm, int64_t B, void *output, pmha_wmode wmode, float *weights,
                            void *workspace, size_t ws_bytes, cudaStream_t s)
 {
     pmha_status st = check_params(g, p, B);
@@ -349,7 +350,7 @@ pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void
     }
     char *ws = (char *)workspace;
     const void *mixed = nullptr;
-    st = attend(g, p, query, key, value, B, wmode, weights, ws, lay, true, s, &mixed);
+    st = attend(g, p, query, key, value, kpm, B, wmode, weights, ws, lay, true, s, &mixed);
     if (st != PMHA_OK) return st;
     // step 5: out_proj over the joined heads, mixed (intermediate type) -> output (layer dtype)
     const int64_t E = p->embed_dim;
@@ -471,16 +472,16 @@ size_t pmha_edge_weights_workspace_size(const pmha_graph *g, const pmha_params *
 }
 
 pmha_status pmha_forward(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
-                         const void *value, int64_t batch, void *output, pmha_wmode wmode, float *weights,
-                         void *workspace, size_t ws_bytes, pmha_stream stream)
+                         const void *value, const uint8_t *key_padding_mask, int64_t batch, void *output,
+                         pmha_wmode wmode, float *weights, void *workspace, size_t ws_bytes, pmha_stream stream)
 {
-    return forward_device(g, p, query, key, value, batch, output, wmode, weights, workspace, ws_bytes,
+    return forward_device(g, p, query, key, value, key_padding_mask, batch, output, wmode, weights, workspace, ws_bytes,
                           (cudaStream_t)stream);
 }
 
-// Host-buffer variant: [inputs | output | weights | forward workspace].
+// Host-buffer variant: [inputs | key_padding_mask | output | weights | forward workspace].
 static size_t host_staging(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode wmode, size_t *off_in,
-                           size_t *off_out, size_t *off_w, size_t *off_ws)
+                           size_t *off_mask, size_t *off_out, size_t *off_w, size_t *off_ws)
 {
     const size_t es = elem_size(p->dtype);
     const size_t q = align256((size_t)(B * g->L * p->embed_dim) * es);
@@ -488,6 +489,8 @@ static size_t host_staging(const pmha_graph *g, const pmha_params *p, int64_t B,
     size_t o = 0;
     *off_in = o;
     o += q + 2 * kv;
+    *off_mask = o;
+    o += align256((size_t)(B * g->S));
     *off_out = o;
     o += q;
     *off_w = o;
@@ -501,12 +504,12 @@ size_t pmha_forward_host_workspace_size(const pmha_graph *g, const pmha_params *
 {
     if (check_params(g, p, batch) != PMHA_OK) return 0;
     if (wmode != PMHA_WEIGHTS_NONE && wmode != PMHA_WEIGHTS_AVG && wmode != PMHA_WEIGHTS_PER_HEAD) return 0;
-    size_t a, b, c, d;
-    return host_staging(g, p, batch, wmode, &a, &b, &c, &d);
+    size_t a, b, c, d, e;
+    return host_staging(g, p, batch, wmode, &a, &b, &c, &d, &e);
 }
 
 pmha_status pmha_forward_host(const pmha_graph *g, const pmha_params *p, const void *qh, const void *kh,
-                              const void *vh, int64_t B, void *oh, pmha_wmode wmode, float *wh, void *workspace,
+                              const void *vh, const uint8_t *mh, int64_t B, void *oh, pmha_wmode wmode, float *wh, void *workspace,
                               size_t ws_bytes, pmha_stream stream)
 {
     pmha_status st = check_params(g, p, B);
@@ -516,8 +519,8 @@ pmha_status pmha_forward_host(const pmha_graph *g, const pmha_params *p, const v
         set_error("pmha_forward_host: NULL host buffer");
         return PMHA_ERR_INVALID_ARG;
     }
-    size_t off_in, off_out, off_w, off_ws;
-    const size_t need = host_staging(g, p, B, wmode, &off_in, &off_out, &off_w, &off_ws);
+    size_t off_in, off_mask, off_out, off_w, off_ws;
+    const size_t need = host_staging(g, p, B, wmode, &off_in, &off_mask, &off_out, &off_w, &off_ws);
     if (!workspace || ws_bytes < need || ((uintptr_t)workspace & 255u)) {
         set_error("pmha_forward_host: workspace needs %zu bytes, 256-byte aligned", need);
         return PMHA_ERR_WORKSPACE;
@@ -538,9 +541,11 @@ pmha_status pmha_forward_host(const pmha_graph *g, const pmha_params *p, const v
         if (vh == kh) v_dev = k_dev;
         else if (vh == qh && g->L == g->S) v_dev = dq;
         else PMHA_CUDA_TRY(cudaMemcpyAsync(dv, vh, kb, cudaMemcpyHostToDevice, s));
+        if (mh) PMHA_CUDA_TRY(cudaMemcpyAsync(ws + off_mask, mh, (size_t)(B * g->S), cudaMemcpyHostToDevice, s));
     }
+    const uint8_t *m_dev = mh ? (const uint8_t *)(ws + off_mask) : nullptr;
     float *dw = wmode != PMHA_WEIGHTS_NONE ? (float *)(ws + off_w) : nullptr;
-    st = forward_device(g, p, q_dev, k_dev, v_dev, B, ws + off_out, wmode, dw, ws + off_ws, ws_bytes - off_ws, s);
+    st = forward_device(g, p, q_dev, k_dev, v_dev, m_dev, B, ws + off_out, wmode, dw, ws + off_ws, ws_bytes - off_ws, s);
     if (st != PMHA_OK) return st;
     {
         StageTimer timer("d2h", s);
@@ -554,7 +559,7 @@ pmha_status pmha_forward_host(const pmha_graph *g, const pmha_params *p, const v
 }
 
 pmha_status pmha_edge_weights(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
-                              int64_t B, pmha_wmode wmode, float *weights, void *workspace, size_t ws_bytes,
+                              const uint8_t *key_padding_mask, int64_t B, pmha_wmode wmode, float *weights, void *workspace, size_t ws_bytes,
                               pmha_stream stream)
 {
     pmha_status st = check_params(g, p, B);
@@ -573,7 +578,7 @@ pmha_status pmha_edge_weights(const pmha_graph *g, const pmha_params *p, const v
         set_error("workspace needs %zu bytes, 256-byte aligned (got %zu)", lay.total, ws_bytes);
         return PMHA_ERR_WORKSPACE;
     }
-    return attend(g, p, query, key, key, B, wmode, weights, (char *)workspace, lay, false, (cudaStream_t)stream,
+    return attend(g, p, query, key, key, key_padding_mask, B, wmode, weights, (char *)workspace, lay, false, (cudaStream_t)stream,
                   nullptr);
 }
 

@@ -65,12 +65,16 @@ __global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge
     if (lane < H) {
         float mh = -INFINITY;
         for (int i = 0; i < n_pieces; ++i) mh = fmaxf(mh, piece(i)[lane]);
+        // A piece whose keys were all dropped has m = -inf and l = 0, and
+        // ex2.approx(-inf) is +0, so it adds nothing; when every piece is
+        // empty (M = -inf) the offset 0 stands in for M and avoids -inf - -inf.
+        const float mo = mh == -INFINITY ? 0.f : mh;
         float lh = 0.f;
         for (int i = 0; i < n_pieces; ++i) {
             const float *p = piece(i);
-            lh = __fadd_rn(lh, __fmul_rn(p[H + lane], ex2(__fsub_rn(p[lane], mh))));
+            lh = __fadd_rn(lh, __fmul_rn(p[H + lane], ex2(__fsub_rn(p[lane], mo))));
         }
-        sm_m[wib][lane] = mh;
+        sm_m[wib][lane] = mo;
         sm_l[wib][lane] = lh;
         if (mlrow) {
             mlrow[2 * lane] = mh;
@@ -126,7 +130,10 @@ __global__ void k_weights(const float *scores, const float *__restrict__ ml,
     const float *st = ml + ((b * L + t) * H) * 2;
     float sum = 0.f;
     for (int h = 0; h < H; ++h) {
-        const float w = __fmul_rn(ex2(__fsub_rn(s[h], st[2 * h])), __frcp_rn(st[2 * h + 1]));
+        // a dropped key (score -inf) or a target with no live key (l = 0) weighs 0
+        const float w = (st[2 * h + 1] == 0.f || s[h] == -INFINITY)
+                            ? 0.f
+                            : __fmul_rn(ex2(__fsub_rn(s[h], st[2 * h])), __frcp_rn(st[2 * h + 1]));
         if (average) sum = __fadd_rn(sum, w);
         else out[i * H + h] = w;
     }
@@ -182,6 +189,7 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.col = g->col;
     k.perm = g->perm;
     k.unit_first_t = g->unit_first_t;
+    k.kpm = a.kpm;
     k.n_units = g->n_units;
     k.nnz = g->nnz;
     k.B = (int)a.B;

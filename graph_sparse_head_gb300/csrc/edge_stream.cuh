@@ -59,6 +59,7 @@ struct Args {
     const int32_t *col;
     const int32_t *perm;
     const int32_t *unit_first_t;
+    const uint8_t *kpm;  // (B, S) key_padding_mask, nonzero = key dropped; or null
     long long n_units, nnz;
     int B, L, S, E, H, d;
     float score_scale;
@@ -211,7 +212,9 @@ __device__ __forceinline__ void store_row(T *p, const f2 (&v)[CPL / 2])
     }
 }
 
-template <typename T, int CPL, int LPE, bool WV, bool WS>
+// WV: mix values (else scores and (m, l) only); WS: write raw scores;
+// KPM: read a key_padding_mask (a dropped key scores -inf).
+template <typename T, int CPL, int LPE, bool WV, bool WS, bool KPM>
 __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
 {
     constexpr int P = 32 / LPE;               // slots per warp
@@ -297,6 +300,23 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
             perm_nxt = p < n ? a.perm[e0 + p] : 0;
         }
         return __shfl_sync(smask, perm_cur, j & (LPE - 1), LPE);
+    };
+
+    // ---- key_padding_mask of the sources, one window of LPE positions ahead
+    // (lane grp holds the flag of position w * LPE + grp)
+    const uint8_t *kpm_b = KPM ? a.kpm + (long long)b * a.S : nullptr;
+    auto ldmask = [&](int w) -> int {
+        const int p = w * LPE + grp;
+        return (KPM && p < n) ? (int)kpm_b[colu[p]] : 0;
+    };
+    int mw = 0, km_cur = ldmask(0), km_nxt = ldmask(1);
+    auto masked = [&](int j) -> bool {  // j never decreases
+        if (j >= (mw + 1) * LPE) {
+            ++mw;
+            km_cur = km_nxt;
+            km_nxt = ldmask(mw + 1);
+        }
+        return __shfl_sync(smask, km_cur, j & (LPE - 1), LPE) != 0;
     };
 
     // ---- target bounds: lane grp holds row_ptr[tw + grp + 1], the end of target tw + grp
@@ -409,14 +429,18 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     auto one = [&](int j, const Raw<CB> &kr, const Raw<CB> &vr) {
         const int pos = e0 + j;
         if (pos >= bound) advance(pos);
-        const float dot = score(kr);
+        float dot = score(kr);
+        if constexpr (KPM)
+            if (masked(j)) dot = -INFINITY;
         if constexpr (WS) {
             const int e = edge_id(j);
             if (head_leader) scores_b[(long long)e * a.H + head] = dot;
         }
         const float m_new = fmaxf(m, dot);
         const float scale = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, m_new));
-        const float p = ex2(__fsub_rn(dot, m_new));
+        // ex2.approx(-inf) is +0, so a dropped edge gives p = 0 once some key
+        // is live; before that m_new is -inf and the offset 0 avoids -inf - -inf
+        const float p = ex2(__fsub_rn(dot, (KPM && m_new == -INFINITY) ? 0.f : m_new));
         l = __fadd_rn(__fmul_rn(l, scale), p);
         if constexpr (WV) {
             rescale(scale);
@@ -441,7 +465,11 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
         const int pos = e0 + j;
         if (j + 1 < n && pos + 1 < bound) {
             // both edges belong to t: two independent scores, one rescale
-            const float d0 = score(kr0), d1 = score(kr1);
+            float d0 = score(kr0), d1 = score(kr1);
+            if constexpr (KPM) {
+                if (masked(j)) d0 = -INFINITY;
+                if (masked(j + 1)) d1 = -INFINITY;
+            }
             if constexpr (WS) {
                 const int i0 = edge_id(j), i1 = edge_id(j + 1);
                 if (head_leader) {
@@ -451,8 +479,9 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
             }
             const float m_new = fmaxf(m, fmaxf(d0, d1));
             const float scale = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, m_new));
-            const float p0 = ex2(__fsub_rn(d0, m_new));
-            const float p1 = ex2(__fsub_rn(d1, m_new));
+            const float m_off = (KPM && m_new == -INFINITY) ? 0.f : m_new;
+            const float p0 = ex2(__fsub_rn(d0, m_off));
+            const float p1 = ex2(__fsub_rn(d1, m_off));
             l = __fadd_rn(__fadd_rn(__fmul_rn(l, scale), p0), p1);
             if constexpr (WV) {
                 rescale(scale);
@@ -478,7 +507,10 @@ pmha_status launch(const Args &k, long long slots, cudaStream_t s)
     const long long warps = (k.B + P - 1) / P * k.n_units;
     const long long blocks = (warps + kWarps - 1) / kWarps;
     (void)slots;
-    auto kern = k.scores ? k_edge_stream<T, CPL, LPE, WV, true> : k_edge_stream<T, CPL, LPE, WV, false>;
+    auto kern = k.kpm ? (k.scores ? k_edge_stream<T, CPL, LPE, WV, true, true>
+                                  : k_edge_stream<T, CPL, LPE, WV, false, true>)
+                      : (k.scores ? k_edge_stream<T, CPL, LPE, WV, true, false>
+                                  : k_edge_stream<T, CPL, LPE, WV, false, false>);
     if constexpr (smem > 48 * 1024) {
         PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     }

@@ -35,7 +35,8 @@ void *g_scratch_addr[kMaxDevices] = {nullptr};
 }  // namespace
 
 extern "C" pmha_status pmha_forward_noalloc(const pmha_graph *graph, const pmha_params *params, const void *query,
-                                            const void *key, const void *value, int64_t batch, void *output,
+                                            const void *key, const void *value,
+                                            const uint8_t *key_padding_mask, int64_t batch, void *output,
                                             pmha_wmode wmode, float *weights, pmha_stream stream)
 {
     int dev = 0;
@@ -65,6 +66,6 @@ extern "C" pmha_status pmha_forward_noalloc(const pmha_graph *graph, const pmha_
                         need, (size_t)PMHA_NOALLOC_SCRATCH_BYTES);
         return PMHA_ERR_WORKSPACE;
     }
-    return pmha_forward(graph, params, query, key, value, batch, output, wmode, weights, scratch,
+    return pmha_forward(graph, params, query, key, value, key_padding_mask, batch, output, wmode, weights, scratch,
                         (size_t)PMHA_NOALLOC_SCRATCH_BYTES, stream);
 }

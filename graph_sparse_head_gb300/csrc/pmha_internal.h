@@ -112,6 +112,7 @@ struct EdgeArgs {
     float *part;          // (B, 2 n_units, 2H + E): per slot m[H], l[H], acc[E] of a crossing target
     float *ml;            // (B, L, H, 2): running max (log2 units) and sum per target/head
     float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
+    const uint8_t *kpm;   // (B, S) key_padding_mask, nonzero = key dropped, or null
     int64_t B, L, S, E, H, nnz;
     float score_scale;    // log2(e) / sqrt(d)
     bool with_values;     // false: scores and (m, l) only

@@ -150,6 +150,11 @@ size_t pmha_edge_weights_workspace_size(const pmha_graph *graph, const pmha_para
  *         Passing the same pointer for all three (with L == S) is attention
  *         within one graph and lets the library project them in one GEMM;
  *         key == value shares one GEMM for both.
+ *  key_padding_mask  device (B, S) bytes or NULL (forward()'s key_padding_mask):
+ *         a nonzero byte drops key s of sample b from the softmax of every
+ *         target it feeds; such an edge weighs 0, and a target whose keys
+ *         are all dropped mixes to zeros, so its output row is out_proj's
+ *         bias. Read-only; NULL drops nothing.
  *  batch  B >= 1.
  *  output device (B, L, E) in params->dtype; must not overlap the inputs.
  *  wmode  PMHA_WEIGHTS_NONE, _AVG or _PER_HEAD (need_weights /
@@ -165,9 +170,9 @@ size_t pmha_edge_weights_workspace_size(const pmha_graph *graph, const pmha_para
  * the call does not synchronize).
  */
 pmha_status pmha_forward(const pmha_graph *graph, const pmha_params *params, const void *query,
-                         const void *key, const void *value, int64_t batch, void *output,
-                         pmha_wmode wmode, float *weights, void *workspace,
-                         size_t workspace_bytes, pmha_stream stream);
+                         const void *key, const void *value, const uint8_t *key_padding_mask,
+                         int64_t batch, void *output, pmha_wmode wmode, float *weights,
+                         void *workspace, size_t workspace_bytes, pmha_stream stream);
 
 /*
  * pmha_forward_host - pmha_forward on HOST buffers: copies query / key / value
@@ -176,14 +181,15 @@ pmha_status pmha_forward(const pmha_graph *graph, const pmha_params *params, con
  * returns after queuing the work, so synchronize `stream` before reading the
  * results. Host buffers should be pinned for the copies to overlap.
  * Same shapes as pmha_forward; equal host pointers for query / key / value
- * are copied once. The workspace must hold pmha_forward_host_workspace_size()
+ * are copied once. key_padding_mask_host is a host (B, S) byte array or NULL. The workspace must hold pmha_forward_host_workspace_size()
  * bytes (the device copies of inputs and results live there).
  */
 size_t pmha_forward_host_workspace_size(const pmha_graph *graph, const pmha_params *params,
                                         int64_t batch, pmha_wmode wmode);
 pmha_status pmha_forward_host(const pmha_graph *graph, const pmha_params *params,
                               const void *query_host, const void *key_host,
-                              const void *value_host, int64_t batch, void *output_host,
+                              const void *value_host, const uint8_t *key_padding_mask_host,
+                              int64_t batch, void *output_host,
                               pmha_wmode wmode, float *weights_host, void *workspace,
                               size_t workspace_bytes, pmha_stream stream);
 
@@ -197,7 +203,8 @@ pmha_status pmha_forward_host(const pmha_graph *graph, const pmha_params *params
  * Other arguments as in pmha_forward.
  */
 pmha_status pmha_edge_weights(const pmha_graph *graph, const pmha_params *params,
-                              const void *query, const void *key, int64_t batch, pmha_wmode wmode,
+                              const void *query, const void *key,
+                              const uint8_t *key_padding_mask, int64_t batch, pmha_wmode wmode,
                               float *weights, void *workspace, size_t workspace_bytes,
                               pmha_stream stream);
 
@@ -227,7 +234,8 @@ pmha_status pmha_device_status(pmha_stream stream);
  */
 #define PMHA_NOALLOC_SCRATCH_BYTES (64u << 20)
 pmha_status pmha_forward_noalloc(const pmha_graph *graph, const pmha_params *params, const void *query,
-                                 const void *key, const void *value, int64_t batch, void *output,
+                                 const void *key, const void *value,
+                                 const uint8_t *key_padding_mask, int64_t batch, void *output,
                                  pmha_wmode wmode, float *weights, pmha_stream stream);
 
 /* Message describing the last failure of a call made by this thread ("" if none). */

@@ -95,6 +95,18 @@ def make_tokens(rng: np.random.Generator, batch: int, seq: int, embed_dim: int,
     return _store(x, dtype)
 
 
+def padding_mask(rng: np.random.Generator, batch: int, seq: int, min_keep: float = 0.5) -> np.ndarray:
+    """key_padding_mask of samples padded at the end: sample b keeps its first
+    n_b ~ U[min_keep * seq, seq] keys and flags the rest (True = padding)."""
+    keep = rng.integers(int(np.ceil(min_keep * seq)), seq + 1, size=batch)
+    return np.arange(seq)[None, :] >= keep[:, None]
+
+
+def scattered_mask(rng: np.random.Generator, batch: int, seq: int, p: float) -> np.ndarray:
+    """key_padding_mask with each key flagged independently with probability p."""
+    return rng.random((batch, seq)) < p
+
+
 def shuffle_edges(rng, src, tgt):
     p = rng.permutation(len(src))
     return np.ascontiguousarray(src[p], dtype=np.int64), np.ascontiguousarray(tgt[p], dtype=np.int64)

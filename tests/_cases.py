@@ -84,7 +84,8 @@ class Case:
         xkv = xq if self.xkv is self.xq else torch.from_numpy(self.xkv).to(dev).to(tdt)
         return xq, xkv
 
-    def run(self, dev, wmode="none", add_self_loops=False, graph=None):
+    def run(self, dev, wmode="none", add_self_loops=False, graph=None, kpm=None):
+        """kpm: (B, S) bool numpy key_padding_mask or None."""
         import torch
         import graph_sparse_head_gb300 as pmha
         params = pmha.Params.from_arrays(self.params, self.H, torch_dtype(self.dt), dev)
@@ -92,13 +93,15 @@ class Case:
             graph = pmha.pmha_build_csr(torch.from_numpy(self.src).to(dev), torch.from_numpy(self.tgt).to(dev),
                                         self.L, self.S, add_self_loops)
         xq, xkv = self.device_inputs(dev)
-        out, w = pmha.pmha_forward(graph, params, xq, xkv, xkv, wmode)
+        mask = None if kpm is None else torch.from_numpy(np.ascontiguousarray(kpm, dtype=np.bool_)).to(dev)
+        out, w = pmha.pmha_forward(graph, params, xq, xkv, xkv, wmode, key_padding_mask=mask)
         pmha.pmha_device_status()
         return graph, params, out, w
 
     # ------------------------------------------------------------ oracle
-    def oracle(self, need_weights=True, src=None, tgt=None):
+    def oracle(self, need_weights=True, src=None, tgt=None, kpm=None):
         import oracle
         src = self.src if src is None else src
         tgt = self.tgt if tgt is None else tgt
-        return oracle.forward(self.xq, self.xkv, self.xkv, self.params, src, tgt, self.H, need_weights)
+        return oracle.forward(self.xq, self.xkv, self.xkv, self.params, src, tgt, self.H, need_weights,
+                              key_padding_mask=kpm)

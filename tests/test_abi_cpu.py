@@ -62,8 +62,8 @@ def test_host_checks_before_device_work(lib):
     # misaligned index pointers
     assert lib.pmha_build_csr(ctypes.c_void_p(65), ctypes.c_void_p(64), 3, 4, 4, 0, None, ctypes.byref(out)) == 1
     # NULL graph / params
-    assert lib.pmha_forward(None, None, None, None, None, 1, None, 0, None, None, 0, None) == 1
-    assert lib.pmha_edge_weights(None, None, None, None, 1, 1, None, None, 0, None) == 1
+    assert lib.pmha_forward(None, None, None, None, None, None, 1, None, 0, None, None, 0, None) == 1
+    assert lib.pmha_edge_weights(None, None, None, None, None, 1, 1, None, None, 0, None) == 1
     assert lib.pmha_forward_workspace_size(None, None, 1, 0) == 0
     assert lib.pmha_graph_info(None, None, None, None, None) == 1
     lib.pmha_graph_destroy(None)

@@ -185,13 +185,13 @@ def test_argument_errors():
     import ctypes
     lib = pmha._lib.load()
     p = params.as_struct()
-    st = lib.pmha_forward(g.handle, ctypes.byref(p), xq.data_ptr(), xq.data_ptr(), xq.data_ptr(), 2,
+    st = lib.pmha_forward(g.handle, ctypes.byref(p), xq.data_ptr(), xq.data_ptr(), xq.data_ptr(), None, 2,
                           out.data_ptr(), 0, None, small_ws.data_ptr(), 16, None)
     assert pmha._lib.STATUS_NAMES[st] == "PMHA_ERR_WORKSPACE"
-    st = lib.pmha_forward(g.handle, ctypes.byref(p), xq.data_ptr(), xq.data_ptr(), xq.data_ptr(), 2,
+    st = lib.pmha_forward(g.handle, ctypes.byref(p), xq.data_ptr(), xq.data_ptr(), xq.data_ptr(), None, 2,
                           out.data_ptr(), 7, None, small_ws.data_ptr(), 16, None)
     assert pmha._lib.STATUS_NAMES[st] == "PMHA_ERR_INVALID_ARG"
-    st = lib.pmha_forward(g.handle, ctypes.byref(p), xq.data_ptr() + 4, xq.data_ptr(), xq.data_ptr(), 2,
+    st = lib.pmha_forward(g.handle, ctypes.byref(p), xq.data_ptr() + 4, xq.data_ptr(), xq.data_ptr(), None, 2,
                           out.data_ptr(), 0, None, small_ws.data_ptr(), 16, None)
     assert pmha._lib.STATUS_NAMES[st] == "PMHA_ERR_INVALID_ARG"
     bad = pmha._lib.PmhaParams(32, 5, 0, p.wq, p.wk, p.wv, p.wo, None, None, None, None)

@@ -22,7 +22,7 @@ DEV = "cuda:0"
 
 def _noalloc(lib, g, p, xq, xkv, out, wmode, w):
     import graph_sparse_head_gb300 as pmha
-    st = lib.pmha_forward_noalloc(g.handle, ctypes.byref(p), xq.data_ptr(), xkv.data_ptr(), xkv.data_ptr(),
+    st = lib.pmha_forward_noalloc(g.handle, ctypes.byref(p), xq.data_ptr(), xkv.data_ptr(), xkv.data_ptr(), None,
                                   xq.shape[0], out.data_ptr(), pmha.WMODES[wmode],
                                   None if w is None else w.data_ptr(), torch.cuda.current_stream().cuda_stream)
     pmha._lib.check(st, "pmha_forward_noalloc")
@@ -56,7 +56,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     p = params.as_struct()
     xq, xkv = c.device_inputs(DEV)
     out = torch.empty_like(ref_out)
-    st = lib.pmha_forward_noalloc(g.handle, ctypes.byref(p), xq.data_ptr(), xkv.data_ptr(), xkv.data_ptr(), 4,
+    st = lib.pmha_forward_noalloc(g.handle, ctypes.byref(p), xq.data_ptr(), xkv.data_ptr(), xkv.data_ptr(), None, 4,
                                   out.data_ptr(), 0, None, torch.cuda.current_stream().cuda_stream)
     assert pmha._lib.STATUS_NAMES[st] == "PMHA_ERR_WORKSPACE"
     assert b"scratch" in lib.pmha_last_error()
