@@ -183,7 +183,7 @@ pmha_status check_params(const pmha_graph *g, const pmha_params *p, int64_t batc
 }
 
 struct Layout {
-    size_t qkv = 0, mixed = 0, part = 0, ml = 0, scores = 0, wo16 = 0, total = 0;
+    size_t qkv = 0, mixed = 0, part = 0, ml = 0, scores = 0, wo16 = 0, vt = 0, total = 0;
 };
 
 bool out_proj_on_tensor_cores(const pmha_params *p)
@@ -213,6 +213,8 @@ Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode w
     if (wmode == PMHA_WEIGHTS_AVG) o += align256((size_t)(B * g->nnz * H) * 4);
     l.wo16 = o;
     if (with_values && out_proj_on_tensor_cores(p)) o += align256((size_t)(E * E) * 2);
+    l.vt = o;
+    if (with_values && dense_supported(g, E, H, inter_type(p->dtype))) o += align256(dense_vt_bytes(g, B, E));
     l.total = o;
     return l;
 }
@@ -298,6 +300,34 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.score_scale = (float)(1.4426950408889634 / sqrt((double)(E / H)));
     a.with_values = with_values;
     a.kpm = kpm;
+    const TcType it = inter_type(p->dtype);
+    if (with_values && dense_supported(g, E, H, it)) {
+        // most (target, source) pairs are edges: steps 2-4 as masked-dense tiles
+        DenseInputs din;
+        din.q = a.q;
+        din.q_ld = a.q_ld;
+        din.k = a.kv;
+        din.k_ld = a.kv_ld;
+        din.v = (const char *)a.kv + (size_t)a.v_off * es;
+        din.v_ld = a.kv_ld;
+        din.vt = ws + lay.vt;
+        din.mixed = a.mixed;
+        din.kpm = kpm;
+        din.B = B;
+        din.E = E;
+        din.H = H;
+        if ((st = dense_attention(g, din, s)) != PMHA_OK) return st;
+        if (wmode != PMHA_WEIGHTS_NONE) {
+            // weights from the per-edge scores: the kernels pmha_edge_weights runs
+            EdgeArgs w = a;
+            w.with_values = false;
+            if ((st = edge_attention(it, g, w, s)) != PMHA_OK) return st;
+            if ((st = split_merge(it, g, w, s)) != PMHA_OK) return st;
+            if ((st = weights_finalize(g, w, wmode, weights, s)) != PMHA_OK) return st;
+        }
+        if (mixed_out) *mixed_out = a.mixed;
+        return PMHA_OK;
+    }
     if ((st = edge_attention(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
     if ((st = split_merge(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
     if (wmode != PMHA_WEIGHTS_NONE)
@@ -453,6 +483,7 @@ void pmha_graph_destroy(pmha_graph *g)
     cudaGetDevice(&cur);
     if (cur != g->device) cudaSetDevice(g->device);
     cudaFree(g->mem);
+    if (g->adj) cudaFree(g->adj);
     if (cur != g->device) cudaSetDevice(cur);
     delete g;
 }

@@ -322,6 +322,20 @@ __global__ void k_check_and_view(const K *__restrict__ keys, const int *__restri
     tgt_of_edge[vals[i]] = (int32_t)t;
 }
 
+// Adjacency bits of a dense graph: block t sets bit s of row t for every
+// source s of target t.
+__global__ void k_adj_bits(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col, int64_t words,
+                           uint32_t *__restrict__ adj)
+{
+    const int t = blockIdx.x;
+    const int beg = row_ptr[t], end = row_ptr[t + 1];
+    uint32_t *row = adj + (int64_t)t * words;
+    for (int p = beg + (int)threadIdx.x; p < end; p += blockDim.x) {
+        const int s = col[p];
+        atomicOr(&row[s >> 5], 1u << (s & 31));
+    }
+}
+
 template <typename K>
 __global__ void k_row_ptr(const K *__restrict__ keys, const Summary *__restrict__ sum, int64_t L,
                           int64_t S, int32_t *__restrict__ row_ptr)
@@ -509,6 +523,36 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         g->max_deg = host_sum->max_deg;
         g->n_units = (g->nnz + kUnitEdges - 1) / kUnitEdges;
         g->n_merge = host_sum->n_merge;
+        // A graph with at least a quarter of all (target, source) pairs may run
+        // the masked-dense tensor-core kernel; it keeps the pairs as bits
+        // (none for a complete graph). Without room for the bits the graph
+        // simply stays on the per-edge path.
+        const double pairs = (double)L * (double)S;
+        if ((double)g->nnz * 4.0 >= pairs && pairs <= (double)(1ull << 29)) {
+            g->dense_complete = g->nnz == L * S;
+            g->dense = true;
+            if (!g->dense_complete) {
+                g->adj_words_per_row = (S + 31) / 32;
+                const size_t bytes = (size_t)L * (size_t)g->adj_words_per_row * 4;
+                if (cudaMalloc(&g->adj, bytes) != cudaSuccess) {
+                    cudaGetLastError();
+                    g->adj = nullptr;
+                    g->dense = false;
+                } else {
+                    do {
+                        if ((ce = cudaMemsetAsync(g->adj, 0, bytes, stream)) != cudaSuccess) break;
+                        k_adj_bits<<<(unsigned)L, 256, 0, stream>>>(g->row_ptr, g->col, g->adj_words_per_row, g->adj);
+                        count_launch();
+                        if ((ce = cudaGetLastError()) != cudaSuccess) break;
+                        ce = cudaStreamSynchronize(stream);
+                    } while (0);
+                    if (ce != cudaSuccess) {
+                        st = cuda_fail(ce, "CSR build (adjacency bits)");
+                        cudaFree(g->adj);
+                    }
+                }
+            }
+        }
     }
     cudaFree(tm);
     cudaFreeHost(host_sum);

@@ -1,0 +1,478 @@
+// Edge attention of a dense graph on the 5th-generation tensor cores
+// (kpnn2 PackedMultiheadAttention, Notes steps 2-4). The page observes that
+// restricting attention to the graph's edges gives the same mix as dense
+// attention whose score matrix is masked to the edges; when most (target,
+// source) pairs are edges, the masked dense form is the cheaper one: the
+// scores of a 128-target x 128-source tile are one tensor-core product, and
+// every k|v row is read once per tile instead of once per edge.
+//
+// One CTA per (sample b, head h, tile of 128 targets), 6 warps:
+//   warp 4   TMA producer: the q tile once, then per 128-source step the k tile
+//            (128 sources x d) and the v^T tile (d x 128 sources), 128-byte
+//            swizzle, two stages
+//   warp 5   allocates 256 TMEM columns and issues, from one thread,
+//            S = Q K^T (M=128, N=128, fp32 in TMEM columns 0-127) and
+//            O_step = P V (M=128, N=d, TMEM columns 128-..) with tcgen05.mma
+//   warps 0-3 one thread per target row: read S from TMEM, mask it (the
+//            graph's adjacency bits, key_padding_mask, sources past S),
+//            online softmax in log2 units, P in fp16 into a swizzled shared
+//            tile (the A operand of P V), then O = O * alpha + O_step in
+//            registers; finally mixed = O / l in fp16.
+// V enters transposed (channels x tokens, written by a transpose kernel from
+// the projection) so that both products take K-major operands.
+//
+// Every mbarrier wait is bounded; on expiry the CTA records PMHA_ERR_TIMEOUT,
+// drains its own copies and MMAs (bounded), frees its tensor memory and returns.
+#include <cuda_fp16.h>
+
+#include <set>
+
+#include "tc_util.cuh"
+
+namespace pmha {
+namespace {
+using namespace tcu;
+
+constexpr int kTM = 128;       // targets per CTA
+constexpr int kTN = 128;       // sources per step
+constexpr int kThreads = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kTmemCols = 256;
+
+template <int D>
+struct DenseLayout {
+    static constexpr int DC = D / 64;                       // 64-channel chunks of a head
+    static constexpr int kQBytes = DC * kTM * 128;           // q tile
+    static constexpr int kKBytes = DC * kTN * 128;           // k tile of one stage
+    static constexpr int kVBytes = 2 * D * 128;              // v^T tile of one stage: 2 chunks of 64 sources
+    static constexpr int kPBytes = 2 * kTM * 128;            // P: 2 chunks of 64 sources
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffV = kOffK + 2 * kKBytes;
+    static constexpr int kOffP = kOffV + 2 * kVBytes;
+    static constexpr int kOffWords = kOffP + kPBytes;        // uint32 [2][4] source-validity words
+    static constexpr int kOffBars = kOffWords + 64;
+    static constexpr int kSmem = kOffBars + 256 + 1024;      // + alignment slack
+};
+
+struct DenseArgs {
+    int B, L, S, H, n_tiles_t;
+    int S_pad;                    // columns per sample in V^T (S rounded up to 8)
+    float score_scale;            // log2(e) / sqrt(d)
+    const uint32_t *adj;          // L x words_per_row adjacency bits, or null (complete graph)
+    long long words_per_row;
+    const uint8_t *kpm;           // (B, S) or null
+    __half *mixed;                // (B, L, E)
+    int E;
+    int *err;
+};
+
+// Instruction descriptor, kind::f16 with f16 A/B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
+{
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// barrier 1 over the 128 softmax threads, returning whether any of them passed `pred`
+__device__ __forceinline__ bool softmax_vote(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_vt, DenseArgs a)
+{
+    using LY = DenseLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint32_t *words = (uint32_t *)(smem + LY::kOffWords);
+    uint64_t *bars = (uint64_t *)(smem + LY::kOffBars);
+    uint64_t *q_full = bars;           // [1]
+    uint64_t *kv_full = bars + 1;      // [2]
+    uint64_t *kv_empty = bars + 3;     // [2]
+    uint64_t *s_full = bars + 5;       // [1]
+    uint64_t *s_free = bars + 6;       // [1]
+    uint64_t *p_full = bars + 7;       // [1]
+    uint64_t *o_full = bars + 8;       // [1]
+    uint64_t *o_free = bars + 9;       // [1]
+    uint64_t *mma_done = bars + 10;    // [1]
+    uint32_t *tmem_holder = (uint32_t *)(bars + 11);
+    volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
+    int *issued = (int *)(tmem_holder + 2);  // [3]: TMA phases armed (q, stage 0, stage 1)
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int it = blockIdx.x % a.n_tiles_t;
+    const int bh = blockIdx.x / a.n_tiles_t;
+    const int h = bh % a.H, b = bh / a.H;
+    const int t0 = it * kTM;
+    const int n_steps = (a.S + kTN - 1) / kTN;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(q_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&kv_full[s]), 1);
+            mbar_init(smem_u32(&kv_empty[s]), 1);
+        }
+        mbar_init(smem_u32(s_full), 1);
+        mbar_init(smem_u32(s_free), 128);
+        mbar_init(smem_u32(p_full), 128);
+        mbar_init(smem_u32(o_full), 1);
+        mbar_init(smem_u32(o_free), 128);
+        mbar_init(smem_u32(mma_done), 1);
+        issued[0] = issued[1] = issued[2] = 0;
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t tmem_s = tmem_base, tmem_o = tmem_base + kTN;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            const uint32_t qb = smem_u32(q_full);
+            mbar_arrive_expect_tx(qb, LY::kQBytes);
+            issued[0] = 1;
+#pragma unroll
+            for (int c = 0; c < LY::DC; ++c)
+                tma_load_2d(smem_u32(smem + LY::kOffQ + c * kTM * 128), &tm_q, h * D + c * 64, b * a.L + t0, qb);
+            for (int j = 0; j < n_steps; ++j) {
+                const int s = j & 1;
+                if (!mbar_wait(smem_u32(&kv_empty[s]), ((j >> 1) & 1) ^ 1u, abort_flag, a.err)) break;
+                const uint32_t fb = smem_u32(&kv_full[s]);
+                mbar_arrive_expect_tx(fb, LY::kKBytes + LY::kVBytes);
+                issued[1 + s] += 1;
+                const uint32_t kdst = smem_u32(smem + LY::kOffK + s * LY::kKBytes);
+                const uint32_t vdst = smem_u32(smem + LY::kOffV + s * LY::kVBytes);
+#pragma unroll
+                for (int c = 0; c < LY::DC; ++c)
+                    tma_load_2d(kdst + c * kTN * 128, &tm_k, h * D + c * 64, b * a.S + j * kTN, fb);
+#pragma unroll
+                for (int kc = 0; kc < 2; ++kc)
+                    tma_load_2d(vdst + kc * D * 128, &tm_vt, b * a.S_pad + j * kTN + kc * 64, h * D, fb);
+            }
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, a.err);
+            tc_fence_after();
+            const uint32_t qa = smem_u32(smem + LY::kOffQ);
+            const uint32_t pa = smem_u32(smem + LY::kOffP);
+            for (int j = 0; ok && j < n_steps; ++j) {
+                const int s = j & 1;
+                if (!mbar_wait(smem_u32(&kv_full[s]), (j >> 1) & 1, abort_flag, a.err)) break;
+                if (j > 0 && !mbar_wait(smem_u32(s_free), (j - 1) & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(smem + LY::kOffK + s * LY::kKBytes);
+#pragma unroll
+                for (int c = 0; c < LY::DC; ++c)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16kind(tmem_s, smem_desc(qa + c * kTM * 128) + (uint64_t)(2 * k),
+                                    smem_desc(ka + c * kTN * 128) + (uint64_t)(2 * k), idesc_f16(kTM, kTN),
+                                    (c > 0 || k > 0) ? 1u : 0u);
+                mma_commit(smem_u32(s_full));
+                if (!mbar_wait(smem_u32(p_full), j & 1, abort_flag, a.err)) break;
+                if (j > 0 && !mbar_wait(smem_u32(o_free), (j - 1) & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+                const uint32_t va = smem_u32(smem + LY::kOffV + s * LY::kVBytes);
+#pragma unroll
+                for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_f16kind(tmem_o, smem_desc(pa + kc * kTM * 128) + (uint64_t)(2 * k),
+                                    smem_desc(va + kc * D * 128) + (uint64_t)(2 * k), idesc_f16(kTM, D),
+                                    (kc > 0 || k > 0) ? 1u : 0u);
+                mma_commit(smem_u32(o_full));
+                mma_commit(smem_u32(&kv_empty[s]));
+            }
+            // all MMAs issued by this thread have finished once this arrives
+            mma_commit(smem_u32(mma_done));
+            int dummy = 0;
+            mbar_wait(smem_u32(mma_done), 0, (volatile int *)&dummy, a.err);
+        }
+    } else {
+        // ---------------- softmax and accumulation: thread r owns target row t0 + r
+        const int r = threadIdx.x;  // 0..127
+        const int t = t0 + r;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        float m = -INFINITY, l = 0.f;
+        float o[D];
+#pragma unroll
+        for (int c = 0; c < D; ++c) o[c] = 0.f;
+        const uint32_t *adj_row = (a.adj && t < a.L) ? a.adj + (long long)t * a.words_per_row : nullptr;
+        uint8_t *P = smem + LY::kOffP;
+        bool ok = true;
+        for (int j = 0; j < n_steps; ++j) {
+            // sources of this step that exist and are not padding (one bit per column, one word per warp)
+            const int sc = j * kTN + r;
+            bool col_ok = sc < a.S;
+            if (col_ok && a.kpm) col_ok = a.kpm[(long long)b * a.S + sc] == 0;
+            const unsigned wbits = __ballot_sync(0xffffffffu, col_ok);
+            if (lane == 0) words[(j & 1) * 4 + warp] = wbits;
+            uint32_t rowbits[4];
+            if (a.adj) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const long long wi = (long long)j * 4 + w;
+                    rowbits[w] = (adj_row && wi < a.words_per_row) ? adj_row[wi] : 0u;
+                }
+            }
+            softmax_sync();
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t cw = words[(j & 1) * 4 + w];
+                rowbits[w] = a.adj ? (rowbits[w] & cw) : cw;
+            }
+
+            ok = !softmax_vote(!mbar_wait(smem_u32(s_full), j & 1, abort_flag, a.err));
+            if (!ok) break;
+            tc_fence_after();
+            // pass 1: the step's row max
+            float mx = -INFINITY;
+            uint32_t rb0 = rowbits[0], rb1 = rowbits[1], rb2 = rowbits[2], rb3 = rowbits[3];
+#pragma unroll 1
+            for (int c = 0; c < kTN / 32; ++c) {
+                const uint32_t bits = rb0;  // the 4 words rotate through rb0
+                rb0 = rb1;
+                rb1 = rb2;
+                rb2 = rb3;
+                uint32_t v[32];
+                tmem_ld32(tmem_s + lane_off + (uint32_t)(c * 32), v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if ((bits >> i) & 1u) mx = fmaxf(mx, __fmul_rn(__uint_as_float(v[i]), a.score_scale));
+            }
+            const float m_new = fmaxf(m, mx);
+            // ex2.approx(-inf) is +0: masked columns add nothing; the offset 0
+            // stands in for a max that is still -inf (no live source yet)
+            const float m_off = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = ex2_approx(__fsub_rn(m, m_off));
+            // pass 2: P = 2^(s - m) in fp16 into the swizzled A tile, and the row sum
+            float sum = 0.f;
+            rb0 = rowbits[0];
+            rb1 = rowbits[1];
+            rb2 = rowbits[2];
+            rb3 = rowbits[3];
+#pragma unroll 1
+            for (int c = 0; c < kTN / 32; ++c) {
+                const uint32_t bits = rb0;
+                rb0 = rb1;
+                rb1 = rb2;
+                rb2 = rb3;
+                uint32_t v[32];
+                tmem_ld32(tmem_s + lane_off + (uint32_t)(c * 32), v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float x0 = ((bits >> (2 * i)) & 1u)
+                                         ? __fmul_rn(__uint_as_float(v[2 * i]), a.score_scale)
+                                         : -INFINITY;
+                    const float x1 = ((bits >> (2 * i + 1)) & 1u)
+                                         ? __fmul_rn(__uint_as_float(v[2 * i + 1]), a.score_scale)
+                                         : -INFINITY;
+                    const float p0 = ex2_approx(__fsub_rn(x0, m_off)), p1 = ex2_approx(__fsub_rn(x1, m_off));
+                    sum = __fadd_rn(__fadd_rn(sum, p0), p1);
+                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
+                }
+                // columns c*32 .. c*32+31 = chunk c/2, 16-byte units 4*(c%2) .. +3
+                uint8_t *rowp = P + (c >> 1) * (kTM * 128) + r * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int u = (c & 1) * 4 + q;
+                    *reinterpret_cast<uint4 *>(rowp + ((u ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            // S has been read: the MMA warp may overwrite it; P is ready for the tensor cores
+            tc_fence_before();
+            mbar_arrive(smem_u32(s_free));
+            fence_async_shared();
+            mbar_arrive(smem_u32(p_full));
+            l = __fadd_rn(__fmul_rn(l, alpha), sum);
+            m = m_new;
+
+            ok = !softmax_vote(!mbar_wait(smem_u32(o_full), j & 1, abort_flag, a.err));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem_o + lane_off + (uint32_t)(c * 32), v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[c * 32 + i] = __fmaf_rn(o[c * 32 + i], alpha, __uint_as_float(v[i]));
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(o_free));
+        }
+        if (ok && t < a.L) {
+            // mixed = O / l (a target without a live source mixes to zeros)
+            const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
+            __half *dst = a.mixed + ((long long)b * a.L + t) * a.E + h * D;
+            bool bad = false;
+#pragma unroll
+            for (int c = 0; c < D; c += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float v0 = __fmul_rn(o[c + 2 * i], inv), v1 = __fmul_rn(o[c + 2 * i + 1], inv);
+                    if (!(fabsf(v0) <= 65504.f) || !(fabsf(v1) <= 65504.f)) bad = true;
+                    const __half2 hv = __floats2half2_rn(v0, v1);
+                    w[i] = *reinterpret_cast<const uint32_t *>(&hv);
+                }
+                *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (bad) atomicOr(a.err, kErrRangeBit);
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // let the copies this CTA started land before its shared memory goes away
+        int dummy = 0;
+        if (issued[0]) mbar_wait(smem_u32(q_full), 0, (volatile int *)&dummy, a.err);
+        for (int s = 0; s < 2; ++s)
+            if (issued[1 + s] > 0)
+                mbar_wait(smem_u32(&kv_full[s]), (uint32_t)((issued[1 + s] - 1) & 1), (volatile int *)&dummy,
+                          a.err);
+    }
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// V (B*S rows of pitch v_ld, E channels) -> V^T (E rows, B*S_pad columns;
+// sample b at columns b*S_pad.., its padding columns zero): 32 x 32 tiles
+// through shared memory.
+__global__ void k_transpose_v(const __half *__restrict__ v, long long v_ld, int S, int S_pad, long long cols, int E,
+                              __half *__restrict__ vt)
+{
+    __shared__ __half tile[32][33];
+    const long long r0 = (long long)blockIdx.x * 32;  // padded token index
+    const int c0 = blockIdx.y * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    for (int i = ty; i < 32; i += 8) {
+        const long long r = r0 + i;
+        const long long b = r / S_pad, s = r - b * S_pad;
+        tile[i][tx] = (r < cols && s < S && c0 + tx < E) ? v[(b * S + s) * v_ld + c0 + tx] : __float2half_rn(0.f);
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int c = c0 + i;
+        const long long r = r0 + tx;
+        if (c < E && r < cols) vt[(long long)c * cols + r] = tile[tx][i];
+    }
+}
+
+template <int D>
+pmha_status launch_dense(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mvt, const DenseArgs &a,
+                         cudaStream_t s)
+{
+    using LY = DenseLayout<D>;
+    static std::mutex mu;
+    static std::set<int> configured;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!configured.count(dev)) {
+            PMHA_CUDA_TRY(
+                cudaFuncSetAttribute(k_dense_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmem));
+            configured.insert(dev);
+        }
+    }
+    const long long grid = (long long)a.B * a.H * a.n_tiles_t;
+    k_dense_attn<D><<<(unsigned)grid, kThreads, LY::kSmem, s>>>(mq, mk, mvt, a);
+    return PMHA_OK;
+}
+
+}  // namespace
+
+bool dense_supported(const pmha_graph *g, int64_t E, int64_t H, TcType t)
+{
+    if (!g->dense || t != TcType::F16 || H < 1 || E % H) return false;
+    const int64_t d = E / H;
+    return d == 64 || d == 128;
+}
+
+static int64_t s_pad(const pmha_graph *g) { return (g->S + 7) / 8 * 8; }
+
+size_t dense_vt_bytes(const pmha_graph *g, int64_t B, int64_t E) { return (size_t)(B * s_pad(g) * E) * 2; }
+
+pmha_status dense_attention(const pmha_graph *g, const DenseInputs &in, cudaStream_t s)
+{
+    const int64_t E = in.E, H = in.H, d = E / H, B = in.B, L = g->L, S = g->S, SP = s_pad(g);
+    if (B * SP > 0x7fffffffLL || B * L > 0x7fffffffLL) {
+        set_error("dense attention: more than 2^31 token rows");
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    {
+        StageTimer timer("transpose_v", s);
+        dim3 grid((unsigned)((B * SP + 31) / 32), (unsigned)((E + 31) / 32));
+        k_transpose_v<<<grid, dim3(32, 8), 0, s>>>((const __half *)in.v, in.v_ld, (int)S, (int)SP, B * SP, (int)E,
+                                                   (__half *)in.vt);
+        count_launch();
+        PMHA_CUDA_TRY(cudaGetLastError());
+    }
+    CUtensorMap mq, mk, mvt;
+    if (!make_map_box(&mq, in.q, B * L, E, in.q_ld, false, 64, kTM) ||
+        !make_map_box(&mk, in.k, B * S, E, in.k_ld, false, 64, kTN) ||
+        !make_map_box(&mvt, in.vt, E, B * SP, B * SP, false, 64, (uint32_t)d)) {
+        set_error("dense attention: cuTensorMapEncodeTiled failed");
+        return PMHA_ERR_CUDA;
+    }
+    DenseArgs a;
+    a.B = (int)B;
+    a.L = (int)L;
+    a.S = (int)S;
+    a.S_pad = (int)SP;
+    a.H = (int)H;
+    a.n_tiles_t = (int)((L + kTM - 1) / kTM);
+    a.score_scale = (float)(1.4426950408889634 / sqrt((double)d));
+    a.adj = g->dense_complete ? nullptr : g->adj;
+    a.words_per_row = g->adj_words_per_row;
+    a.kpm = in.kpm;
+    a.mixed = (__half *)in.mixed;
+    a.E = (int)E;
+    a.err = device_error_word();
+    if (!a.err) return PMHA_ERR_CUDA;
+    StageTimer timer("dense_attn", s);
+    const pmha_status st = d == 64 ? launch_dense<64>(mq, mk, mvt, a, s) : launch_dense<128>(mq, mk, mvt, a, s);
+    if (st != PMHA_OK) return st;
+    count_launch();
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+}  // namespace pmha

@@ -40,6 +40,12 @@ struct pmha_graph {
     int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
     int32_t *unit_first_t = nullptr;  // n_units, target of each unit's first position
     int32_t *merge_t = nullptr;       // n_merge, targets to merge (crossing a unit boundary, or without edges)
+    // Dense graphs (most (target, source) pairs are edges): the adjacency as
+    // bits, row t = words [t * adj_words_per_row, ...), bit s % 32 of word s / 32.
+    bool dense = false;               // the masked-dense kernel may run this graph
+    bool dense_complete = false;      // every pair is an edge: no mask needed
+    uint32_t *adj = nullptr;          // L * adj_words_per_row words (own allocation), or null
+    int64_t adj_words_per_row = 0;
     void *mem = nullptr;              // the single allocation behind the arrays above
 };
 
@@ -121,6 +127,27 @@ struct EdgeArgs {
 bool edge_supported(int64_t E, int64_t H, TcType t);
 pmha_status edge_attention(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
 pmha_status split_merge(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------- dense graphs
+struct DenseInputs {
+    const void *q;   // (B, L) fp16 rows of pitch q_ld, head h at columns h*d..
+    int64_t q_ld;
+    const void *k;   // (B, S) fp16 rows of pitch k_ld
+    int64_t k_ld;
+    const void *v;   // (B, S) fp16 rows of pitch v_ld
+    int64_t v_ld;
+    void *vt;        // workspace: E x (B * S) fp16, V transposed
+    void *mixed;     // (B, L, E) fp16 output of the mix
+    const uint8_t *kpm;  // (B, S) key_padding_mask or null
+    int64_t B, E, H;
+};
+// The tensor-core path for dense graphs applies: the graph was built dense,
+// fp16 intermediates, head_dim 64 or 128.
+bool dense_supported(const pmha_graph *g, int64_t E, int64_t H, TcType t);
+size_t dense_vt_bytes(const pmha_graph *g, int64_t B, int64_t E);
+// Steps 2-4 for every target of a dense graph: V transposed, then the
+// masked-dense tile kernel writes `mixed`.
+pmha_status dense_attention(const pmha_graph *g, const DenseInputs &in, cudaStream_t s);
 // weights[b, e(, h)] from raw scores and (m, l); in place when out == scores.
 pmha_status weights_finalize(const pmha_graph *g, const EdgeArgs &a, pmha_wmode mode, float *out,
                              cudaStream_t s);
