@@ -33,7 +33,7 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
-WORKLOAD_ID = 3
+WORKLOAD_ID = 3  # default: the skewed n = 20,000 workload (--workload picks another)
 METRIC = "edge·head·sample scores/s and layer fwd µs at n=20k; % HBM / tensor roofline"
 UNIT = "scores/s"
 FLUSH_BYTES = 512 << 20
@@ -62,20 +62,37 @@ def algorithmic_bytes(stage: str, w: synth.Workload, B: int, nnz: int) -> float 
                 + B * L * E * bf        # mixed, written
                 + nnz * 4               # source index per CSR position
                 + (L + 1) * 4)          # row pointers
+    if stage == "dense_attn":
+        return B * L * E * bf + B * S * 2 * E * bf + B * L * E * bf  # q, k, v^T once; mixed
+    if stage == "transpose_v":
+        return 2 * B * S * E * bf
     if stage == "proj_qkv":
         return B * L * E * bf + 3 * E * E * bf + B * L * 3 * E * bf
+    if stage == "proj_q":
+        return B * L * E * bf + E * E * bf + B * L * E * bf
+    if stage == "proj_kv":
+        return B * S * E * bf + 2 * E * E * bf + B * S * 2 * E * bf
     if stage == "out_proj":
         return B * L * E * bf + E * E * bf + B * L * E * bf
     return None
 
 
 def stage_flops(stage: str, w: synth.Workload, B: int) -> float | None:
-    E, L = w.embed_dim, w.query_features
+    E, L, S = w.embed_dim, w.query_features, w.key_features
     if stage == "proj_qkv":
         return 2.0 * B * L * E * 3 * E
+    if stage == "proj_q":
+        return 2.0 * B * L * E * E
+    if stage == "proj_kv":
+        return 2.0 * B * S * E * 2 * E
     if stage == "out_proj":
         return 2.0 * B * L * E * E
+    if stage == "dense_attn":
+        return 4.0 * B * L * S * E  # Q K^T and P V over every (target, source) pair and head
     return None
+
+
+TENSOR_BOUND = {"dense_attn"}  # stages whose roofline is the tensor pipe, not HBM
 
 
 def source_digest(paths) -> str:
@@ -88,8 +105,9 @@ def source_digest(paths) -> str:
 
 KERNEL_SOURCES = {
     "edge_attn": ["graph_sparse_head_gb300/csrc/edge_stream.cuh", "graph_sparse_head_gb300/csrc/edge_attn_f16.cu"],
-    "proj_qkv": ["graph_sparse_head_gb300/csrc/gemm_tc.cu"],
-    "out_proj": ["graph_sparse_head_gb300/csrc/gemm_tc.cu"],
+    "proj_qkv": ["graph_sparse_head_gb300/csrc/gemm_tc.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
+    "out_proj": ["graph_sparse_head_gb300/csrc/gemm_tc.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
+    "dense_attn": ["graph_sparse_head_gb300/csrc/dense_attn.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
 }
 
 
@@ -176,12 +194,16 @@ def shard_seed(rank: int) -> int:
 
 
 def make_rank_inputs(rank: int, batch: int):
+    """(query tokens, key/value tokens, params); key/value is the query for
+    attention within one graph."""
     w = synth.workload(WORKLOAD_ID)
-    xq, _, params = synth.make_inputs(WORKLOAD_ID, batch)
+    xq, xkv, params = synth.make_inputs(WORKLOAD_ID, batch)
     if shard_seed(rank):
         rng = np.random.default_rng([1000 + WORKLOAD_ID, shard_seed(rank)])
         xq = synth.make_tokens(rng, batch, w.query_features, w.embed_dim, w.dtype)
-    return xq, params
+        if xkv is not None:
+            xkv = synth.make_tokens(rng, batch, w.key_features, w.embed_dim, w.dtype)
+    return xq, (xq if xkv is None else xkv), params
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -196,16 +218,16 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def run_cpu_baseline(budget_s: float, src, tgt, w, xq, params):
+def run_cpu_baseline(budget_s: float, src, tgt, w, xq, xkv, params):
     """The oracle as it stands, on whole samples of the workload, until about
     budget_s seconds of CPU time have passed (at least one sample)."""
     import oracle
     cores = oracle.num_threads()
     done, t_total = 0, 0.0
     while done < xq.shape[0]:
-        x = xq[done:done + 1]
+        x, kv = xq[done:done + 1], xkv[done:done + 1]
         t0 = time.perf_counter()
-        oracle.forward(x, x, x, params, src, tgt, w.num_heads, need_weights=False)
+        oracle.forward(x, kv, kv, params, src, tgt, w.num_heads, need_weights=False)
         t_total += time.perf_counter() - t0
         done += 1
         if t_total >= budget_s:
@@ -222,16 +244,16 @@ def bench_reference(args):
         return 0
     w = synth.workload(WORKLOAD_ID)
     src, tgt = synth.make_graph(WORKLOAD_ID)
-    xq, params = make_rank_inputs(0, w.batch)
+    xq, xkv, params = make_rank_inputs(0, w.batch)
     import oracle
     oracle.build()
     cores = oracle.num_threads()
     times = []
     for i in range(args.warmup + args.steps):
         b = i % w.batch
-        x = xq[b:b + 1]
+        x, kv = xq[b:b + 1], xkv[b:b + 1]
         t0 = time.perf_counter()
-        oracle.forward(x, x, x, params, src, tgt, w.num_heads, need_weights=False)
+        oracle.forward(x, kv, kv, params, src, tgt, w.num_heads, need_weights=False)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -268,19 +290,21 @@ def bench_ours(args):
     w = synth.workload(WORKLOAD_ID)
     B = w.batch
     src, tgt = synth.make_graph(WORKLOAD_ID)
-    xq_np, prm = make_rank_inputs(rank, B)
+    xq_np, xkv_np, prm = make_rank_inputs(rank, B)
+    self_attn = xkv_np is xq_np
     params = pmha.Params.from_arrays(prm, w.num_heads, torch.bfloat16, dev)
     graph = pmha.pmha_build_csr(torch.from_numpy(src).to(dev), torch.from_numpy(tgt).to(dev),
                                 w.query_features, w.key_features)
     nnz, H = graph.nnz, w.num_heads
     x = torch.from_numpy(xq_np).to(torch.bfloat16).to(dev)
+    kv = x if self_attn else torch.from_numpy(xkv_np).to(torch.bfloat16).to(dev)
     out = torch.empty_like(x)
     ws = torch.empty(pmha.pmha_forward_workspace_size(graph, params, B, "none"), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        pmha.pmha_forward(graph, params, x, x, x, "none", out=out, workspace=ws, stream=stream)
+        pmha.pmha_forward(graph, params, x, kv, kv, "none", out=out, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -326,7 +350,8 @@ def bench_ours(args):
     kpm = torch.from_numpy(synth.padding_mask(np.random.default_rng(7 + rank), B, w.key_features)).to(dev)
     masked_steps = max(3, min(args.steps, 100))
     for _ in range(3):
-        pmha.pmha_forward(graph, params, x, x, x, "none", out=out, workspace=ws, stream=stream, key_padding_mask=kpm)
+        pmha.pmha_forward(graph, params, x, kv, kv, "none", out=out, workspace=ws, stream=stream,
+                          key_padding_mask=kpm)
     pmha.pmha_device_status()
     pmha.pmha_profile_enable(True)
     pmha.pmha_profile_read()
@@ -334,7 +359,8 @@ def bench_ours(args):
     for i, (e_start, e_end) in enumerate(m_ev):
         flush.fill_(i & 0xFF)
         e_start.record(stream)
-        pmha.pmha_forward(graph, params, x, x, x, "none", out=out, workspace=ws, stream=stream, key_padding_mask=kpm)
+        pmha.pmha_forward(graph, params, x, kv, kv, "none", out=out, workspace=ws, stream=stream,
+                          key_padding_mask=kpm)
         e_end.record(stream)
     torch.cuda.synchronize()
     pmha.pmha_profile_enable(False)
@@ -349,22 +375,23 @@ def bench_ours(args):
     # ---- end to end through the C ABI with host buffers (pinned), per step:
     # copy the step's tokens in, run, copy the output back
     xh = torch.from_numpy(xq_np).to(torch.bfloat16).pin_memory()
+    kvh = xh if self_attn else torch.from_numpy(xkv_np).to(torch.bfloat16).pin_memory()
     oh = torch.empty_like(xh).pin_memory()
     ws_h = torch.empty(pmha.pmha_forward_host_workspace_size(graph, params, B, "none"), dtype=torch.uint8,
                        device=dev)
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
-        pmha.pmha_forward_host(graph, params, xh, xh, xh, oh, "none", workspace=ws_h, stream=stream)
+        pmha.pmha_forward_host(graph, params, xh, kvh, kvh, oh, "none", workspace=ws_h, stream=stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        pmha.pmha_forward_host(graph, params, xh, xh, xh, oh, "none", workspace=ws_h, stream=stream)
+        pmha.pmha_forward_host(graph, params, xh, kvh, kvh, oh, "none", workspace=ws_h, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e_value = world * scores / (e2e_ms / 1e3)
-    h2d = xh.numel() * xh.element_size()
+    h2d = xh.numel() * xh.element_size() + (0 if self_attn else kvh.numel() * kvh.element_size())
     d2h = oh.numel() * oh.element_size()
 
     # ---- roofline of the dominant kernel
@@ -378,7 +405,17 @@ def bench_ours(args):
     if dom is not None:
         avg_s = stages[dom]["avg_us"] / 1e6
         alg = algorithmic_bytes(dom, w, B, nnz)
-        if alg is not None:
+        fl = stage_flops(dom, w, B)
+        if dom in TENSOR_BOUND and fl is not None:
+            # timed inside a long loop of steps: the sustained tensor peak
+            achieved = fl / avg_s / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": ncu_traffic(dom), "algorithmic_flops_per_launch": fl,
+                    "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
+                    "peak_source": f"{peaks['source']} sustained bf16 GEMM (MEASURED_PEAKS.json "
+                                   "bf16_tflops_sustained; fp16 runs at the bf16 rate)"}
+        elif alg is not None:
             achieved = alg / avg_s / 1e9
             roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom),
@@ -398,7 +435,7 @@ def bench_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        cpu = run_cpu_baseline(args.cpu_seconds, src, tgt, w, xq_np, prm)
+        cpu = run_cpu_baseline(args.cpu_seconds, src, tgt, w, xq_np, xkv_np, prm)
 
     if rank == 0:
         line = {
@@ -427,6 +464,7 @@ def bench_ours(args):
 
 
 def main(argv=None):
+    global WORKLOAD_ID
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
@@ -434,7 +472,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(synth.WORKLOADS),
+                    help="synthetic workload id (default: the skewed n=20,000 graph the metric is quoted on)")
     args = ap.parse_args(argv)
+    WORKLOAD_ID = args.workload
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

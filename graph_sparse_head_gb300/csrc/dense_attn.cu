@@ -40,18 +40,18 @@ constexpr int kTmemCols = 256;
 
 template <int D>
 struct DenseLayout {
-    static constexpr int DC = D / 64;                       // 64-channel chunks of a head
-    static constexpr int kQBytes = DC * kTM * 128;           // q tile
-    static constexpr int kKBytes = DC * kTN * 128;           // k tile of one stage
-    static constexpr int kVBytes = 2 * D * 128;              // v^T tile of one stage: 2 chunks of 64 sources
-    static constexpr int kPBytes = 2 * kTM * 128;            // P: 2 chunks of 64 sources
+    static constexpr int DC = D / 64;               // 64-channel chunks of a head
+    static constexpr int kQBytes = DC * kTM * 128;   // q tile
+    static constexpr int kKBytes = DC * kTN * 128;   // k tile (two stages)
+    static constexpr int kVBytes = 2 * D * 128;      // v^T tile (one stage): 2 chunks of 64 sources
+    static constexpr int kPBytes = 2 * kTM * 128;    // P: 2 chunks of 64 sources
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + 2 * kKBytes;
-    static constexpr int kOffP = kOffV + 2 * kVBytes;
-    static constexpr int kOffWords = kOffP + kPBytes;        // uint32 [2][4] source-validity words
-    static constexpr int kOffBars = kOffWords + 64;
-    static constexpr int kSmem = kOffBars + 256 + 1024;      // + alignment slack
+    static constexpr int kOffP = kOffV + kVBytes;
+    static constexpr int kOffWords = kOffP + kPBytes;  // uint32 [2][4] source-validity words
+    static constexpr int kOffBars = kOffWords + 32;
+    static constexpr int kSmem = kOffBars + 160 + 1024;  // + alignment slack
 };
 
 struct DenseArgs {
@@ -93,9 +93,26 @@ __device__ __forceinline__ float ex2_approx(float x)
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// 32 columns of this warp's 32 TMEM lanes, without waiting for them
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// head_dim 64: two CTAs per SM (registers capped at 170 a thread); 128: one
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
 k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_vt, DenseArgs a)
 {
@@ -104,18 +121,20 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint32_t *words = (uint32_t *)(smem + LY::kOffWords);
     uint64_t *bars = (uint64_t *)(smem + LY::kOffBars);
-    uint64_t *q_full = bars;           // [1]
-    uint64_t *kv_full = bars + 1;      // [2]
-    uint64_t *kv_empty = bars + 3;     // [2]
-    uint64_t *s_full = bars + 5;       // [1]
-    uint64_t *s_free = bars + 6;       // [1]
-    uint64_t *p_full = bars + 7;       // [1]
-    uint64_t *o_full = bars + 8;       // [1]
-    uint64_t *o_free = bars + 9;       // [1]
-    uint64_t *mma_done = bars + 10;    // [1]
-    uint32_t *tmem_holder = (uint32_t *)(bars + 11);
+    uint64_t *q_full = bars;         // [1]
+    uint64_t *k_full = bars + 1;     // [2]
+    uint64_t *k_empty = bars + 3;    // [2]
+    uint64_t *v_full = bars + 5;     // [1]
+    uint64_t *v_empty = bars + 6;    // [1]
+    uint64_t *s_full = bars + 7;     // [1]
+    uint64_t *s_free = bars + 8;     // [1]
+    uint64_t *p_full = bars + 9;     // [1]
+    uint64_t *o_full = bars + 10;    // [1]
+    uint64_t *o_free = bars + 11;    // [1]
+    uint64_t *mma_done = bars + 12;  // [1]
+    uint32_t *tmem_holder = (uint32_t *)(bars + 13);
     volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
-    int *issued = (int *)(tmem_holder + 2);  // [3]: TMA phases armed (q, stage 0, stage 1)
+    int *issued = (int *)(tmem_holder + 2);  // [4]: TMA phases armed (q, k stage 0, k stage 1, v)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int it = blockIdx.x % a.n_tiles_t;
@@ -127,16 +146,18 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(q_full), 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(smem_u32(&kv_full[s]), 1);
-            mbar_init(smem_u32(&kv_empty[s]), 1);
+            mbar_init(smem_u32(&k_full[s]), 1);
+            mbar_init(smem_u32(&k_empty[s]), 1);
         }
+        mbar_init(smem_u32(v_full), 1);
+        mbar_init(smem_u32(v_empty), 1);
         mbar_init(smem_u32(s_full), 1);
         mbar_init(smem_u32(s_free), 128);
         mbar_init(smem_u32(p_full), 128);
         mbar_init(smem_u32(o_full), 1);
         mbar_init(smem_u32(o_free), 128);
         mbar_init(smem_u32(mma_done), 1);
-        issued[0] = issued[1] = issued[2] = 0;
+        issued[0] = issued[1] = issued[2] = issued[3] = 0;
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -155,27 +176,36 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
     if (warp == 4) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer: q, k_0, then per step v_j and k_{j+1}
             const uint32_t qb = smem_u32(q_full);
             mbar_arrive_expect_tx(qb, LY::kQBytes);
             issued[0] = 1;
 #pragma unroll
             for (int c = 0; c < LY::DC; ++c)
                 tma_load_2d(smem_u32(smem + LY::kOffQ + c * kTM * 128), &tm_q, h * D + c * 64, b * a.L + t0, qb);
-            for (int j = 0; j < n_steps; ++j) {
+            auto load_k = [&](int j) -> bool {
                 const int s = j & 1;
-                if (!mbar_wait(smem_u32(&kv_empty[s]), ((j >> 1) & 1) ^ 1u, abort_flag, a.err)) break;
-                const uint32_t fb = smem_u32(&kv_full[s]);
-                mbar_arrive_expect_tx(fb, LY::kKBytes + LY::kVBytes);
+                if (!mbar_wait(smem_u32(&k_empty[s]), ((j >> 1) & 1) ^ 1u, abort_flag, a.err)) return false;
+                const uint32_t fb = smem_u32(&k_full[s]);
+                mbar_arrive_expect_tx(fb, LY::kKBytes);
                 issued[1 + s] += 1;
                 const uint32_t kdst = smem_u32(smem + LY::kOffK + s * LY::kKBytes);
-                const uint32_t vdst = smem_u32(smem + LY::kOffV + s * LY::kVBytes);
 #pragma unroll
                 for (int c = 0; c < LY::DC; ++c)
                     tma_load_2d(kdst + c * kTN * 128, &tm_k, h * D + c * 64, b * a.S + j * kTN, fb);
+                return true;
+            };
+            bool ok = load_k(0);
+            for (int j = 0; ok && j < n_steps; ++j) {
+                if (!mbar_wait(smem_u32(v_empty), (j & 1) ^ 1u, abort_flag, a.err)) break;
+                const uint32_t fb = smem_u32(v_full);
+                mbar_arrive_expect_tx(fb, LY::kVBytes);
+                issued[3] += 1;
+                const uint32_t vdst = smem_u32(smem + LY::kOffV);
 #pragma unroll
                 for (int kc = 0; kc < 2; ++kc)
                     tma_load_2d(vdst + kc * D * 128, &tm_vt, b * a.S_pad + j * kTN + kc * 64, h * D, fb);
+                if (j + 1 < n_steps) ok = load_k(j + 1);
             }
         }
     } else if (warp == 5) {
@@ -185,9 +215,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_after();
             const uint32_t qa = smem_u32(smem + LY::kOffQ);
             const uint32_t pa = smem_u32(smem + LY::kOffP);
+            const uint32_t va = smem_u32(smem + LY::kOffV);
             for (int j = 0; ok && j < n_steps; ++j) {
                 const int s = j & 1;
-                if (!mbar_wait(smem_u32(&kv_full[s]), (j >> 1) & 1, abort_flag, a.err)) break;
+                if (!mbar_wait(smem_u32(&k_full[s]), (j >> 1) & 1, abort_flag, a.err)) break;
                 if (j > 0 && !mbar_wait(smem_u32(s_free), (j - 1) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(smem + LY::kOffK + s * LY::kKBytes);
@@ -199,10 +230,11 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                     smem_desc(ka + c * kTN * 128) + (uint64_t)(2 * k), idesc_f16(kTM, kTN),
                                     (c > 0 || k > 0) ? 1u : 0u);
                 mma_commit(smem_u32(s_full));
+                mma_commit(smem_u32(&k_empty[s]));
                 if (!mbar_wait(smem_u32(p_full), j & 1, abort_flag, a.err)) break;
                 if (j > 0 && !mbar_wait(smem_u32(o_free), (j - 1) & 1, abort_flag, a.err)) break;
+                if (!mbar_wait(smem_u32(v_full), j & 1, abort_flag, a.err)) break;
                 tc_fence_after();
-                const uint32_t va = smem_u32(smem + LY::kOffV + s * LY::kVBytes);
 #pragma unroll
                 for (int kc = 0; kc < 2; ++kc)
 #pragma unroll
@@ -211,7 +243,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                     smem_desc(va + kc * D * 128) + (uint64_t)(2 * k), idesc_f16(kTM, D),
                                     (kc > 0 || k > 0) ? 1u : 0u);
                 mma_commit(smem_u32(o_full));
-                mma_commit(smem_u32(&kv_empty[s]));
+                mma_commit(smem_u32(v_empty));
             }
             // all MMAs issued by this thread have finished once this arrives
             mma_commit(smem_u32(mma_done));
@@ -231,75 +263,76 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         uint8_t *P = smem + LY::kOffP;
         bool ok = true;
         for (int j = 0; j < n_steps; ++j) {
-            // sources of this step that exist and are not padding (one bit per column, one word per warp)
-            const int sc = j * kTN + r;
-            bool col_ok = sc < a.S;
-            if (col_ok && a.kpm) col_ok = a.kpm[(long long)b * a.S + sc] == 0;
-            const unsigned wbits = __ballot_sync(0xffffffffu, col_ok);
-            if (lane == 0) words[(j & 1) * 4 + warp] = wbits;
-            uint32_t rowbits[4];
-            if (a.adj) {
+            // A step whose 128 sources all exist and are all live for every row
+            // (complete graph, no padding mask, not past S) needs no mask.
+            const bool full = !a.adj && !a.kpm && (j + 1) * kTN <= a.S;
+            uint32_t rb[4] = {~0u, ~0u, ~0u, ~0u};
+            if (!full) {
+                // sources that exist and are not padding: one bit per column, one word per warp
+                const int sc = j * kTN + r;
+                bool col_ok = sc < a.S;
+                if (col_ok && a.kpm) col_ok = a.kpm[(long long)b * a.S + sc] == 0;
+                const unsigned wbits = __ballot_sync(0xffffffffu, col_ok);
+                if (lane == 0) words[(j & 1) * 4 + warp] = wbits;
+                if (a.adj) {
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const long long wi = (long long)j * 4 + w;
-                    rowbits[w] = (adj_row && wi < a.words_per_row) ? adj_row[wi] : 0u;
+                    for (int w = 0; w < 4; ++w) {
+                        const long long wi = (long long)j * 4 + w;
+                        rb[w] = (adj_row && wi < a.words_per_row) ? adj_row[wi] : 0u;
+                    }
                 }
-            }
-            softmax_sync();
+                softmax_sync();
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t cw = words[(j & 1) * 4 + w];
-                rowbits[w] = a.adj ? (rowbits[w] & cw) : cw;
+                for (int w = 0; w < 4; ++w) rb[w] &= words[(j & 1) * 4 + w];
             }
 
             ok = !softmax_vote(!mbar_wait(smem_u32(s_full), j & 1, abort_flag, a.err));
             if (!ok) break;
             tc_fence_after();
-            // pass 1: the step's row max
+            uint32_t v0[32], v1[32];
+            // pass 1: the step's row max of the raw products (the scale is positive)
             float mx = -INFINITY;
-            uint32_t rb0 = rowbits[0], rb1 = rowbits[1], rb2 = rowbits[2], rb3 = rowbits[3];
-#pragma unroll 1
-            for (int c = 0; c < kTN / 32; ++c) {
-                const uint32_t bits = rb0;  // the 4 words rotate through rb0
-                rb0 = rb1;
-                rb1 = rb2;
-                rb2 = rb3;
-                uint32_t v[32];
-                tmem_ld32(tmem_s + lane_off + (uint32_t)(c * 32), v);
+            tmem_ld32_async(tmem_s + lane_off, v0);
+            tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if ((bits >> i) & 1u) mx = fmaxf(mx, __fmul_rn(__uint_as_float(v[i]), a.score_scale));
+            for (int c = 0; c < kTN / 32; ++c) {
+                uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
+                uint32_t(&nxt)[32] = (c & 1) ? v0 : v1;
+                if (c + 1 < kTN / 32) tmem_ld32_async(tmem_s + lane_off + (uint32_t)((c + 1) * 32), nxt);
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float x = __uint_as_float(cur[i]);
+                    m4[i & 3] = fmaxf(m4[i & 3], full ? x : (((rb[c] >> i) & 1u) ? x : -INFINITY));
+                }
+                mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                if (c + 1 < kTN / 32) tmem_wait_ld();
             }
-            const float m_new = fmaxf(m, mx);
+            const float m_new = fmaxf(m, __fmul_rn(mx, a.score_scale));
             // ex2.approx(-inf) is +0: masked columns add nothing; the offset 0
             // stands in for a max that is still -inf (no live source yet)
             const float m_off = m_new == -INFINITY ? 0.f : m_new;
             const float alpha = ex2_approx(__fsub_rn(m, m_off));
-            // pass 2: P = 2^(s - m) in fp16 into the swizzled A tile, and the row sum
-            float sum = 0.f;
-            rb0 = rowbits[0];
-            rb1 = rowbits[1];
-            rb2 = rowbits[2];
-            rb3 = rowbits[3];
-#pragma unroll 1
+            // pass 2: P = 2^(s * scale - m) in fp16 into the swizzled A tile, and the row sum
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            tmem_ld32_async(tmem_s + lane_off, v0);
+            tmem_wait_ld();
+#pragma unroll
             for (int c = 0; c < kTN / 32; ++c) {
-                const uint32_t bits = rb0;
-                rb0 = rb1;
-                rb1 = rb2;
-                rb2 = rb3;
-                uint32_t v[32];
-                tmem_ld32(tmem_s + lane_off + (uint32_t)(c * 32), v);
+                uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
+                uint32_t(&nxt)[32] = (c & 1) ? v0 : v1;
+                if (c + 1 < kTN / 32) tmem_ld32_async(tmem_s + lane_off + (uint32_t)((c + 1) * 32), nxt);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float x0 = ((bits >> (2 * i)) & 1u)
-                                         ? __fmul_rn(__uint_as_float(v[2 * i]), a.score_scale)
-                                         : -INFINITY;
-                    const float x1 = ((bits >> (2 * i + 1)) & 1u)
-                                         ? __fmul_rn(__uint_as_float(v[2 * i + 1]), a.score_scale)
-                                         : -INFINITY;
-                    const float p0 = ex2_approx(__fsub_rn(x0, m_off)), p1 = ex2_approx(__fsub_rn(x1, m_off));
-                    sum = __fadd_rn(__fadd_rn(sum, p0), p1);
+                    float p0 = ex2_approx(__fmaf_rn(__uint_as_float(cur[2 * i]), a.score_scale, -m_off));
+                    float p1 = ex2_approx(__fmaf_rn(__uint_as_float(cur[2 * i + 1]), a.score_scale, -m_off));
+                    if (!full) {
+                        p0 = ((rb[c] >> (2 * i)) & 1u) ? p0 : 0.f;
+                        p1 = ((rb[c] >> (2 * i + 1)) & 1u) ? p1 : 0.f;
+                    }
+                    sum4[(2 * i) & 3] = __fadd_rn(sum4[(2 * i) & 3], p0);
+                    sum4[(2 * i + 1) & 3] = __fadd_rn(sum4[(2 * i + 1) & 3], p1);
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
@@ -311,12 +344,14 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     *reinterpret_cast<uint4 *>(rowp + ((u ^ (r & 7)) << 4)) =
                         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
+                if (c + 1 < kTN / 32) tmem_wait_ld();
             }
             // S has been read: the MMA warp may overwrite it; P is ready for the tensor cores
             tc_fence_before();
             mbar_arrive(smem_u32(s_free));
             fence_async_shared();
             mbar_arrive(smem_u32(p_full));
+            const float sum = __fadd_rn(__fadd_rn(sum4[0], sum4[1]), __fadd_rn(sum4[2], sum4[3]));
             l = __fadd_rn(__fmul_rn(l, alpha), sum);
             m = m_new;
 
@@ -325,10 +360,11 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_after();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem_o + lane_off + (uint32_t)(c * 32), v);
+                uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
+                tmem_ld32_async(tmem_o + lane_off + (uint32_t)(c * 32), cur);
+                tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[c * 32 + i] = __fmaf_rn(o[c * 32 + i], alpha, __uint_as_float(v[i]));
+                for (int i = 0; i < 32; ++i) o[c * 32 + i] = __fmaf_rn(o[c * 32 + i], alpha, __uint_as_float(cur[i]));
             }
             tc_fence_before();
             mbar_arrive(smem_u32(o_free));
@@ -343,9 +379,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float v0 = __fmul_rn(o[c + 2 * i], inv), v1 = __fmul_rn(o[c + 2 * i + 1], inv);
-                    if (!(fabsf(v0) <= 65504.f) || !(fabsf(v1) <= 65504.f)) bad = true;
-                    const __half2 hv = __floats2half2_rn(v0, v1);
+                    const float x0 = __fmul_rn(o[c + 2 * i], inv), x1 = __fmul_rn(o[c + 2 * i + 1], inv);
+                    if (!(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f)) bad = true;
+                    const __half2 hv = __floats2half2_rn(x0, x1);
                     w[i] = *reinterpret_cast<const uint32_t *>(&hv);
                 }
                 *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -361,8 +397,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (issued[0]) mbar_wait(smem_u32(q_full), 0, (volatile int *)&dummy, a.err);
         for (int s = 0; s < 2; ++s)
             if (issued[1 + s] > 0)
-                mbar_wait(smem_u32(&kv_full[s]), (uint32_t)((issued[1 + s] - 1) & 1), (volatile int *)&dummy,
+                mbar_wait(smem_u32(&k_full[s]), (uint32_t)((issued[1 + s] - 1) & 1), (volatile int *)&dummy,
                           a.err);
+        if (issued[3] > 0)
+            mbar_wait(smem_u32(v_full), (uint32_t)((issued[3] - 1) & 1), (volatile int *)&dummy, a.err);
     }
     __syncthreads();
     if (warp == 5) {
@@ -373,25 +411,41 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 }
 
 // V (B*S rows of pitch v_ld, E channels) -> V^T (E rows, B*S_pad columns;
-// sample b at columns b*S_pad.., its padding columns zero): 32 x 32 tiles
-// through shared memory.
-__global__ void k_transpose_v(const __half *__restrict__ v, long long v_ld, int S, int S_pad, long long cols, int E,
-                              __half *__restrict__ vt)
+// sample b at columns b*S_pad.., its padding columns zero). 64 x 64 tiles:
+// 16-byte loads of 8 channels, a shared tile with a 66-element pitch (the
+// transposed reads hit 8 different banks), 16-byte stores of 8 tokens.
+// E, v_ld and S_pad are multiples of 8.
+__global__ void __launch_bounds__(256) k_transpose_v(const __half *__restrict__ v, long long v_ld, int S, int S_pad,
+                                                     long long cols, int E, __half *__restrict__ vt)
 {
-    __shared__ __half tile[32][33];
-    const long long r0 = (long long)blockIdx.x * 32;  // padded token index
-    const int c0 = blockIdx.y * 32;
-    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-    for (int i = ty; i < 32; i += 8) {
-        const long long r = r0 + i;
+    __shared__ __half tile[64][66];
+    const long long r0 = (long long)blockIdx.x * 64;  // padded token index
+    const int c0 = blockIdx.y * 64;                    // channel
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int idx = t + 256 * k;
+        const int row = idx >> 3, cu = idx & 7;
+        const long long r = r0 + row;
         const long long b = r / S_pad, s = r - b * S_pad;
-        tile[i][tx] = (r < cols && s < S && c0 + tx < E) ? v[(b * S + s) * v_ld + c0 + tx] : __float2half_rn(0.f);
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r < cols && s < S && c0 + cu * 8 < E)
+            val = *reinterpret_cast<const uint4 *>(v + (b * S + s) * v_ld + c0 + cu * 8);
+        const __half *hv = reinterpret_cast<const __half *>(&val);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tile[row][cu * 8 + i] = hv[i];
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-        const int c = c0 + i;
-        const long long r = r0 + tx;
-        if (c < E && r < cols) vt[(long long)c * cols + r] = tile[tx][i];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int idx = t + 256 * k;
+        const int ch = idx >> 3, tu = idx & 7;
+        __align__(16) __half hv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hv[i] = tile[tu * 8 + i][ch];
+        const long long r = r0 + tu * 8;
+        if (c0 + ch < E && r < cols)
+            *reinterpret_cast<uint4 *>(vt + (long long)(c0 + ch) * cols + r) = *reinterpret_cast<const uint4 *>(hv);
     }
 }
 
@@ -439,9 +493,9 @@ pmha_status dense_attention(const pmha_graph *g, const DenseInputs &in, cudaStre
     }
     {
         StageTimer timer("transpose_v", s);
-        dim3 grid((unsigned)((B * SP + 31) / 32), (unsigned)((E + 31) / 32));
-        k_transpose_v<<<grid, dim3(32, 8), 0, s>>>((const __half *)in.v, in.v_ld, (int)S, (int)SP, B * SP, (int)E,
-                                                   (__half *)in.vt);
+        dim3 grid((unsigned)((B * SP + 63) / 64), (unsigned)((E + 63) / 64));
+        k_transpose_v<<<grid, 256, 0, s>>>((const __half *)in.v, in.v_ld, (int)S, (int)SP, B * SP, (int)E,
+                                           (__half *)in.vt);
         count_launch();
         PMHA_CUDA_TRY(cudaGetLastError());
     }

@@ -24,7 +24,7 @@ def _worker(rank, world, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
     w, r, local = bench.dist_env()
-    xq, params = bench.make_rank_inputs(r, 1)
+    xq, _, params = bench.make_rank_inputs(r, 1)
     step_ms = 1.0 + r  # rank 1 is slower
     out[r] = (w, r, float(xq[0, :4, :4].sum()), bench.max_over_ranks(step_ms, w))
     dist.barrier()
@@ -44,6 +44,21 @@ def test_two_ranks_own_batches_and_max_time():
 def test_rank0_tokens_are_the_workload_tokens():
     import bench
     import synth
-    xq, _ = bench.make_rank_inputs(0, 2)
+    xq, kv, _ = bench.make_rank_inputs(0, 2)
     ref, _, _ = synth.make_inputs(bench.WORKLOAD_ID, 2)
     assert np.array_equal(xq, ref)
+    assert kv is xq  # attention within one graph: key/value are the query tokens
+
+
+def test_bipartite_workload_has_its_own_key_tokens():
+    import bench
+    import synth
+    saved = bench.WORKLOAD_ID
+    try:
+        bench.WORKLOAD_ID = 4
+        xq, kv, _ = bench.make_rank_inputs(1, 1)
+        w = synth.workload(4)
+        assert xq.shape == (1, w.query_features, w.embed_dim)
+        assert kv.shape == (1, w.key_features, w.embed_dim)
+    finally:
+        bench.WORKLOAD_ID = saved
