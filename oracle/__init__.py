@@ -68,6 +68,10 @@ def _load():
         lib.oracle_forward_masked.restype = ctypes.c_int
         lib.oracle_attend_masked.argtypes = [_i64, _i64, _D, _i64, _D, _D, _U8, _D, _D]
         lib.oracle_attend_masked.restype = ctypes.c_int
+        lib.oracle_linear_backward.argtypes = [_i64, _i64, _i64, _D, _D, _D, _D, _D, _D]
+        lib.oracle_linear_backward.restype = None
+        lib.oracle_backward.argtypes = ([_i64] * 5 + [_D] * 11 + [_i64, _I64, _I64, _U8] + [_D] * 12)
+        lib.oracle_backward.restype = ctypes.c_int
         lib.oracle_average_heads.argtypes = [_i64, _i64, _D, _D]
         lib.oracle_average_heads.restype = None
         lib.oracle_num_threads.argtypes = []
@@ -213,6 +217,55 @@ def forward_rows(query, key, value, params: dict, source_index, target_index, nu
         out = linear(mixed, params["wo"], params.get("bo"))
         res.append((out, e_ids, w))
     return res
+
+
+def linear_backward(x, w, dy):
+    """Gradients of Y = X W^T + b: returns (dX, dW, db)."""
+    x, w, dy = _f64(x), _f64(w), _f64(dy)
+    out_dim, in_dim = w.shape
+    rows = x.size // in_dim
+    dx = np.empty(x.shape, np.float64)
+    dw = np.empty((out_dim, in_dim), np.float64)
+    db = np.empty(out_dim, np.float64)
+    _load().oracle_linear_backward(rows, in_dim, out_dim, _dp(x), _dp(w), _dp(dy), _dp(dx), _dp(dw), _dp(db))
+    return dx, dw, db
+
+
+def backward(query, key, value, params: dict, source_index, target_index, num_heads: int, dout,
+             key_padding_mask=None) -> dict:
+    """Gradients of sum(output * dout) for the forward of ``forward``: one
+    gradient per input (dquery, dkey, dvalue; add them when inputs are one
+    tensor), dwq..dwo and dbq..dbo (None when the layer has no bias)."""
+    q, k, v = _f64(query), _f64(key), _f64(value)
+    B, L, E = q.shape
+    S = k.shape[1]
+    s, t = _i64a(source_index), _i64a(target_index)
+    p = {n: (None if params.get(n) is None else _f64(params[n]))
+         for n in ("wq", "bq", "wk", "bk", "wv", "bv", "wo", "bo")}
+    g = _f64(dout)
+    if g.shape != (B, L, E):
+        raise ValueError(f"dout must be ({B}, {L}, {E})")
+    mk = _mask(key_padding_mask)
+    if mk is not None and mk.shape != (B, S):
+        raise ValueError(f"key_padding_mask must be ({B}, {S})")
+    r = {"dquery": np.empty((B, L, E)), "dkey": np.empty((B, S, E)), "dvalue": np.empty((B, S, E))}
+    for n in ("wq", "wk", "wv", "wo"):
+        r["d" + n] = np.empty((E, E))
+    for n in ("bq", "bk", "bv", "bo"):
+        r["d" + n] = np.empty(E)
+    st = _load().oracle_backward(B, L, S, E, num_heads, _dp(q), _dp(k), _dp(v),
+                                 _dp(p["wq"]), _dp(p["bq"]), _dp(p["wk"]), _dp(p["bk"]),
+                                 _dp(p["wv"]), _dp(p["bv"]), _dp(p["wo"]), _dp(p["bo"]),
+                                 s.size, _ip(s), _ip(t), _mp(mk), _dp(g),
+                                 _dp(r["dquery"]), _dp(r["dkey"]), _dp(r["dvalue"]),
+                                 _dp(r["dwq"]), _dp(r["dbq"]), _dp(r["dwk"]), _dp(r["dbk"]),
+                                 _dp(r["dwv"]), _dp(r["dbv"]), _dp(r["dwo"]), _dp(r["dbo"]))
+    if st != OK:
+        raise ValueError(f"oracle_backward status {st}")
+    for n in ("bq", "bk", "bv", "bo"):
+        if p[n] is None:
+            r["d" + n] = None
+    return r
 
 
 def average_heads(w_head) -> np.ndarray:

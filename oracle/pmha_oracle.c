@@ -335,6 +335,242 @@ int oracle_forward(int64_t batch, int64_t query_features, int64_t key_features,
 
 /* Mean over heads of per-head weights: kpnn2 forward(), average_attn_weights
  * (True averages the weights over the heads). w_head is (rows, H); w_avg (rows). */
+/* ------------------------------------------------------------------------ */
+/* Backward of one nn.Linear layer (the projections of Notes step 1 and      */
+/* out_proj of step 5): for Y = X W^T + b and a gradient dY of Y,            */
+/*   dX[r, i] = sum_o dY[r, o] * W[o, i]                                     */
+/*   dW[o, i] = sum_r dY[r, o] * X[r, i]                                     */
+/*   db[o]    = sum_r dY[r, o]                                               */
+/* Any of dX, dW, db may be NULL. Sums run over r in increasing order.       */
+/* ------------------------------------------------------------------------ */
+
+void oracle_linear_backward(int64_t rows, int64_t in_dim, int64_t out_dim, const double *X,
+                            const double *W, const double *dY, double *dX, double *dW, double *db)
+{
+    if (dX) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t i = 0; i < in_dim; ++i) {
+                double acc = 0.0;
+                for (int64_t o = 0; o < out_dim; ++o) acc += dY[r * out_dim + o] * W[o * in_dim + i];
+                dX[r * in_dim + i] = acc;
+            }
+    }
+    if (dW) {
+#pragma omp parallel for schedule(static)
+        for (int64_t o = 0; o < out_dim; ++o)
+            for (int64_t i = 0; i < in_dim; ++i) {
+                double acc = 0.0;
+                for (int64_t r = 0; r < rows; ++r) acc += dY[r * out_dim + o] * X[r * in_dim + i];
+                dW[o * in_dim + i] = acc;
+            }
+    }
+    if (db) {
+#pragma omp parallel for schedule(static)
+        for (int64_t o = 0; o < out_dim; ++o) {
+            double acc = 0.0;
+            for (int64_t r = 0; r < rows; ++r) acc += dY[r * out_dim + o];
+            db[o] = acc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward of one full forward pass: the chain rule of Notes steps 1-5.     */
+/* (The page's training path recomputes the attention in the backward pass  */
+/* instead of keeping the packed per-edge tensors; so does this function:    */
+/* it recomputes the forward from the inputs.)                               */
+/* Given dout = dLoss/d output (B, L, E):                                    */
+/*   step 5:  dmixed = dout Wo, dWo = dout^T mixed, dbo = sum dout           */
+/*   steps 2-4, per (sample b, target t, head h), over the live edges e into */
+/*   t, with weights w_e and scores s_e of the forward:                      */
+/*     dw_e  = dot(dmixed[t, h], v[s_e, h])                                  */
+/*     ds_e  = w_e * (dw_e - sum_e' w_e' dw_e')      (softmax backward)      */
+/*     dq[t, h]   += ds_e * k[s_e, h] / sqrt(d)                              */
+/*     dk[s_e, h] += ds_e * q[t, h] / sqrt(d)                                */
+/*     dv[s_e, h] += w_e * dmixed[t, h]                                      */
+/*   dropped keys (key_padding_mask) have no weight and get nothing;         */
+/*   step 1:  each projection through oracle_linear_backward.                */
+/* Outputs: dquery (B, L, E), dkey and dvalue (B, S, E) - one per input even */
+/* when the caller passes one tensor for several inputs (the caller adds     */
+/* them) - and dwq.. dwo (E, E), dbq.. dbo (E) (bias gradients may be NULL). */
+/* ------------------------------------------------------------------------ */
+
+int oracle_backward(int64_t batch, int64_t query_features, int64_t key_features, int64_t embed_dim,
+                    int64_t num_heads, const double *query, const double *key, const double *value,
+                    const double *wq, const double *bq, const double *wk, const double *bk, const double *wv,
+                    const double *bv, const double *wo, const double *bo, int64_t nnz,
+                    const int64_t *source_index, const int64_t *target_index,
+                    const unsigned char *key_padding_mask, const double *dout, double *dquery, double *dkey,
+                    double *dvalue, double *dwq, double *dbq, double *dwk, double *dbk, double *dwv, double *dbv,
+                    double *dwo, double *dbo)
+{
+    (void)bo;
+    const int64_t B = batch, L = query_features, S = key_features, E = embed_dim, H = num_heads;
+    if (B < 1 || L < 1 || S < 1 || E < 1 || H < 1 || E % H != 0) return ORACLE_ERR_ARG;
+    const int64_t d = E / H;
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    int status = ORACLE_OK;
+    double *q = (double *)malloc((size_t)(B * L * E) * sizeof(double));
+    double *k = (double *)malloc((size_t)(B * S * E) * sizeof(double));
+    double *v = (double *)malloc((size_t)(B * S * E) * sizeof(double));
+    double *mixed = (double *)calloc((size_t)(B * L * E), sizeof(double));
+    double *dmixed = (double *)malloc((size_t)(B * L * E) * sizeof(double));
+    double *dq = (double *)calloc((size_t)(B * L * E), sizeof(double));
+    double *dk = (double *)calloc((size_t)(B * S * E), sizeof(double));
+    double *dv = (double *)calloc((size_t)(B * S * E), sizeof(double));
+    int64_t *first = (int64_t *)malloc((size_t)(L + 1) * sizeof(int64_t));
+    int64_t *fill = (int64_t *)malloc((size_t)(L + 1) * sizeof(int64_t));
+    int64_t *edges_of = (int64_t *)malloc((size_t)(nnz > 0 ? nnz : 1) * sizeof(int64_t));
+    if (!q || !k || !v || !mixed || !dmixed || !dq || !dk || !dv || !first || !fill || !edges_of) {
+        status = ORACLE_ERR_NOMEM;
+        goto done;
+    }
+    /* forward recompute: projections and, per target, its edges in index-array order */
+    oracle_linear(B * L, E, E, query, wq, bq, q);
+    oracle_linear(B * S, E, E, key, wk, bk, k);
+    oracle_linear(B * S, E, E, value, wv, bv, v);
+    for (int64_t t = 0; t <= L; ++t) first[t] = 0;
+    for (int64_t e = 0; e < nnz; ++e) first[target_index[e] + 1] += 1;
+    for (int64_t t = 0; t < L; ++t) first[t + 1] += first[t];
+    for (int64_t t = 0; t <= L; ++t) fill[t] = first[t];
+    for (int64_t e = 0; e < nnz; ++e) edges_of[fill[target_index[e]]++] = e;
+
+    /* steps 2-4 forward (weights and mixed) and backward, one sample per thread:
+       dk and dv of a sample only receive from that sample's targets */
+#pragma omp parallel
+    {
+        int64_t max_deg = 0;
+        for (int64_t t = 0; t < L; ++t)
+            if (first[t + 1] - first[t] > max_deg) max_deg = first[t + 1] - first[t];
+        const int64_t cap = max_deg > 0 ? max_deg : 1;
+        double *w = (double *)malloc((size_t)cap * sizeof(double));
+        double *dw = (double *)malloc((size_t)cap * sizeof(double));
+        int local_status = (w && dw) ? ORACLE_OK : ORACLE_ERR_NOMEM;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t b = 0; b < B; ++b) {
+            if (local_status != ORACLE_OK) continue;
+            /* forward mixed of every target of this sample, then step 5's dmixed */
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t deg = first[t + 1] - first[t];
+                for (int64_t h = 0; h < H; ++h) {
+                    double m = -INFINITY;
+                    int64_t live = 0;
+                    for (int64_t j = 0; j < deg; ++j) {
+                        const int64_t s = source_index[edges_of[first[t] + j]];
+                        if (key_padding_mask && key_padding_mask[b * S + s]) continue;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += q[(b * L + t) * E + h * d + c] * k[(b * S + s) * E + h * d + c];
+                        w[j] = dot * inv_sqrt_d;
+                        if (w[j] > m) m = w[j];
+                        ++live;
+                    }
+                    if (live == 0) continue;
+                    double denom = 0.0;
+                    for (int64_t j = 0; j < deg; ++j) {
+                        const int64_t s = source_index[edges_of[first[t] + j]];
+                        if (key_padding_mask && key_padding_mask[b * S + s]) continue;
+                        denom += exp(w[j] - m);
+                    }
+                    for (int64_t j = 0; j < deg; ++j) {
+                        const int64_t s = source_index[edges_of[first[t] + j]];
+                        if (key_padding_mask && key_padding_mask[b * S + s]) continue;
+                        const double wj = exp(w[j] - m) / denom;
+                        for (int64_t c = 0; c < d; ++c)
+                            mixed[(b * L + t) * E + h * d + c] += wj * v[(b * S + s) * E + h * d + c];
+                    }
+                }
+            }
+        }
+        free(w);
+        free(dw);
+        if (local_status != ORACLE_OK) {
+#pragma omp atomic write
+            status = local_status;
+        }
+    }
+    if (status != ORACLE_OK) goto done;
+    /* step 5 backward */
+    oracle_linear_backward(B * L, E, E, mixed, wo, dout, dmixed, dwo, dbo);
+#pragma omp parallel
+    {
+        int64_t max_deg = 0;
+        for (int64_t t = 0; t < L; ++t)
+            if (first[t + 1] - first[t] > max_deg) max_deg = first[t + 1] - first[t];
+        const int64_t cap = max_deg > 0 ? max_deg : 1;
+        double *w = (double *)malloc((size_t)cap * sizeof(double));
+        double *dw = (double *)malloc((size_t)cap * sizeof(double));
+        int local_status = (w && dw) ? ORACLE_OK : ORACLE_ERR_NOMEM;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t b = 0; b < B; ++b) {
+            if (local_status != ORACLE_OK) continue;
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t deg = first[t + 1] - first[t];
+                const double *qt = q + (b * L + t) * E;
+                const double *gt = dmixed + (b * L + t) * E;
+                for (int64_t h = 0; h < H; ++h) {
+                    /* the forward weights of this (target, head) */
+                    double m = -INFINITY;
+                    int64_t live = 0;
+                    for (int64_t j = 0; j < deg; ++j) {
+                        const int64_t s = source_index[edges_of[first[t] + j]];
+                        if (key_padding_mask && key_padding_mask[b * S + s]) continue;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += qt[h * d + c] * k[(b * S + s) * E + h * d + c];
+                        w[j] = dot * inv_sqrt_d;
+                        if (w[j] > m) m = w[j];
+                        ++live;
+                    }
+                    if (live == 0) continue;
+                    double denom = 0.0;
+                    for (int64_t j = 0; j < deg; ++j) {
+                        const int64_t s = source_index[edges_of[first[t] + j]];
+                        if (key_padding_mask && key_padding_mask[b * S + s]) continue;
+                        denom += exp(w[j] - m);
+                    }
+                    /* dw_e and their weighted sum */
+                    double wdw = 0.0;
+                    for (int64_t j = 0; j < deg; ++j) {
+                        const int64_t s = source_index[edges_of[first[t] + j]];
+                        if (key_padding_mask && key_padding_mask[b * S + s]) continue;
+                        w[j] = exp(w[j] - m) / denom;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += gt[h * d + c] * v[(b * S + s) * E + h * d + c];
+                        dw[j] = dot;
+                        wdw += w[j] * dot;
+                    }
+                    for (int64_t j = 0; j < deg; ++j) {
+                        const int64_t s = source_index[edges_of[first[t] + j]];
+                        if (key_padding_mask && key_padding_mask[b * S + s]) continue;
+                        const double ds = w[j] * (dw[j] - wdw);
+                        for (int64_t c = 0; c < d; ++c) {
+                            dq[(b * L + t) * E + h * d + c] += ds * k[(b * S + s) * E + h * d + c] * inv_sqrt_d;
+                            dk[(b * S + s) * E + h * d + c] += ds * qt[h * d + c] * inv_sqrt_d;
+                            dv[(b * S + s) * E + h * d + c] += w[j] * gt[h * d + c];
+                        }
+                    }
+                }
+            }
+        }
+        free(w);
+        free(dw);
+        if (local_status != ORACLE_OK) {
+#pragma omp atomic write
+            status = local_status;
+        }
+    }
+    if (status != ORACLE_OK) goto done;
+    /* step 1 backward */
+    oracle_linear_backward(B * L, E, E, query, wq, dq, dquery, dwq, dbq);
+    oracle_linear_backward(B * S, E, E, key, wk, dk, dkey, dwk, dbk);
+    oracle_linear_backward(B * S, E, E, value, wv, dv, dvalue, dwv, dbv);
+
+done:
+    free(q); free(k); free(v); free(mixed); free(dmixed); free(dq); free(dk); free(dv);
+    free(first); free(fill); free(edges_of);
+    return status;
+}
+
 void oracle_average_heads(int64_t rows, int64_t num_heads, const double *w_head, double *w_avg)
 {
     for (int64_t r = 0; r < rows; ++r) {
