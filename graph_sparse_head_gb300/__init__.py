@@ -28,6 +28,7 @@ __all__ = [
     "pmha_graph_export", "pmha_forward", "pmha_forward_host", "pmha_edge_weights",
     "pmha_forward_workspace_size", "pmha_edge_weights_workspace_size", "pmha_forward_host_workspace_size",
     "pmha_device_status", "pmha_profile_enable", "pmha_profile_read", "pmha_launch_count",
+    "pmha_backward", "pmha_backward_workspace_size", "pmha_graph_export_by_source",
     "WMODES",
 ]
 
@@ -154,6 +155,16 @@ def pmha_graph_export(graph: Graph, stream=None):
     _lib.check(_lib.load().pmha_graph_export(graph.handle, _ptr(row_ptr), _ptr(col), _ptr(perm),
                                              _stream_ptr(stream)), "pmha_graph_export")
     return row_ptr, col, perm
+
+
+def pmha_graph_export_by_source(graph: Graph, stream=None):
+    """(src_row_ptr, target) of the per-source view as int32 CUDA tensors."""
+    dev = graph.device
+    src_row_ptr = torch.empty(graph.key_features + 1, dtype=torch.int32, device=dev)
+    target = torch.empty(graph.nnz, dtype=torch.int32, device=dev)
+    _lib.check(_lib.load().pmha_graph_export_by_source(graph.handle, _ptr(src_row_ptr), _ptr(target),
+                                                       _stream_ptr(stream)), "pmha_graph_export_by_source")
+    return src_row_ptr, target
 
 
 def pmha_forward_workspace_size(graph: Graph, params: Params, batch: int, wmode: str = "none") -> int:
@@ -291,6 +302,61 @@ def pmha_edge_weights(graph: Graph, params: Params, query: torch.Tensor, key: to
                                    _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
     _lib.check(st, "pmha_edge_weights")
     return weights
+
+
+def pmha_backward_workspace_size(graph: Graph, params: Params, batch: int) -> int:
+    p = params.as_struct()
+    return int(_lib.load().pmha_backward_workspace_size(graph.handle, ctypes.byref(p), int(batch)))
+
+
+def pmha_backward(graph: Graph, params: Params, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                  dout: torch.Tensor, key_padding_mask: torch.Tensor | None = None, input_grads: bool = True,
+                  param_grads: bool = True, workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Gradients of the layer for dout = dLoss/d(output): recomputes the forward
+    from (query, key, value) and returns {"dquery", "dkey", "dvalue"} in the layer
+    dtype (one shared tensor when inputs are one tensor, holding the sum) and
+    {"dwq", "dwk", "dwv", "dwo", "dbq", "dbk", "dbv", "dbo"} in float32 (None
+    for biases the layer does not have)."""
+    B = int(query.shape[0])
+    E = params.embed_dim
+    dev = query.device
+    _check_tokens("query", query, B, graph.query_features, E, params.dtype, dev)
+    _check_tokens("key", key, B, graph.key_features, E, params.dtype, dev)
+    _check_tokens("value", value, B, graph.key_features, E, params.dtype, dev)
+    _check_tokens("dout", dout, B, graph.query_features, E, params.dtype, dev)
+    mp = _check_mask(key_padding_mask, B, graph.key_features, True, dev)
+    p = params.as_struct()
+    lib = _lib.load()
+    out = {}
+    gx = [None, None, None]
+    if input_grads:
+        made = {}
+        for i, (name, x) in enumerate((("dquery", query), ("dkey", key), ("dvalue", value))):
+            if x.data_ptr() not in made:
+                made[x.data_ptr()] = torch.empty_like(x)
+            out[name] = made[x.data_ptr()]
+            gx[i] = _ptr(out[name])
+    g = _lib.PmhaGrads()
+    if param_grads:
+        for n in ("wq", "wk", "wv", "wo"):
+            out["d" + n] = torch.empty((E, E), dtype=torch.float32, device=dev)
+            setattr(g, n, _ptr(out["d" + n]))
+        for n in ("bq", "bk", "bv", "bo"):
+            if getattr(params, n) is None:
+                out["d" + n] = None
+            else:
+                out["d" + n] = torch.empty(E, dtype=torch.float32, device=dev)
+                setattr(g, n, _ptr(out["d" + n]))
+    need = lib.pmha_backward_workspace_size(graph.handle, ctypes.byref(p), B)
+    if need == 0:
+        _lib.check(_lib.PMHA_OK + 5, "pmha_backward_workspace_size (unsupported shape)")
+    ws = _workspace(need, dev, workspace)
+    with torch.cuda.device(dev):
+        st = lib.pmha_backward(graph.handle, ctypes.byref(p), _ptr(query), _ptr(key), _ptr(value), mp, B, _ptr(dout),
+                               gx[0], gx[1], gx[2], ctypes.byref(g), _ptr(ws), ws.numel() * ws.element_size(),
+                               _stream_ptr(stream))
+    _lib.check(st, "pmha_backward")
+    return out
 
 
 def pmha_device_status(stream=None) -> None:

@@ -29,7 +29,12 @@ class PmhaParams(ctypes.Structure):
                 ("bq", _vp), ("bk", _vp), ("bv", _vp), ("bo", _vp)]
 
 
+class PmhaGrads(ctypes.Structure):
+    _fields_ = [(n, _vp) for n in ("wq", "wk", "wv", "wo", "bq", "bk", "bv", "bo")]
+
+
 _P = ctypes.POINTER(PmhaParams)
+_G = ctypes.POINTER(PmhaGrads)
 _I64P = ctypes.POINTER(ctypes.c_int64)
 
 SIGNATURES = {
@@ -50,6 +55,9 @@ SIGNATURES = {
     "pmha_profile_read": (ctypes.c_int, [ctypes.c_int, ctypes.c_char_p, _I64P,
                                          ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
     "pmha_launch_count": (ctypes.c_int64, []),
+    "pmha_backward_workspace_size": (_sz, [_vp, _P, _i64]),
+    "pmha_backward": (ctypes.c_int, [_vp, _P, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _G, _vp, _sz, _vp]),
+    "pmha_graph_export_by_source": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
 }
 
 _lock = threading.Lock()

@@ -12,6 +12,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <string>
@@ -245,7 +246,8 @@ GemmSegments segs(const void *w0, const void *b0, const void *w1 = nullptr, cons
 // Steps 1-4 (and the weights); with_values = false stops after the scores.
 pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
                    const void *value, const uint8_t *kpm, int64_t B, pmha_wmode wmode, float *weights, char *ws, const Layout &lay,
-                   bool with_values, cudaStream_t s, const void **mixed_out)
+                   bool with_values, cudaStream_t s, const void **mixed_out, float *ml_keep = nullptr,
+                   bool allow_dense = true, EdgeArgs *args_out = nullptr)
 {
     const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
     const size_t es = type_size(inter_type(p->dtype));
@@ -289,7 +291,7 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.v_off = E;
     a.mixed = with_values ? ws + lay.mixed : nullptr;
     a.part = (float *)(ws + lay.part);
-    a.ml = wmode != PMHA_WEIGHTS_NONE ? (float *)(ws + lay.ml) : nullptr;
+    a.ml = ml_keep ? ml_keep : (wmode != PMHA_WEIGHTS_NONE ? (float *)(ws + lay.ml) : nullptr);
     a.scores = wmode == PMHA_WEIGHTS_NONE ? nullptr : (wmode == PMHA_WEIGHTS_AVG ? (float *)(ws + lay.scores) : weights);
     a.B = B;
     a.L = L;
@@ -301,7 +303,8 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.with_values = with_values;
     a.kpm = kpm;
     const TcType it = inter_type(p->dtype);
-    if (with_values && dense_supported(g, E, H, it)) {
+    if (args_out) *args_out = a;
+    if (allow_dense && with_values && dense_supported(g, E, H, it)) {
         // most (target, source) pairs are edges: steps 2-4 as masked-dense tiles
         DenseInputs din;
         din.q = a.q;
@@ -394,6 +397,47 @@ pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void
                      segs(p->wo, p->bo), output, E, "out_proj", s);
 }
 
+// Workspace of the backward pass: the forward's regions, then (m, l), D,
+// dmixed, dq, dk, dv, partial sums, an fp32 input-gradient accumulator and
+// the chunk partials of the weight-gradient sums.
+struct BwdLayout {
+    Layout f;
+    size_t ml = 0, D = 0, dmixed = 0, dq = 0, dk = 0, dv = 0, pdq = 0, pdkv = 0, dx = 0, scratch = 0, total = 0;
+    int64_t chunks = 1;
+};
+
+BwdLayout bwd_layout(const pmha_graph *g, const pmha_params *p, int64_t B)
+{
+    const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
+    const size_t es = type_size(inter_type(p->dtype));
+    BwdLayout b;
+    b.f = layout(g, p, B, PMHA_WEIGHTS_NONE, true);
+    size_t o = b.f.total;
+    b.ml = o;
+    o += align256((size_t)(B * L * H * 2) * 4);
+    b.D = o;
+    o += align256((size_t)(B * L * H) * 4);
+    b.dmixed = o;
+    o += align256((size_t)(B * L * E) * es);
+    b.dq = o;
+    o += align256((size_t)(B * L * E) * 4);
+    b.dk = o;
+    o += align256((size_t)(B * S * E) * 4);
+    b.dv = o;
+    o += align256((size_t)(B * S * E) * 4);
+    b.pdq = o;
+    o += align256((size_t)(B * 2 * g->n_units * E) * 4);
+    b.pdkv = o;
+    o += align256((size_t)(B * 2 * g->n_units * 2 * E) * 4);
+    b.dx = o;
+    o += align256((size_t)(std::max(B * L, B * S) * E) * 4);
+    b.chunks = std::max<int64_t>(1, std::min<int64_t>(64, std::max(B * L, B * S) / 4096));
+    b.scratch = o;
+    o += align256((size_t)(b.chunks * E * E) * 4);
+    b.total = o;
+    return b;
+}
+
 }  // namespace
 }  // namespace pmha
 
@@ -473,6 +517,21 @@ pmha_status pmha_graph_export(const pmha_graph *g, int32_t *row_ptr, int32_t *co
         PMHA_CUDA_TRY(cudaMemcpyAsync(row_ptr, g->row_ptr, (size_t)(g->L + 1) * 4, cudaMemcpyDeviceToDevice, s));
     if (col) PMHA_CUDA_TRY(cudaMemcpyAsync(col, g->col, (size_t)g->nnz * 4, cudaMemcpyDeviceToDevice, s));
     if (perm) PMHA_CUDA_TRY(cudaMemcpyAsync(perm, g->perm, (size_t)g->nnz * 4, cudaMemcpyDeviceToDevice, s));
+    return PMHA_OK;
+}
+
+pmha_status pmha_graph_export_by_source(const pmha_graph *g, int32_t *src_row_ptr, int32_t *target,
+                                        pmha_stream stream)
+{
+    if (!g) {
+        set_error("graph is NULL");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    if (src_row_ptr)
+        PMHA_CUDA_TRY(cudaMemcpyAsync(src_row_ptr, g->src_row_ptr, (size_t)(g->S + 1) * 4, cudaMemcpyDeviceToDevice,
+                                      s));
+    if (target) PMHA_CUDA_TRY(cudaMemcpyAsync(target, g->tgt_by_src, (size_t)g->nnz * 4, cudaMemcpyDeviceToDevice, s));
     return PMHA_OK;
 }
 
@@ -611,6 +670,134 @@ pmha_status pmha_edge_weights(const pmha_graph *g, const pmha_params *p, const v
     }
     return attend(g, p, query, key, key, key_padding_mask, B, wmode, weights, (char *)workspace, lay, false, (cudaStream_t)stream,
                   nullptr);
+}
+
+size_t pmha_backward_workspace_size(const pmha_graph *g, const pmha_params *p, int64_t batch)
+{
+    if (check_params(g, p, batch) != PMHA_OK) return 0;
+    int cpl, lph;
+    if (!bwd_shape(p->embed_dim, p->num_heads, &cpl, &lph)) return 0;
+    return bwd_layout(g, p, batch).total;
+}
+
+pmha_status pmha_backward(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
+                          const void *value, const uint8_t *key_padding_mask, int64_t B, const void *dout,
+                          void *dquery, void *dkey, void *dvalue, const pmha_grads *grads, void *workspace,
+                          size_t ws_bytes, pmha_stream stream)
+{
+    pmha_status st = check_params(g, p, B);
+    if (st != PMHA_OK) return st;
+    const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
+    if (!query || !key || !value || !dout || !aligned16(query) || !aligned16(key) || !aligned16(value) ||
+        !aligned16(dout)) {
+        set_error("pmha_backward: query, key, value and dout must be non-NULL, 16-byte aligned device pointers");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if ((E * (int64_t)elem_size(p->dtype)) % 16) {
+        set_error("embed_dim %lld gives rows that are not a multiple of 16 bytes", (long long)E);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    int cpl, lph;
+    if (!bwd_shape(E, H, &cpl, &lph)) {
+        set_error("pmha_backward: no kernel for embed_dim %lld, num_heads %lld", (long long)E, (long long)H);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    if ((query == key || query == value) && L != S) {
+        set_error("pmha_backward: one tensor cannot be the query (%lld tokens) and a key/value (%lld tokens)",
+                  (long long)L, (long long)S);
+        return PMHA_ERR_INVALID_ARG;
+    }
+    // roles sharing one input tensor must share (or leave NULL) their gradient buffer
+    const void *in[3] = {query, key, value};
+    void *gx[3] = {dquery, dkey, dvalue};
+    for (int i = 0; i < 3; ++i)
+        for (int j = i + 1; j < 3; ++j)
+            if (in[i] == in[j] && gx[i] && gx[j] && gx[i] != gx[j]) {
+                set_error("pmha_backward: inputs %d and %d are one tensor, so their gradients must be one buffer", i,
+                          j);
+                return PMHA_ERR_INVALID_ARG;
+            }
+    const BwdLayout bl = bwd_layout(g, p, B);
+    if (!workspace || ws_bytes < bl.total || ((uintptr_t)workspace & 255u)) {
+        set_error("pmha_backward: workspace needs %zu bytes, 256-byte aligned (got %zu)", bl.total, ws_bytes);
+        return PMHA_ERR_WORKSPACE;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    char *ws = (char *)workspace;
+    const TcType it = inter_type(p->dtype), pt = param_type(p->dtype);
+    const size_t es = type_size(it);
+    float *ml = (float *)(ws + bl.ml), *D = (float *)(ws + bl.D);
+    void *dmixed = ws + bl.dmixed;
+    float *dq = (float *)(ws + bl.dq), *dk = (float *)(ws + bl.dk), *dv = (float *)(ws + bl.dv);
+    float *dx = (float *)(ws + bl.dx), *scratch = (float *)(ws + bl.scratch);
+
+    // forward recompute: projections, (m, l) of every target, the mix
+    EdgeArgs a;
+    const void *mixed = nullptr;
+    st = attend(g, p, query, key, value, key_padding_mask, B, PMHA_WEIGHTS_NONE, nullptr, ws, bl.f, true, s, &mixed,
+                ml, false, &a);
+    if (st != PMHA_OK) return st;
+    // step 5
+    if ((st = bwd_gemm_nn(pt, pt, it, dout, E, p->wo, E, dmixed, E, B * L, E, E, false, s)) != PMHA_OK) return st;
+    if (grads && (grads->wo || grads->bo))
+        if ((st = bwd_gemm_tn(pt, it, dout, E, mixed, E, B * L, E, E, grads->wo, grads->bo, scratch, bl.chunks, s)) !=
+            PMHA_OK)
+            return st;
+    // steps 2-4
+    if ((st = bwd_rowdot(it, dmixed, mixed, B * L, E, H, D, s)) != PMHA_OK) return st;
+    BwdAttnArgs x;
+    x.q = a.q;
+    x.q_ld = a.q_ld;
+    x.k = a.kv;
+    x.v = (const char *)a.kv + (size_t)a.v_off * es;
+    x.kv_ld = a.kv_ld;
+    x.dmixed = dmixed;
+    x.ml = ml;
+    x.D = D;
+    x.kpm = key_padding_mask;
+    x.dq = dq;
+    x.dk = dk;
+    x.dv = dv;
+    x.part_dq = (float *)(ws + bl.pdq);
+    x.part_dkv = (float *)(ws + bl.pdkv);
+    x.B = B;
+    x.E = E;
+    x.H = H;
+    if ((st = bwd_attention(it, g, x, s)) != PMHA_OK) return st;
+    // step 1: weight and bias gradients of the projections
+    const float *dy[3] = {dq, dk, dv};
+    const void *w[3] = {p->wq, p->wk, p->wv};
+    const int64_t rows[3] = {B * L, B * S, B * S};
+    float *gw[3] = {grads ? grads->wq : nullptr, grads ? grads->wk : nullptr, grads ? grads->wv : nullptr};
+    float *gb[3] = {grads ? grads->bq : nullptr, grads ? grads->bk : nullptr, grads ? grads->bv : nullptr};
+    for (int r = 0; r < 3; ++r)
+        if (gw[r] || gb[r])
+            if ((st = bwd_gemm_tn(TcType::F32, pt, dy[r], E, in[r], E, rows[r], E, E, gw[r], gb[r], scratch,
+                                  bl.chunks, s)) != PMHA_OK)
+                return st;
+    // input gradients: one sum per distinct input tensor
+    for (int r = 0; r < 3; ++r) {
+        bool seen = false;
+        for (int q = 0; q < r; ++q) seen |= in[q] == in[r];
+        if (seen) continue;
+        void *target = nullptr;
+        for (int q = r; q < 3; ++q)
+            if (in[q] == in[r] && gx[q]) {
+                target = gx[q];
+                break;
+            }
+        if (!target) continue;
+        bool first = true;
+        for (int q = r; q < 3; ++q) {
+            if (in[q] != in[r]) continue;
+            if ((st = bwd_gemm_nn(TcType::F32, pt, TcType::F32, dy[q], E, w[q], E, dx, E, rows[r], E, E, !first, s)) !=
+                PMHA_OK)
+                return st;
+            first = false;
+        }
+        if ((st = bwd_convert(dx, rows[r] * E, pt, target, s)) != PMHA_OK) return st;
+    }
+    return PMHA_OK;
 }
 
 pmha_status pmha_device_status(pmha_stream stream)

@@ -1,0 +1,661 @@
+// Backward pass of the layer: the chain rule of kpnn2 PackedMultiheadAttention,
+// Notes steps 1-5, given dL/d(output). Like the page's training path it
+// recomputes the forward instead of keeping per-edge tensors: the caller's
+// inputs are projected again, the edge kernel gives each target's softmax
+// statistics (m, l) and its mix, and every per-edge weight is recomputed
+// from those when needed.
+//
+//   step 5   dmixed = dout Wo;  dWo = dout^T mixed;  dbo = sum dout
+//   steps 2-4, for each live edge e = (s -> t) and head h, with
+//            w_e = 2^(s_e - m_t) / l_t and D_t = dot(dmixed_t, mixed_t)
+//            (= sum_e w_e dw_e, since mixed_t = sum_e w_e v_s):
+//              dw_e = dot(dmixed_t, v_s),  ds_e = w_e (dw_e - D_t)
+//              dq_t += ds_e k_s / sqrt(d)  (a sum over the edges INTO t)
+//              dk_s += ds_e q_t / sqrt(d)  (a sum over the edges OUT of s)
+//              dv_s += w_e dmixed_t        (likewise)
+//            Both sums are segmented reductions without atomics: dq walks
+//            the per-target view, dk and dv the per-source view, each in
+//            units of kUnitEdges positions; a row that crosses a unit
+//            boundary leaves partial sums that an ordered merge adds up.
+//   step 1   dX = dq Wq (+ dk Wk + dv Wv for one shared input tensor),
+//            dWq = dq^T Xq, dbq = sum dq, likewise for k and v.
+// All sums run in a fixed order: results are deterministic.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "pmha_internal.h"
+
+namespace pmha {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float ex2f(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------- D = dot(dmixed, mixed) per (row, head)
+template <typename T>
+__global__ void k_rowdot(const T *__restrict__ dmixed, const T *__restrict__ mixed, long long rows, int E, int H,
+                         float *__restrict__ D)
+{
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows * H) return;
+    const long long r = i / H;
+    const int h = (int)(i - r * H), d = E / H;
+    const T *g = dmixed + r * E + h * d;
+    const T *o = mixed + r * E + h * d;
+    float acc = 0.f;
+    for (int c = 0; c < d; ++c) acc = __fmaf_rn(to_f(g[c]), to_f(o[c]), acc);
+    D[i] = acc;
+}
+
+struct WalkArgs {
+    const void *q;    // (B, L) rows of pitch q_ld (intermediate type)
+    long long q_ld;
+    const void *k;    // (B, S) rows of pitch kv_ld
+    const void *v;
+    long long kv_ld;
+    const void *g;    // dmixed (B, L, E), intermediate type
+    const float *ml;  // (B, L, H, 2): m (log2 units), l
+    const float *D;   // (B, L, H)
+    const uint8_t *kpm;
+    const int32_t *row_ptr, *idx, *unit_first;  // the walked view: row pointers, the other end, unit plan
+    long long n_units, nnz;
+    int B, L, S, E, H, n_rows;  // n_rows: rows of the walked view (L for dq, S for dk/dv)
+    float score_scale;          // log2(e) / sqrt(d)
+    float inv_sqrt_d;
+    float *out0, *out1;   // dq (B, L, E) | dk, dv (B, S, E)
+    float *part;          // (B, 2 n_units, W) partial sums of rows crossing a unit boundary
+};
+
+// Sum over the lanes of one head (LPH lanes, aligned groups).
+template <int LPH>
+__device__ __forceinline__ float head_sum(float x)
+{
+#pragma unroll
+    for (int o = 1; o < LPH; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// dq: one warp per (sample, unit of the per-target view). Lane owns CPL
+// channels; the warp's lanes past E idle in the arithmetic but shuffle.
+template <typename T, int CPL, int LPH>
+__global__ void __launch_bounds__(256) k_bwd_dq(WalkArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= (long long)a.B * a.n_units) return;
+    const int b = (int)(gw / a.n_units), u = (int)(gw - (long long)b * a.n_units);
+    const int e0 = u * kUnitEdges;
+    const int e1 = (int)min((long long)e0 + kUnitEdges, a.nnz);
+    const int c0 = lane * CPL;
+    const bool act = c0 < a.E;
+    const int d = a.E / a.H, head = act ? c0 / d : 0;
+    const T *Q = (const T *)a.q + (long long)b * a.L * a.q_ld;
+    const T *G = (const T *)a.g + (long long)b * a.L * a.E;
+    const T *K = (const T *)a.k + (long long)b * a.S * a.kv_ld;
+    const T *V = (const T *)a.v + (long long)b * a.S * a.kv_ld;
+    const uint8_t *kpm = a.kpm ? a.kpm + (long long)b * a.S : nullptr;
+
+    int t = a.unit_first[u];
+    const bool first_started_here = a.row_ptr[t] == e0;
+    bool is_first = true;
+    int bound = a.row_ptr[t + 1];
+    float q[CPL], gv[CPL], acc[CPL], m = 0.f, inv_l = 0.f, Dt = 0.f;
+    auto load_row = [&]() {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            q[c] = act ? to_f(Q[(long long)t * a.q_ld + c0 + c]) : 0.f;
+            gv[c] = act ? to_f(G[(long long)t * a.E + c0 + c]) : 0.f;
+            acc[c] = 0.f;
+        }
+        const long long st = ((long long)b * a.L + t) * a.H + head;
+        m = a.ml[2 * st];
+        const float l = a.ml[2 * st + 1];
+        inv_l = l > 0.f ? __frcp_rn(l) : 0.f;
+        Dt = a.D[st];
+    };
+    auto finish = [&]() {
+        const bool complete = (is_first ? first_started_here : true) && bound <= e1;
+        if (!act) return;
+        if (complete) {
+            float *o = a.out0 + ((long long)b * a.L + t) * a.E + c0;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) o[c] = __fmul_rn(acc[c], a.inv_sqrt_d);
+        } else {
+            float *o = a.part + ((long long)b * 2 * a.n_units + 2 * u + (is_first ? 0 : 1)) * a.E + c0;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) o[c] = __fmul_rn(acc[c], a.inv_sqrt_d);
+        }
+    };
+    load_row();
+    for (int p = e0; p < e1; ++p) {
+        if (p >= bound) {
+            finish();
+            is_first = false;
+            do {
+                ++t;
+                bound = a.row_ptr[t + 1];
+            } while (bound <= p);
+            load_row();
+        }
+        const int s = a.idx[p];
+        if (kpm && kpm[s]) continue;  // a dropped key has no weight
+        float kk[CPL], vv[CPL], d1 = 0.f, d2 = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            kk[c] = act ? to_f(K[(long long)s * a.kv_ld + c0 + c]) : 0.f;
+            vv[c] = act ? to_f(V[(long long)s * a.kv_ld + c0 + c]) : 0.f;
+            d1 = __fmaf_rn(q[c], kk[c], d1);
+            d2 = __fmaf_rn(gv[c], vv[c], d2);
+        }
+        d1 = head_sum<LPH>(d1);
+        d2 = head_sum<LPH>(d2);
+        const float w = __fmul_rn(ex2f(__fsub_rn(__fmul_rn(d1, a.score_scale), m)), inv_l);
+        const float ds = __fmul_rn(w, __fsub_rn(d2, Dt));
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[c] = __fmaf_rn(ds, kk[c], acc[c]);
+    }
+    finish();
+}
+
+// dk and dv: one warp per (sample, unit of the per-source view).
+template <typename T, int CPL, int LPH>
+__global__ void __launch_bounds__(256) k_bwd_dkv(WalkArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= (long long)a.B * a.n_units) return;
+    const int b = (int)(gw / a.n_units), u = (int)(gw - (long long)b * a.n_units);
+    const int e0 = u * kUnitEdges;
+    const int e1 = (int)min((long long)e0 + kUnitEdges, a.nnz);
+    const int c0 = lane * CPL;
+    const bool act = c0 < a.E;
+    const int d = a.E / a.H, head = act ? c0 / d : 0;
+    const T *Q = (const T *)a.q + (long long)b * a.L * a.q_ld;
+    const T *G = (const T *)a.g + (long long)b * a.L * a.E;
+    const T *K = (const T *)a.k + (long long)b * a.S * a.kv_ld;
+    const T *V = (const T *)a.v + (long long)b * a.S * a.kv_ld;
+    const float *ML = a.ml + (long long)b * a.L * a.H * 2;
+    const float *DD = a.D + (long long)b * a.L * a.H;
+    const uint8_t *kpm = a.kpm ? a.kpm + (long long)b * a.S : nullptr;
+
+    int s = a.unit_first[u];
+    const bool first_started_here = a.row_ptr[s] == e0;
+    bool is_first = true;
+    int bound = a.row_ptr[s + 1];
+    bool dropped = false;
+    float kk[CPL], vv[CPL], ak[CPL], av[CPL];
+    auto load_row = [&]() {
+        dropped = kpm && kpm[s];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            kk[c] = act ? to_f(K[(long long)s * a.kv_ld + c0 + c]) : 0.f;
+            vv[c] = act ? to_f(V[(long long)s * a.kv_ld + c0 + c]) : 0.f;
+            ak[c] = 0.f;
+            av[c] = 0.f;
+        }
+    };
+    auto finish = [&]() {
+        const bool complete = (is_first ? first_started_here : true) && bound <= e1;
+        if (!act) return;
+        float *ok, *ov;
+        if (complete) {
+            ok = a.out0 + ((long long)b * a.S + s) * a.E + c0;
+            ov = a.out1 + ((long long)b * a.S + s) * a.E + c0;
+        } else {
+            ok = a.part + ((long long)b * 2 * a.n_units + 2 * u + (is_first ? 0 : 1)) * 2 * a.E + c0;
+            ov = ok + a.E;
+        }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            ok[c] = __fmul_rn(ak[c], a.inv_sqrt_d);
+            ov[c] = av[c];
+        }
+    };
+    load_row();
+    for (int p = e0; p < e1; ++p) {
+        if (p >= bound) {
+            finish();
+            is_first = false;
+            do {
+                ++s;
+                bound = a.row_ptr[s + 1];
+            } while (bound <= p);
+            load_row();
+        }
+        if (dropped) continue;  // every edge of a dropped key has weight 0
+        const int t = a.idx[p];
+        const long long st = (long long)t * a.H + head;
+        const float m = ML[2 * st], l = ML[2 * st + 1], Dt = DD[st];
+        float qq[CPL], gg[CPL], d1 = 0.f, d2 = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            qq[c] = act ? to_f(Q[(long long)t * a.q_ld + c0 + c]) : 0.f;
+            gg[c] = act ? to_f(G[(long long)t * a.E + c0 + c]) : 0.f;
+            d1 = __fmaf_rn(qq[c], kk[c], d1);
+            d2 = __fmaf_rn(gg[c], vv[c], d2);
+        }
+        d1 = head_sum<LPH>(d1);
+        d2 = head_sum<LPH>(d2);
+        const float w = l > 0.f ? __fmul_rn(ex2f(__fsub_rn(__fmul_rn(d1, a.score_scale), m)), __frcp_rn(l)) : 0.f;
+        const float ds = __fmul_rn(w, __fsub_rn(d2, Dt));
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            ak[c] = __fmaf_rn(ds, qq[c], ak[c]);
+            av[c] = __fmaf_rn(w, gg[c], av[c]);
+        }
+    }
+    finish();
+}
+
+// Rows of a view that cross a unit boundary, or have no edges: add the
+// pieces in unit order (no edges: zeros). One warp per (sample, row);
+// width W floats per piece, written to out (+ out1 for the second half
+// when W = 2E).
+__global__ void __launch_bounds__(256) k_bwd_merge(const int32_t *__restrict__ merge_rows, long long n_merge,
+                                                   const int32_t *__restrict__ row_ptr, const float *__restrict__ part,
+                                                   long long n_units, int B, int n_rows, int E, int W,
+                                                   float *__restrict__ out0, float *__restrict__ out1)
+{
+    const int lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= (long long)B * n_merge) return;
+    const int b = (int)(gw / n_merge);
+    const int r = merge_rows[gw - (long long)b * n_merge];
+    const int beg = row_ptr[r], end = row_ptr[r + 1];
+    const float *base = part + (long long)b * 2 * n_units * W;
+    for (int c = lane; c < W; c += 32) {
+        float acc = 0.f;
+        if (end > beg) {
+            const int u0 = beg / kUnitEdges, u1 = (end - 1) / kUnitEdges;
+            for (int i = 0; i <= u1 - u0; ++i) {
+                const int slot = 2 * (u0 + i) + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
+                acc = __fadd_rn(acc, base[(long long)slot * W + c]);
+            }
+        }
+        float *o = c < E ? out0 + ((long long)b * n_rows + r) * E + c : out1 + ((long long)b * n_rows + r) * E + c - E;
+        *o = acc;
+    }
+}
+
+// ---------------------------------------------------------------- CUDA-core GEMMs (fp32 accumulation)
+// C (M x N, pitch ldc) (+)= A (M x K, pitch lda) . B (K x N, pitch ldb)
+template <typename TA, typename TB, typename TC, bool ACC>
+__global__ void __launch_bounds__(256) k_gemm_nn(const TA *__restrict__ A, long long lda, const TB *__restrict__ B,
+                                                 long long ldb, TC *__restrict__ C, long long ldc, long long M, int N,
+                                                 int K)
+{
+    __shared__ float As[16][68], Bs[16][68];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const long long m0 = (long long)blockIdx.x * 64;
+    const int n0 = blockIdx.y * 64;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+            const int r = i / 16, c = i % 16;  // A tile: 64 rows x 16 k
+            const long long gm = m0 + r;
+            As[c][r] = (gm < M && k0 + c < K) ? to_f(A[gm * lda + k0 + c]) : 0.f;
+            const int kr = i / 64, nc = i % 64;  // B tile: 16 k x 64 cols
+            Bs[kr][nc] = (k0 + kr < K && n0 + nc < N) ? to_f(B[(long long)(k0 + kr) * ldb + n0 + nc]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                av[i] = As[kk][ty + 16 * i];
+                bv[i] = Bs[kk][tx + 16 * i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const long long gm = m0 + ty + 16 * i;
+        if (gm >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gn = n0 + tx + 16 * j;
+            if (gn >= N) continue;
+            float v = acc[i][j];
+            if (ACC) v = __fadd_rn(to_f(C[gm * ldc + gn]), v);
+            C[gm * ldc + gn] = from_f<TC>(v);
+        }
+    }
+}
+
+// P[chunk] (K x N) = A[rows of chunk]^T . B[rows of chunk]; A (M x K), B (M x N).
+// With B null, P[chunk] (K) = column sums of A over the chunk.
+template <typename TA, typename TB>
+__global__ void __launch_bounds__(256) k_gemm_tn_part(const TA *__restrict__ A, long long lda,
+                                                      const TB *__restrict__ B, long long ldb, long long M, int K,
+                                                      int N, long long rows_per_chunk, float *__restrict__ P)
+{
+    __shared__ float As[16][68], Bs[16][68];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int k0 = blockIdx.x * 64, n0 = blockIdx.y * 64;
+    const long long chunk = blockIdx.z;
+    const long long r_beg = chunk * rows_per_chunk, r_end = min(M, r_beg + rows_per_chunk);
+    float acc[4][4] = {};
+    for (long long r0 = r_beg; r0 < r_end; r0 += 16) {
+        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+            const int rr = i / 64, cc = i % 64;
+            const long long gr = r0 + rr;
+            As[rr][cc] = (gr < r_end && k0 + cc < K) ? to_f(A[gr * lda + k0 + cc]) : 0.f;
+            Bs[rr][cc] = (gr < r_end && n0 + cc < N) ? to_f(B[gr * ldb + n0 + cc]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            float av[4], bv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                av[i] = As[rr][ty + 16 * i];
+                bv[i] = Bs[rr][tx + 16 * i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+    float *out = P + chunk * (long long)K * N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gk = k0 + ty + 16 * i;
+        if (gk >= K) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gn = n0 + tx + 16 * j;
+            if (gn < N) out[(long long)gk * N + gn] = acc[i][j];
+        }
+    }
+}
+
+template <typename TA>
+__global__ void __launch_bounds__(256) k_colsum_part(const TA *__restrict__ A, long long lda, long long M, int K,
+                                                     long long rows_per_chunk, float *__restrict__ P)
+{
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    const long long chunk = blockIdx.y;
+    if (c >= K) return;
+    const long long r_beg = chunk * rows_per_chunk, r_end = min(M, r_beg + rows_per_chunk);
+    float acc = 0.f;
+    for (long long r = r_beg; r < r_end; ++r) acc = __fadd_rn(acc, to_f(A[r * lda + c]));
+    P[chunk * K + c] = acc;
+}
+
+// out[i] = sum over chunks of P[chunk][i], in chunk order
+__global__ void k_sum_chunks(const float *__restrict__ P, long long n, int chunks, float *__restrict__ out)
+{
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float acc = 0.f;
+    for (int c = 0; c < chunks; ++c) acc = __fadd_rn(acc, P[(long long)c * n + i]);
+    out[i] = acc;
+}
+
+template <typename TO>
+__global__ void k_convert(const float *__restrict__ in, long long n, TO *__restrict__ out)
+{
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = from_f<TO>(in[i]);
+}
+
+inline unsigned blocks(long long n, int t) { return (unsigned)((n + t - 1) / t); }
+
+template <typename T, int CPL>
+bool launch_walks_lph(int lph, const WalkArgs &dq, const WalkArgs &dkv, cudaStream_t s)
+{
+    const unsigned grid = blocks((long long)dq.B * dq.n_units, 8);
+    switch (lph) {
+#define PMHA_WALK(L)                                                    \
+    case L:                                                             \
+        k_bwd_dq<T, CPL, L><<<grid, 256, 0, s>>>(dq);                   \
+        k_bwd_dkv<T, CPL, L><<<grid, 256, 0, s>>>(dkv);                 \
+        return true;
+        PMHA_WALK(1) PMHA_WALK(2) PMHA_WALK(4) PMHA_WALK(8) PMHA_WALK(16) PMHA_WALK(32)
+#undef PMHA_WALK
+    default: return false;
+    }
+}
+
+template <typename T>
+bool launch_walks(int cpl, int lph, const WalkArgs &dq, const WalkArgs &dkv, cudaStream_t s)
+{
+    switch (cpl) {
+    case 1: return launch_walks_lph<T, 1>(lph, dq, dkv, s);
+    case 2: return launch_walks_lph<T, 2>(lph, dq, dkv, s);
+    case 4: return launch_walks_lph<T, 4>(lph, dq, dkv, s);
+    case 8: return launch_walks_lph<T, 8>(lph, dq, dkv, s);
+    case 16: return launch_walks_lph<T, 16>(lph, dq, dkv, s);
+    default: return false;
+    }
+}
+
+}  // namespace
+
+// Channels per lane and lanes per head of the per-edge backward kernels.
+bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lph)
+{
+    if (H < 1 || E % H || E > 512) return false;
+    const int64_t c = E >= 32 ? E / 32 : 1;
+    if ((c & (c - 1)) || E % c) return false;
+    if (E >= 32 && E % 32) return false;
+    const int64_t d = E / H;
+    if (d % c) return false;
+    const int64_t l = d / c;
+    if (l < 1 || l > 32 || (l & (l - 1))) return false;
+    *cpl = (int)c;
+    *lph = (int)l;
+    return true;
+}
+
+pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t rows, int64_t E, int64_t H, float *D,
+                       cudaStream_t s)
+{
+    StageTimer timer("bwd_rowdot", s);
+    if (t == TcType::F16)
+        k_rowdot<__half><<<blocks(rows * H, 256), 256, 0, s>>>((const __half *)dmixed, (const __half *)mixed, rows,
+                                                              (int)E, (int)H, D);
+    else
+        k_rowdot<float><<<blocks(rows * H, 256), 256, 0, s>>>((const float *)dmixed, (const float *)mixed, rows,
+                                                             (int)E, (int)H, D);
+    count_launch();
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+pmha_status bwd_attention(TcType t, const pmha_graph *g, const BwdAttnArgs &x, cudaStream_t s)
+{
+    int cpl, lph;
+    if (!bwd_shape(x.E, x.H, &cpl, &lph)) {
+        set_error("backward: no kernel for embed_dim %lld, num_heads %lld", (long long)x.E, (long long)x.H);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    WalkArgs dq;
+    dq.q = x.q;
+    dq.q_ld = x.q_ld;
+    dq.k = x.k;
+    dq.v = x.v;
+    dq.kv_ld = x.kv_ld;
+    dq.g = x.dmixed;
+    dq.ml = x.ml;
+    dq.D = x.D;
+    dq.kpm = x.kpm;
+    dq.n_units = g->n_units;
+    dq.nnz = g->nnz;
+    dq.B = (int)x.B;
+    dq.L = (int)g->L;
+    dq.S = (int)g->S;
+    dq.E = (int)x.E;
+    dq.H = (int)x.H;
+    dq.score_scale = (float)(1.4426950408889634 / sqrt((double)(x.E / x.H)));
+    dq.inv_sqrt_d = (float)(1.0 / sqrt((double)(x.E / x.H)));
+    WalkArgs dkv = dq;
+    dq.row_ptr = g->row_ptr;
+    dq.idx = g->col;
+    dq.unit_first = g->unit_first_t;
+    dq.n_rows = (int)g->L;
+    dq.out0 = x.dq;
+    dq.out1 = nullptr;
+    dq.part = x.part_dq;
+    dkv.row_ptr = g->src_row_ptr;
+    dkv.idx = g->tgt_by_src;
+    dkv.unit_first = g->unit_first_s;
+    dkv.n_rows = (int)g->S;
+    dkv.out0 = x.dk;
+    dkv.out1 = x.dv;
+    dkv.part = x.part_dkv;
+    if (x.B * g->n_units > 0) {
+        StageTimer timer("bwd_edges", s);
+        const bool ok = t == TcType::F16 ? launch_walks<__half>(cpl, lph, dq, dkv, s)
+                                         : launch_walks<float>(cpl, lph, dq, dkv, s);
+        if (!ok) {
+            set_error("backward: no kernel for %d channels per lane", cpl);
+            return PMHA_ERR_UNSUPPORTED;
+        }
+        count_launch(2);
+        PMHA_CUDA_TRY(cudaGetLastError());
+    }
+    StageTimer timer("bwd_merge", s);
+    if (g->n_merge > 0) {
+        k_bwd_merge<<<blocks(x.B * g->n_merge, 8), 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, x.part_dq,
+                                                                g->n_units, (int)x.B, (int)g->L, (int)x.E, (int)x.E,
+                                                                x.dq, nullptr);
+        count_launch();
+    }
+    if (g->n_merge_s > 0) {
+        k_bwd_merge<<<blocks(x.B * g->n_merge_s, 8), 256, 0, s>>>(g->merge_s, g->n_merge_s, g->src_row_ptr,
+                                                                  x.part_dkv, g->n_units, (int)x.B, (int)g->S,
+                                                                  (int)x.E, (int)(2 * x.E), x.dk, x.dv);
+        count_launch();
+    }
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+// ---------------------------------------------------------------- GEMM entry points
+namespace {
+template <typename TA, typename TB, typename TC>
+void nn_launch(const void *A, long long lda, const void *B, long long ldb, void *C, long long ldc, long long M, int N,
+               int K, bool acc, cudaStream_t s)
+{
+    dim3 grid(blocks(M, 64), blocks(N, 64));
+    if (acc)
+        k_gemm_nn<TA, TB, TC, true><<<grid, 256, 0, s>>>((const TA *)A, lda, (const TB *)B, ldb, (TC *)C, ldc, M, N,
+                                                          K);
+    else
+        k_gemm_nn<TA, TB, TC, false><<<grid, 256, 0, s>>>((const TA *)A, lda, (const TB *)B, ldb, (TC *)C, ldc, M,
+                                                           N, K);
+}
+}  // namespace
+
+// C (M x N) (+)= A (M x K) . B (K x N); types: A in {F32, BF16, F16}, B in
+// {F32, BF16}, C in {F32, F16}.
+pmha_status bwd_gemm_nn(TcType ta, TcType tb, TcType tc, const void *A, int64_t lda, const void *B, int64_t ldb,
+                        void *C, int64_t ldc, int64_t M, int64_t N, int64_t K, bool accumulate, cudaStream_t s)
+{
+    if (M <= 0) return PMHA_OK;
+#define PMHA_NN(TA_, TB_, TC_) nn_launch<TA_, TB_, TC_>(A, lda, B, ldb, C, ldc, M, (int)N, (int)K, accumulate, s)
+    if (tc == TcType::F32) {
+        if (ta == TcType::F32 && tb == TcType::F32) PMHA_NN(float, float, float);
+        else if (ta == TcType::F32 && tb == TcType::BF16) PMHA_NN(float, __nv_bfloat16, float);
+        else if (ta == TcType::BF16 && tb == TcType::BF16) PMHA_NN(__nv_bfloat16, __nv_bfloat16, float);
+        else {
+            set_error("bwd_gemm_nn: unsupported operand types");
+            return PMHA_ERR_UNSUPPORTED;
+        }
+    } else if (tc == TcType::F16) {
+        if (ta == TcType::BF16 && tb == TcType::BF16) PMHA_NN(__nv_bfloat16, __nv_bfloat16, __half);
+        else {
+            set_error("bwd_gemm_nn: unsupported operand types");
+            return PMHA_ERR_UNSUPPORTED;
+        }
+    } else {
+        set_error("bwd_gemm_nn: unsupported output type");
+        return PMHA_ERR_UNSUPPORTED;
+    }
+#undef PMHA_NN
+    count_launch();
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+// dW (K x N, fp32) = A^T B over M rows (A: M x K, B: M x N), and, when db is
+// given, db (K) = column sums of A; `scratch` holds the per-chunk partials.
+pmha_status bwd_gemm_tn(TcType ta, TcType tb, const void *A, int64_t lda, const void *B, int64_t ldb, int64_t M,
+                        int64_t K, int64_t N, float *dW, float *db, float *scratch, int64_t chunks, cudaStream_t s)
+{
+    if (chunks < 1) chunks = 1;
+    const long long rpc = (M + chunks - 1) / chunks;
+    if (dW) {
+        dim3 grid(blocks(K, 64), blocks(N, 64), (unsigned)chunks);
+#define PMHA_TN(TA_, TB_)                                                                                       \
+    k_gemm_tn_part<TA_, TB_><<<grid, 256, 0, s>>>((const TA_ *)A, lda, (const TB_ *)B, ldb, M, (int)K, (int)N, \
+                                                  rpc, scratch)
+        if (ta == TcType::F32 && tb == TcType::F32) PMHA_TN(float, float);
+        else if (ta == TcType::F32 && tb == TcType::BF16) PMHA_TN(float, __nv_bfloat16);
+        else if (ta == TcType::F32 && tb == TcType::F16) PMHA_TN(float, __half);
+        else if (ta == TcType::BF16 && tb == TcType::F16) PMHA_TN(__nv_bfloat16, __half);
+        else if (ta == TcType::BF16 && tb == TcType::BF16) PMHA_TN(__nv_bfloat16, __nv_bfloat16);
+        else {
+            set_error("bwd_gemm_tn: unsupported operand types");
+            return PMHA_ERR_UNSUPPORTED;
+        }
+#undef PMHA_TN
+        k_sum_chunks<<<blocks(K * N, 256), 256, 0, s>>>(scratch, K * N, (int)chunks, dW);
+        count_launch(2);
+    }
+    if (db) {
+        dim3 grid(blocks(K, 256), (unsigned)chunks);
+        if (ta == TcType::F32) k_colsum_part<float><<<grid, 256, 0, s>>>((const float *)A, lda, M, (int)K, rpc, scratch);
+        else k_colsum_part<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16 *)A, lda, M, (int)K, rpc, scratch);
+        k_sum_chunks<<<blocks(K, 256), 256, 0, s>>>(scratch, K, (int)chunks, db);
+        count_launch(2);
+    }
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+pmha_status bwd_convert(const float *in, int64_t n, TcType out_t, void *out, cudaStream_t s)
+{
+    if (n <= 0) return PMHA_OK;
+    if (out_t == TcType::BF16) k_convert<__nv_bfloat16><<<blocks(n, 256), 256, 0, s>>>(in, n, (__nv_bfloat16 *)out);
+    else if (out_t == TcType::F32) k_convert<float><<<blocks(n, 256), 256, 0, s>>>(in, n, (float *)out);
+    else k_convert<__half><<<blocks(n, 256), 256, 0, s>>>(in, n, (__half *)out);
+    count_launch();
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+}  // namespace pmha

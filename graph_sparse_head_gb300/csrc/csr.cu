@@ -387,6 +387,44 @@ __global__ void k_merge_write(const int *__restrict__ flag, const int *__restric
     if (t < L && flag[t]) merge_t[off[t]] = t;
 }
 
+// Keys of the by-source view: for CSR position p (target t, source s),
+// key = s * L + t; positions past nnz_total get the sentinel (sorted last).
+template <typename K>
+__global__ void k_csc_keys(const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col, int64_t L,
+                           const Summary *__restrict__ sum, int cap, K sentinel, K *__restrict__ keys,
+                           int *__restrict__ vals)
+{
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= cap) return;
+    vals[p] = p;
+    if (p >= sum->nnz_total) {
+        keys[p] = sentinel;
+        return;
+    }
+    int lo = 0, hi = (int)L;  // row_ptr[lo] <= p < row_ptr[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (row_ptr[mid] <= p) lo = mid;
+        else hi = mid;
+    }
+    keys[p] = (K)col[p] * (K)L + (K)lo;
+}
+
+// Target of each by-source position.
+template <typename K>
+__global__ void k_csc_view(const K *__restrict__ keys, const Summary *__restrict__ sum, int64_t L,
+                           int32_t *__restrict__ tgt_by_src)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= sum->nnz_total) return;
+    tgt_by_src[i] = (int32_t)((int64_t)(keys[i] % (K)L));
+}
+
+__global__ void k_copy_total(const Summary *__restrict__ from, Summary *__restrict__ to)
+{
+    to->nnz_total = from->nnz_total;
+}
+
 inline int blocks_for(int64_t n, int threads) { return (int)std::max<int64_t>(1, (n + threads - 1) / threads); }
 
 template <typename K>
@@ -418,11 +456,16 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     size_t off_tge = off_perm + align((size_t)cap * 4);
     size_t off_units = off_tge + align((size_t)cap * 4);
     size_t off_merge = off_units + align((size_t)max_units * 4);
-    size_t graph_bytes = off_merge + align((size_t)L * 4);
+    size_t off_srp = off_merge + align((size_t)L * 4);
+    size_t off_tbs = off_srp + align((size_t)(S + 1) * 4);
+    size_t off_ufs = off_tbs + align((size_t)cap * 4);
+    size_t off_ms = off_ufs + align((size_t)max_units * 4);
+    size_t graph_bytes = off_ms + align((size_t)S * 4);
 
     // temporaries
     const int n_tiles = std::max(1, (cap + kSortTile - 1) / kSortTile);
-    const int64_t scan_max = std::max<int64_t>({(int64_t)kRadix * n_tiles, L + 1, 1});
+    const int64_t LS1 = std::max(L, S) + 1;  // room for the per-target and the per-source passes
+    const int64_t scan_max = std::max<int64_t>({(int64_t)kRadix * n_tiles, LS1, 1});
     size_t t_keys_a = 0;
     size_t t_keys_b = t_keys_a + align((size_t)cap * sizeof(K));
     size_t t_vals_a = t_keys_b + align((size_t)cap * sizeof(K));
@@ -431,12 +474,12 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     size_t t_scan = t_hist + align((size_t)kRadix * n_tiles * 4);
     size_t t_loop = t_scan + align((size_t)(scan_max / kScanTile + 2) * 4);
     size_t t_miss = t_loop + align((size_t)(L + 1) * 4);
-    size_t t_c1 = t_miss + align((size_t)(L + 1) * 4);
-    size_t t_c2 = t_c1 + align((size_t)(L + 1) * 4);
-    size_t t_c3 = t_c2 + align((size_t)(L + 1) * 4);
-    size_t t_tot = t_c3 + align((size_t)(L + 1) * 4);
+    size_t t_c1 = t_miss + align((size_t)LS1 * 4);
+    size_t t_c2 = t_c1 + align((size_t)LS1 * 4);
+    size_t t_c3 = t_c2 + align((size_t)LS1 * 4);
+    size_t t_tot = t_c3 + align((size_t)LS1 * 4);
     size_t t_sum = t_tot + align(4 * sizeof(int));
-    size_t tmp_bytes = t_sum + align(sizeof(Summary));
+    size_t tmp_bytes = t_sum + align(2 * sizeof(Summary));
 
     char *gm = nullptr, *tm = nullptr;
     Summary *host_sum = nullptr;
@@ -448,7 +491,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         delete g;
         return cuda_fail(ce, "cudaMalloc(build temporaries)");
     }
-    if ((ce = cudaMallocHost(&host_sum, sizeof(Summary))) != cudaSuccess) {
+    if ((ce = cudaMallocHost(&host_sum, 2 * sizeof(Summary))) != cudaSuccess) {
         cudaFree(gm);
         cudaFree(tm);
         delete g;
@@ -461,6 +504,10 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     g->tgt_of_edge = (int32_t *)(gm + off_tge);
     g->unit_first_t = (int32_t *)(gm + off_units);
     g->merge_t = (int32_t *)(gm + off_merge);
+    g->src_row_ptr = (int32_t *)(gm + off_srp);
+    g->tgt_by_src = (int32_t *)(gm + off_tbs);
+    g->unit_first_s = (int32_t *)(gm + off_ufs);
+    g->merge_s = (int32_t *)(gm + off_ms);
 
     K *keys_a = (K *)(tm + t_keys_a), *keys_b = (K *)(tm + t_keys_b);
     int *vals_a = (int *)(tm + t_vals_a), *vals_b = (int *)(tm + t_vals_b);
@@ -469,6 +516,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     int *c1 = (int *)(tm + t_c1), *c2 = (int *)(tm + t_c2);
     int *tot = (int *)(tm + t_tot);
     Summary *dsum = (Summary *)(tm + t_sum);
+    Summary *dsum_src = dsum + 1;  // the by-source pass
 
     const int TB = 256;
     do {
@@ -503,7 +551,28 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         k_merge_write<<<blocks_for(L, TB), TB, 0, stream>>>(c1, c2, (int)L, g->merge_t);
         count_launch();
         if ((ce = cudaGetLastError()) != cudaSuccess) break;
-        if ((ce = cudaMemcpyAsync(host_sum, dsum, sizeof(Summary), cudaMemcpyDeviceToHost, stream)) !=
+        // the by-source view (for the backward pass): sort (source, target) keys
+        if ((ce = cudaMemsetAsync(dsum_src, 0, sizeof(Summary), stream)) != cudaSuccess) break;
+        k_copy_total<<<1, 1, 0, stream>>>(dsum, dsum_src);
+        k_csc_keys<K><<<blocks_for(cap, TB), TB, 0, stream>>>(g->row_ptr, g->col, L, dsum, cap, sentinel, keys_a,
+                                                              vals_a);
+        count_launch(2);
+        {
+            K *keys_s2;
+            int *vals_s2;
+            radix_sort<K>(keys_a, vals_a, keys_b, vals_b, cap, bits, hist, scan_tmp, stream, &keys_s2, &vals_s2);
+            k_csc_view<K><<<blocks_for(cap, TB), TB, 0, stream>>>(keys_s2, dsum, L, g->tgt_by_src);
+            k_row_ptr<K><<<blocks_for(S + 1, TB), TB, 0, stream>>>(keys_s2, dsum, S, L, g->src_row_ptr);
+            k_unit_first<<<blocks_for(max_units, TB), TB, 0, stream>>>(g->src_row_ptr, (int)S, dsum,
+                                                                       g->unit_first_s);
+            k_merge_flags<<<blocks_for(S, TB), TB, 0, stream>>>(g->src_row_ptr, (int)S, c1, dsum_src);
+            count_launch(4);
+            exclusive_scan(c1, c2, (int)S, &dsum_src->n_merge, scan_tmp, stream);
+            k_merge_write<<<blocks_for(S, TB), TB, 0, stream>>>(c1, c2, (int)S, g->merge_s);
+            count_launch();
+        }
+        if ((ce = cudaGetLastError()) != cudaSuccess) break;
+        if ((ce = cudaMemcpyAsync(host_sum, dsum, 2 * sizeof(Summary), cudaMemcpyDeviceToHost, stream)) !=
             cudaSuccess)
             break;
         ce = cudaStreamSynchronize(stream);
@@ -523,6 +592,8 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         g->max_deg = host_sum->max_deg;
         g->n_units = (g->nnz + kUnitEdges - 1) / kUnitEdges;
         g->n_merge = host_sum->n_merge;
+        g->n_merge_s = host_sum[1].n_merge;
+        g->max_out_deg = host_sum[1].max_deg;
         // A graph with at least a quarter of all (target, source) pairs may run
         // the masked-dense tensor-core kernel; it keeps the pairs as bits
         // (none for a complete graph). Without room for the bits the graph

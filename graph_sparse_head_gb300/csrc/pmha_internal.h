@@ -40,6 +40,14 @@ struct pmha_graph {
     int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
     int32_t *unit_first_t = nullptr;  // n_units, target of each unit's first position
     int32_t *merge_t = nullptr;       // n_merge, targets to merge (crossing a unit boundary, or without edges)
+    // The same edges by source (for the backward pass): positions sorted by
+    // (source, target); units of kUnitEdges positions; sources to merge.
+    int32_t *src_row_ptr = nullptr;   // S + 1
+    int32_t *tgt_by_src = nullptr;    // nnz, target per by-source position
+    int32_t *unit_first_s = nullptr;  // n_units, source of each unit's first position
+    int32_t *merge_s = nullptr;       // n_merge_s, sources crossing a unit boundary, or without edges
+    int64_t n_merge_s = 0;
+    int64_t max_out_deg = 0;
     // Dense graphs (most (target, source) pairs are edges): the adjacency as
     // bits, row t = words [t * adj_words_per_row, ...), bit s % 32 of word s / 32.
     bool dense = false;               // the masked-dense kernel may run this graph
@@ -127,6 +135,35 @@ struct EdgeArgs {
 bool edge_supported(int64_t E, int64_t H, TcType t);
 pmha_status edge_attention(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
 pmha_status split_merge(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------- backward
+struct BwdAttnArgs {
+    const void *q;         // projected q rows (B, L) of pitch q_ld, intermediate type
+    int64_t q_ld;
+    const void *k, *v;     // projected k, v rows (B, S) of pitch kv_ld
+    int64_t kv_ld;
+    const void *dmixed;    // (B, L, E) intermediate type
+    const float *ml;       // (B, L, H, 2) forward softmax statistics (log2 units)
+    const float *D;        // (B, L, H) dot(dmixed, mixed) per head
+    const uint8_t *kpm;    // (B, S) or null
+    float *dq, *dk, *dv;   // (B, L, E), (B, S, E), (B, S, E), scaled
+    float *part_dq;        // (B, 2 n_units, E) partial sums of rows crossing a unit
+    float *part_dkv;       // (B, 2 n_units, 2E)
+    int64_t B, E, H;
+};
+// Lane shape of the per-edge backward kernels (false: no kernel).
+bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lph);
+pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t rows, int64_t E, int64_t H, float *D,
+                       cudaStream_t s);
+// Steps 2-4 backward: dq over the per-target view, dk and dv over the per-source view.
+pmha_status bwd_attention(TcType t, const pmha_graph *g, const BwdAttnArgs &x, cudaStream_t s);
+// C (M x N) (+)= A (M x K) . B (K x N) on CUDA cores, fp32 accumulation.
+pmha_status bwd_gemm_nn(TcType ta, TcType tb, TcType tc, const void *A, int64_t lda, const void *B, int64_t ldb,
+                        void *C, int64_t ldc, int64_t M, int64_t N, int64_t K, bool accumulate, cudaStream_t s);
+// dW (K x N) = A^T B over M rows and/or db (K) = column sums of A; deterministic chunked sums.
+pmha_status bwd_gemm_tn(TcType ta, TcType tb, const void *A, int64_t lda, const void *B, int64_t ldb, int64_t M,
+                        int64_t K, int64_t N, float *dW, float *db, float *scratch, int64_t chunks, cudaStream_t s);
+pmha_status bwd_convert(const float *in, int64_t n, TcType out_t, void *out, cudaStream_t s);
 
 // ---------------------------------------------------------------- dense graphs
 struct DenseInputs {

@@ -238,6 +238,47 @@ pmha_status pmha_forward_noalloc(const pmha_graph *graph, const pmha_params *par
                                  const uint8_t *key_padding_mask, int64_t batch, void *output,
                                  pmha_wmode wmode, float *weights, pmha_stream stream);
 
+/*
+ * pmha_backward - gradients of the layer (the chain rule of kpnn2
+ * PackedMultiheadAttention, Notes steps 1-5) for dout = dLoss/d(output).
+ * Like the page's training path it recomputes the forward from the inputs
+ * instead of keeping per-edge tensors, so it takes the forward's inputs:
+ *  query, key, value, key_padding_mask, batch  as for pmha_forward;
+ *  dout    device (B, L, E), params->dtype;
+ *  dquery  device (B, L, E), dkey and dvalue device (B, S, E), params->dtype,
+ *          or NULL (not computed). When two inputs are one tensor (the same
+ *          pointer), their gradient is the sum of both roles' gradients and
+ *          goes to the one buffer they share (their non-NULL gradient
+ *          pointers must then be equal). Written, not accumulated.
+ *  grads   device float32 parameter gradients, any member NULL to skip it:
+ *          wq, wk, wv, wo (E, E) like the weights, bq, bk, bv, bo (E);
+ *          summed over the batch; written, not accumulated. NULL skips all.
+ *  workspace  device scratch of pmha_backward_workspace_size() bytes,
+ *          256-byte aligned.
+ * Sums run in a fixed order: results are deterministic. Supported shapes:
+ * embed_dim <= 512 whose lanes split evenly over heads (returns
+ * PMHA_ERR_UNSUPPORTED otherwise, and the size function returns 0).
+ * Errors as pmha_forward; the call does not synchronize.
+ */
+typedef struct {
+    float *wq, *wk, *wv, *wo;
+    float *bq, *bk, *bv, *bo;
+} pmha_grads;
+size_t pmha_backward_workspace_size(const pmha_graph *graph, const pmha_params *params, int64_t batch);
+pmha_status pmha_backward(const pmha_graph *graph, const pmha_params *params, const void *query,
+                          const void *key, const void *value, const uint8_t *key_padding_mask,
+                          int64_t batch, const void *dout, void *dquery, void *dkey, void *dvalue,
+                          const pmha_grads *grads, void *workspace, size_t workspace_bytes,
+                          pmha_stream stream);
+
+/*
+ * pmha_graph_export_by_source - the per-source view the backward pass walks:
+ * src_row_ptr (S + 1) and, per position, its target (nnz_total), positions
+ * ordered by (source, target). Device int32 buffers; NULL skips one.
+ */
+pmha_status pmha_graph_export_by_source(const pmha_graph *graph, int32_t *src_row_ptr, int32_t *target,
+                                        pmha_stream stream);
+
 /* Message describing the last failure of a call made by this thread ("" if none). */
 const char *pmha_last_error(void);
 
