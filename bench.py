@@ -372,6 +372,34 @@ def bench_ours(args):
               "mask": "per-sample end padding, n_b ~ U[S/2, S] keys kept (value counts every edge)",
               "stages_avg_us": {k: 1e3 * v[1] / max(v[0], 1) for k, v in m_prof.items()}}
 
+    # ---- the backward pass (pmha_backward: forward recompute + gradients of
+    # inputs, weights and biases) for a seeded dout, timed the same way
+    back = None
+    if not args.no_backward:
+        g_out = torch.from_numpy(synth.make_tokens(np.random.default_rng(11 + rank), B, w.query_features,
+                                                   w.embed_dim, w.dtype)).to(torch.bfloat16).to(dev)
+        ws_b = torch.empty(max(1, pmha.pmha_backward_workspace_size(graph, params, B)), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            pmha.pmha_backward(graph, params, x, kv, kv, g_out, workspace=ws_b, stream=stream)
+        pmha.pmha_device_status()
+        back_steps = max(3, min(args.steps, 30))
+        pmha.pmha_profile_enable(True)
+        pmha.pmha_profile_read()
+        b_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(back_steps)]
+        for i, (e_start, e_end) in enumerate(b_ev):
+            flush.fill_(i & 0xFF)
+            e_start.record(stream)
+            pmha.pmha_backward(graph, params, x, kv, kv, g_out, workspace=ws_b, stream=stream)
+            e_end.record(stream)
+        torch.cuda.synchronize()
+        pmha.pmha_profile_enable(False)
+        b_prof = pmha.pmha_profile_read()
+        pmha.pmha_device_status()
+        b_ms = max_over_ranks(sum(e0_.elapsed_time(e1_) for e0_, e1_ in b_ev) / back_steps, world, dev)
+        back = {"ms_per_step": b_ms, "value": world * float(B) * nnz * H / (b_ms / 1e3), "unit": UNIT,
+                "steps": back_steps, "what": "pmha_backward: forward recompute, input, weight and bias gradients",
+                "stages_avg_us": {k: 1e3 * v[1] / max(v[0], 1) for k, v in b_prof.items()}}
+
     # ---- end to end through the C ABI with host buffers (pinned), per step:
     # copy the step's tokens in, run, copy the output back
     xh = torch.from_numpy(xq_np).to(torch.bfloat16).pin_memory()
@@ -451,7 +479,7 @@ def bench_ours(args):
             "gpu_launches": launches,
             "roofline": roof,
             "stages": stages,
-            "variants": {"key_padding_mask": masked},
+            "variants": {"key_padding_mask": masked, "backward": back},
             "cpu_baseline": cpu,
             "clocks": clocks,
             "wall_s_timed_region": wall,
@@ -472,6 +500,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(synth.WORKLOADS),
                     help="synthetic workload id (default: the skewed n=20,000 graph the metric is quoted on)")
     args = ap.parse_args(argv)

@@ -433,7 +433,7 @@ BwdLayout bwd_layout(const pmha_graph *g, const pmha_params *p, int64_t B)
     o += align256((size_t)(std::max(B * L, B * S) * E) * 4);
     b.chunks = std::max<int64_t>(1, std::min<int64_t>(64, std::max(B * L, B * S) / 4096));
     b.scratch = o;
-    o += align256((size_t)(b.chunks * E * E) * 4);
+    o += align256(bwd_gemm_scratch_bytes(B, L, S, E, param_type(p->dtype)));
     b.total = o;
     return b;
 }
@@ -738,11 +738,39 @@ pmha_status pmha_backward(const pmha_graph *g, const pmha_params *p, const void 
                 ml, false, &a);
     if (st != PMHA_OK) return st;
     // step 5
-    if ((st = bwd_gemm_nn(pt, pt, it, dout, E, p->wo, E, dmixed, E, B * L, E, E, false, s)) != PMHA_OK) return st;
-    if (grads && (grads->wo || grads->bo))
-        if ((st = bwd_gemm_tn(pt, it, dout, E, mixed, E, B * L, E, E, grads->wo, grads->bo, scratch, bl.chunks, s)) !=
-            PMHA_OK)
-            return st;
+    BwdGemmArgs gm;
+    gm.pt = pt;
+    gm.it = it;
+    gm.B = B;
+    gm.L = L;
+    gm.S = S;
+    gm.E = E;
+    gm.dout = dout;
+    gm.mixed = mixed;
+    gm.w[0] = p->wq;
+    gm.w[1] = p->wk;
+    gm.w[2] = p->wv;
+    gm.w[3] = p->wo;
+    for (int r = 0; r < 3; ++r) {
+        gm.in[r] = in[r];
+        gm.gx[r] = gx[r];
+    }
+    gm.dy[0] = dq;
+    gm.dy[1] = dk;
+    gm.dy[2] = dv;
+    gm.gw[0] = grads ? grads->wq : nullptr;
+    gm.gw[1] = grads ? grads->wk : nullptr;
+    gm.gw[2] = grads ? grads->wv : nullptr;
+    gm.gw[3] = grads ? grads->wo : nullptr;
+    gm.gb[0] = grads ? grads->bq : nullptr;
+    gm.gb[1] = grads ? grads->bk : nullptr;
+    gm.gb[2] = grads ? grads->bv : nullptr;
+    gm.gb[3] = grads ? grads->bo : nullptr;
+    gm.dmixed = dmixed;
+    gm.dx32 = dx;
+    gm.scratch = scratch;
+    gm.chunks = bl.chunks;
+    if ((st = bwd_step5(gm, s)) != PMHA_OK) return st;
     // steps 2-4
     if ((st = bwd_rowdot(it, dmixed, mixed, B * L, E, H, D, s)) != PMHA_OK) return st;
     BwdAttnArgs x;
@@ -764,39 +792,8 @@ pmha_status pmha_backward(const pmha_graph *g, const pmha_params *p, const void 
     x.E = E;
     x.H = H;
     if ((st = bwd_attention(it, g, x, s)) != PMHA_OK) return st;
-    // step 1: weight and bias gradients of the projections
-    const float *dy[3] = {dq, dk, dv};
-    const void *w[3] = {p->wq, p->wk, p->wv};
-    const int64_t rows[3] = {B * L, B * S, B * S};
-    float *gw[3] = {grads ? grads->wq : nullptr, grads ? grads->wk : nullptr, grads ? grads->wv : nullptr};
-    float *gb[3] = {grads ? grads->bq : nullptr, grads ? grads->bk : nullptr, grads ? grads->bv : nullptr};
-    for (int r = 0; r < 3; ++r)
-        if (gw[r] || gb[r])
-            if ((st = bwd_gemm_tn(TcType::F32, pt, dy[r], E, in[r], E, rows[r], E, E, gw[r], gb[r], scratch,
-                                  bl.chunks, s)) != PMHA_OK)
-                return st;
-    // input gradients: one sum per distinct input tensor
-    for (int r = 0; r < 3; ++r) {
-        bool seen = false;
-        for (int q = 0; q < r; ++q) seen |= in[q] == in[r];
-        if (seen) continue;
-        void *target = nullptr;
-        for (int q = r; q < 3; ++q)
-            if (in[q] == in[r] && gx[q]) {
-                target = gx[q];
-                break;
-            }
-        if (!target) continue;
-        bool first = true;
-        for (int q = r; q < 3; ++q) {
-            if (in[q] != in[r]) continue;
-            if ((st = bwd_gemm_nn(TcType::F32, pt, TcType::F32, dy[q], E, w[q], E, dx, E, rows[r], E, E, !first, s)) !=
-                PMHA_OK)
-                return st;
-            first = false;
-        }
-        if ((st = bwd_convert(dx, rows[r] * E, pt, target, s)) != PMHA_OK) return st;
-    }
+    // step 1: weight, bias and input gradients of the projections
+    if ((st = bwd_step1(gm, s)) != PMHA_OK) return st;
     return PMHA_OK;
 }
 

@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "pmha_internal.h"
 
 namespace pmha {
@@ -56,19 +58,26 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 // ---------------------------------------------------------------- D = dot(dmixed, mixed) per (row, head)
+// One warp per row: lane l takes channels l, l + 32, ...; each head's sum is
+// added over its channels in channel order through shared memory.
 template <typename T>
-__global__ void k_rowdot(const T *__restrict__ dmixed, const T *__restrict__ mixed, long long rows, int E, int H,
-                         float *__restrict__ D)
+__global__ void __launch_bounds__(256) k_rowdot(const T *__restrict__ dmixed, const T *__restrict__ mixed,
+                                                long long rows, int E, int H, float *__restrict__ D)
 {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= rows * H) return;
-    const long long r = i / H;
-    const int h = (int)(i - r * H), d = E / H;
-    const T *g = dmixed + r * E + h * d;
-    const T *o = mixed + r * E + h * d;
-    float acc = 0.f;
-    for (int c = 0; c < d; ++c) acc = __fmaf_rn(to_f(g[c]), to_f(o[c]), acc);
-    D[i] = acc;
+    __shared__ float prod[8][512];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const long long r = (long long)blockIdx.x * 8 + wib;
+    if (r >= rows) return;
+    const T *g = dmixed + r * E;
+    const T *o = mixed + r * E;
+    for (int c = lane; c < E; c += 32) prod[wib][c] = __fmul_rn(to_f(g[c]), to_f(o[c]));
+    __syncwarp();
+    const int d = E / H;
+    for (int h = lane; h < H; h += 32) {
+        float acc = 0.f;
+        for (int c = 0; c < d; ++c) acc = __fadd_rn(acc, prod[wib][h * d + c]);
+        D[r * H + h] = acc;
+    }
 }
 
 struct WalkArgs {
@@ -414,6 +423,23 @@ __global__ void __launch_bounds__(256) k_colsum_part(const TA *__restrict__ A, l
     P[chunk * K + c] = acc;
 }
 
+// out[c] = sum over tiles of P[tile][c] (P has n columns); one block per c
+__global__ void __launch_bounds__(256) k_sum_tiles(const float *__restrict__ P, long long n, int tiles,
+                                                   float *__restrict__ out)
+{
+    __shared__ float red[256];
+    const long long c = blockIdx.x;
+    float acc = 0.f;
+    for (int t = threadIdx.x; t < tiles; t += 256) acc = __fadd_rn(acc, P[(long long)t * n + c]);
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] = __fadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[c] = red[0];
+}
+
 // out[i] = sum over chunks of P[chunk][i], in chunk order
 __global__ void k_sum_chunks(const float *__restrict__ P, long long n, int chunks, float *__restrict__ out)
 {
@@ -429,6 +455,56 @@ __global__ void k_convert(const float *__restrict__ in, long long n, TO *__restr
 {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) out[i] = from_f<TO>(in[i]);
+}
+
+// out[c * ld_out + r] = in[r * ld_in + c] for r < M, c < E (converted); the
+// columns r in [M, Mpad) of out are zero. 64 x 64 tiles.
+// With colsum non-null, also writes the tile's 64-row column sums of the
+// input (in row order) to colsum[blockIdx.x * E + c].
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(256) k_transpose_cvt(const TIn *__restrict__ in, long long ld_in, long long M, int E,
+                                                       long long Mpad, TOut *__restrict__ out, long long ld_out,
+                                                       float *__restrict__ colsum)
+{
+    __shared__ float tile[64][65];
+    const long long r0 = (long long)blockIdx.x * 64;
+    const int c0 = blockIdx.y * 64;
+    const int lo = threadIdx.x & 63, hi = threadIdx.x >> 6;
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+        const int rr = hi + 4 * k;
+        const long long r = r0 + rr;
+        tile[rr][lo] = (r < M && c0 + lo < E) ? to_f(in[r * ld_in + c0 + lo]) : 0.f;
+    }
+    __syncthreads();
+    if (colsum && threadIdx.x < 64 && c0 + threadIdx.x < E) {
+        float acc = 0.f;
+        for (int rr = 0; rr < 64; ++rr) acc = __fadd_rn(acc, tile[rr][threadIdx.x]);
+        colsum[(long long)blockIdx.x * E + c0 + threadIdx.x] = acc;
+    }
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+        const int cc = hi + 4 * k;
+        const long long r = r0 + lo;
+        if (c0 + cc < E && r < Mpad) out[(long long)(c0 + cc) * ld_out + r] = from_f<TOut>(tile[lo][cc]);
+    }
+}
+
+// fp32 rows -> fp16 rows of another pitch (a slot of a concatenated row);
+// four channels per thread (E % 4 == 0, pitches multiples of 4)
+__global__ void k_rows_f16(const float *__restrict__ in, long long rows, int E, __half *__restrict__ out,
+                           long long ld_out)
+{
+    const long long i = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= rows * E) return;
+    const long long r = i / E;
+    const int c = (int)(i - r * E);
+    const float4 v = *reinterpret_cast<const float4 *>(in + i);
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t *>(&a);
+    w.y = *reinterpret_cast<const uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(out + r * ld_out + c) = w;
 }
 
 inline unsigned blocks(long long n, int t) { return (unsigned)((n + t - 1) / t); }
@@ -485,11 +561,11 @@ pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t 
 {
     StageTimer timer("bwd_rowdot", s);
     if (t == TcType::F16)
-        k_rowdot<__half><<<blocks(rows * H, 256), 256, 0, s>>>((const __half *)dmixed, (const __half *)mixed, rows,
-                                                              (int)E, (int)H, D);
+        k_rowdot<__half><<<blocks(rows, 8), 256, 0, s>>>((const __half *)dmixed, (const __half *)mixed, rows, (int)E,
+                                                         (int)H, D);
     else
-        k_rowdot<float><<<blocks(rows * H, 256), 256, 0, s>>>((const float *)dmixed, (const float *)mixed, rows,
-                                                             (int)E, (int)H, D);
+        k_rowdot<float><<<blocks(rows, 8), 256, 0, s>>>((const float *)dmixed, (const float *)mixed, rows, (int)E,
+                                                        (int)H, D);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;
@@ -642,6 +718,207 @@ pmha_status bwd_gemm_tn(TcType ta, TcType tb, const void *A, int64_t lda, const 
         else k_colsum_part<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16 *)A, lda, M, (int)K, rpc, scratch);
         k_sum_chunks<<<blocks(K, 256), 256, 0, s>>>(scratch, K, (int)chunks, db);
         count_launch(2);
+    }
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+// ---------------------------------------------------------------- steps 5 and 1
+namespace {
+bool use_tc(const BwdGemmArgs &g) { return g.pt == TcType::BF16 && g.E % 128 == 0 && gemm_tc_supported(g.E); }
+int64_t pad64(int64_t m) { return (m + 63) / 64 * 64; }
+constexpr int64_t kMaxSplit = 256;
+
+// bump allocator over the caller's scratch (256-byte steps)
+struct Bump {
+    char *p;
+    size_t used = 0;
+    template <typename T>
+    T *take(size_t n)
+    {
+        T *r = (T *)(p + used);
+        used += (n * sizeof(T) + 255) & ~(size_t)255;
+        return r;
+    }
+};
+
+template <typename TIn, typename TOut>
+void transpose_cvt(const void *in, int64_t ld_in, int64_t M, int64_t E, int64_t Mpad, void *out, int64_t ld_out,
+                   cudaStream_t s, float *colsum = nullptr)
+{
+    StageTimer timer("bwd_transpose", s);
+    dim3 grid(blocks(Mpad, 64), blocks(E, 64));
+    k_transpose_cvt<TIn, TOut><<<grid, 256, 0, s>>>((const TIn *)in, ld_in, M, (int)E, Mpad, (TOut *)out, ld_out,
+                                                    colsum);
+    count_launch();
+}
+
+// db (E) = column sums of an (M x E) matrix from the per-64-row-tile sums a
+// transpose_cvt left in colsum: one block per column, thread i adds tiles
+// i, i + 256, ... in order, then a fixed-order tree over the 256 threads
+void bias_from_tiles(const float *colsum, int64_t M, int64_t E, float *db, cudaStream_t s)
+{
+    StageTimer timer("bwd_bias", s);
+    k_sum_tiles<<<(unsigned)E, 256, 0, s>>>(colsum, E, (int)((M + 63) / 64), db);
+    count_launch();
+}
+
+// dW (E x E) = sum_r dYT[o][r] XT[i][r] on the tensor cores (split K, fp32 partials, ordered sum)
+pmha_status dw_tc(const __half *dyT, const __half *xT, int64_t E, int64_t Mpad, float *dW, float *part,
+                  cudaStream_t s)
+{
+    const int64_t ksplit = std::min<int64_t>(kMaxSplit, std::max<int64_t>(1, Mpad / 64));
+    pmha_status st = gemm_tc_general(TcType::F16, TcType::F32, dyT, Mpad, E, Mpad, xT, Mpad, E, part, E, ksplit,
+                                     "bwd_dw", s);
+    if (st != PMHA_OK) return st;
+    const int64_t kb = Mpad / 64, per = (kb + ksplit - 1) / ksplit, used = (kb + per - 1) / per;
+    k_sum_chunks<<<blocks(E * E, 256), 256, 0, s>>>(part, E * E, (int)used, dW);
+    count_launch();
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+}  // namespace
+
+size_t bwd_gemm_scratch_bytes(int64_t B, int64_t L, int64_t S, int64_t E, TcType pt)
+{
+    const int64_t Mq = B * L, Mk = B * S, M = std::max(Mq, Mk);
+    const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(64, M / 4096));
+    size_t simt = ((size_t)(chunks * E * E) * 4 + 255) & ~(size_t)255;
+    if (!(pt == TcType::BF16 && E % 128 == 0)) return simt;
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const int64_t Mqp = pad64(Mq), Mkp = pad64(Mk), Mp = std::max(Mqp, Mkp);
+    size_t tc = al((size_t)(E * E) * 2)                  // Wo^T
+                + al((size_t)(E * 3 * E) * 2)            // the weights of one input's roles, transposed
+                + 2 * al((size_t)(E * Mqp) * 2)          // dout^T, mixed^T
+                + 3 * al((size_t)(E * Mp) * 2)           // dq^T, dk^T, dv^T
+                + 3 * al((size_t)(E * Mp) * 2)           // the inputs transposed
+                + al((size_t)(M * 3 * E) * 2)            // one input's dY rows in fp16
+                + al((size_t)(kMaxSplit * E * E) * 4)    // split-K partials
+                + al((size_t)(Mp / 64 * E) * 4);         // per-tile column sums
+    return std::max(simt, tc) + 256;
+}
+
+pmha_status bwd_step5(const BwdGemmArgs &g, cudaStream_t s)
+{
+    const int64_t E = g.E, M = g.B * g.L;
+    pmha_status st;
+    if (use_tc(g)) {
+        Bump bump{(char *)g.scratch};
+        __nv_bfloat16 *woT = bump.take<__nv_bfloat16>((size_t)(E * E));
+        transpose_cvt<__nv_bfloat16, __nv_bfloat16>(g.w[3], E, E, E, E, woT, E, s);
+        // dmixed = dout Wo = dout (Wo^T)^T
+        if ((st = gemm_tc_general(TcType::BF16, g.it, g.dout, E, M, E, woT, E, E, g.dmixed, E, 1, "bwd_dmixed", s)) !=
+            PMHA_OK)
+            return st;
+        if (g.gw[3]) {
+            const int64_t Mp = pad64(M);
+            __half *doutT = bump.take<__half>((size_t)(E * Mp));
+            __half *mixT = bump.take<__half>((size_t)(E * Mp));
+            float *part = bump.take<float>((size_t)(kMaxSplit * E * E));
+            float *cs = g.gb[3] ? bump.take<float>((size_t)(Mp / 64 * E)) : nullptr;
+            transpose_cvt<__nv_bfloat16, __half>(g.dout, E, M, E, Mp, doutT, Mp, s, cs);
+            transpose_cvt<__half, __half>(g.mixed, E, M, E, Mp, mixT, Mp, s);
+            if ((st = dw_tc(doutT, mixT, E, Mp, g.gw[3], part, s)) != PMHA_OK) return st;
+            if (cs) bias_from_tiles(cs, M, E, g.gb[3], s);
+        }
+        if (g.gb[3] && !g.gw[3])
+            if ((st = bwd_gemm_tn(g.pt, g.it, g.dout, E, g.mixed, E, M, E, E, nullptr, g.gb[3], (float *)g.scratch,
+                                  g.chunks, s)) != PMHA_OK)
+                return st;
+        PMHA_CUDA_TRY(cudaGetLastError());
+        return PMHA_OK;
+    }
+    if ((st = bwd_gemm_nn(g.pt, g.pt, g.it, g.dout, E, g.w[3], E, g.dmixed, E, M, E, E, false, s)) != PMHA_OK) return st;
+    if (g.gw[3] || g.gb[3])
+        if ((st = bwd_gemm_tn(g.pt, g.it, g.dout, E, g.mixed, E, M, E, E, g.gw[3], g.gb[3], (float *)g.scratch,
+                              g.chunks, s)) != PMHA_OK)
+            return st;
+    return PMHA_OK;
+}
+
+pmha_status bwd_step1(const BwdGemmArgs &g, cudaStream_t s)
+{
+    const int64_t E = g.E;
+    const int64_t rows[3] = {g.B * g.L, g.B * g.S, g.B * g.S};
+    pmha_status st;
+    if (!use_tc(g)) {
+        // bias gradients: column sums of dq, dk, dv (ordered chunks)
+        for (int r = 0; r < 3; ++r)
+            if (g.gb[r])
+                if ((st = bwd_gemm_tn(TcType::F32, g.pt, g.dy[r], E, g.in[r], E, rows[r], E, E, nullptr, g.gb[r],
+                                      (float *)g.scratch, g.chunks, s)) != PMHA_OK)
+                    return st;
+        for (int r = 0; r < 3; ++r)
+            if (g.gw[r])
+                if ((st = bwd_gemm_tn(TcType::F32, g.pt, g.dy[r], E, g.in[r], E, rows[r], E, E, g.gw[r], nullptr,
+                                      (float *)g.scratch, g.chunks, s)) != PMHA_OK)
+                    return st;
+        for (int r = 0; r < 3; ++r) {
+            bool seen = false;
+            for (int q = 0; q < r; ++q) seen |= g.in[q] == g.in[r];
+            if (seen || !g.gx[r]) continue;
+            bool first = true;
+            for (int q = r; q < 3; ++q) {
+                if (g.in[q] != g.in[r]) continue;
+                if ((st = bwd_gemm_nn(TcType::F32, g.pt, TcType::F32, g.dy[q], E, g.w[q], E, g.dx32, E, rows[r], E, E,
+                                      !first, s)) != PMHA_OK)
+                    return st;
+                first = false;
+            }
+            if ((st = bwd_convert(g.dx32, rows[r] * E, g.pt, g.gx[r], s)) != PMHA_OK) return st;
+        }
+        return PMHA_OK;
+    }
+    Bump bump{(char *)g.scratch};
+    (void)bump.take<__nv_bfloat16>((size_t)(E * E));  // Wo^T of step 5 (not needed here; keeps offsets stable)
+    __half *wsub = bump.take<__half>((size_t)(E * 3 * E));
+    const int64_t Mp = pad64(std::max(rows[0], rows[1]));
+    (void)bump.take<__half>((size_t)(E * pad64(rows[0])));
+    (void)bump.take<__half>((size_t)(E * pad64(rows[0])));
+    __half *dyT[3], *xT[3];
+    for (int r = 0; r < 3; ++r) dyT[r] = bump.take<__half>((size_t)(E * Mp));
+    for (int r = 0; r < 3; ++r) xT[r] = bump.take<__half>((size_t)(E * Mp));
+    __half *dy16 = bump.take<__half>((size_t)(std::max(rows[0], rows[1]) * 3 * E));
+    float *part = bump.take<float>((size_t)(kMaxSplit * E * E));
+    float *cs = bump.take<float>((size_t)(Mp / 64 * E));
+    // weight gradients dW_r = dY_r^T X_r: both transposed to fp16 (tokens along K);
+    // the bias gradient (column sums of dY_r) comes out of the same transpose
+    for (int r = 0; r < 3; ++r) {
+        if (!g.gw[r] && !g.gb[r]) continue;
+        const int64_t mp = pad64(rows[r]);
+        transpose_cvt<float, __half>(g.dy[r], E, rows[r], E, mp, dyT[r], mp, s, g.gb[r] ? cs : nullptr);
+        if (g.gb[r]) bias_from_tiles(cs, rows[r], E, g.gb[r], s);
+        if (!g.gw[r]) continue;
+        int src = r;
+        for (int q = 0; q < r; ++q)
+            if (g.in[q] == g.in[r] && g.gw[q]) {
+                src = q;
+                break;
+            }
+        if (src == r) transpose_cvt<__nv_bfloat16, __half>(g.in[r], E, rows[r], E, mp, xT[r], mp, s);
+        if ((st = dw_tc(dyT[r], xT[src], E, mp, g.gw[r], part, s)) != PMHA_OK) return st;
+    }
+    // input gradients: dX = sum over the roles of X of dY_r W_r, one K = n_roles * E product
+    for (int r = 0; r < 3; ++r) {
+        bool seen = false;
+        for (int q = 0; q < r; ++q) seen |= g.in[q] == g.in[r];
+        if (seen || !g.gx[r]) continue;
+        int roles[3], nr = 0;
+        for (int q = r; q < 3; ++q)
+            if (g.in[q] == g.in[r]) roles[nr++] = q;
+        const int64_t K = nr * E;
+        for (int i = 0; i < nr; ++i) {
+            const int q = roles[i];
+            {
+                StageTimer pack_timer("bwd_pack", s);
+                k_rows_f16<<<blocks(rows[r] * E / 4, 256), 256, 0, s>>>(g.dy[q], rows[r], (int)E, dy16 + i * E, K);
+                count_launch();
+            }
+            transpose_cvt<__nv_bfloat16, __half>(g.w[q], E, E, E, E, wsub + i * E, K, s);
+        }
+        if ((st = gemm_tc_general(TcType::F16, g.pt, dy16, K, rows[r], K, wsub, K, E, g.gx[r], E, 1, "bwd_dx", s)) !=
+            PMHA_OK)
+            return st;
     }
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;

@@ -66,6 +66,10 @@ struct TcArgs {
     void *out;
     long long ldy;
     int *err;
+    // split-K (float output only): tile t covers K blocks [ks * kb_per, ..) of
+    // split ks = t % ksplit and writes its partial at out + ks * part_stride
+    int ksplit, kb_per;
+    long long part_stride;
 };
 
 // Two fp32 values to one 32-bit word of the output type. fp16 outputs also
@@ -135,8 +139,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles_n = a.N / BN;
-    const int n_tiles = ((a.M + BM - 1) / BM) * n_tiles_n;
+    const int n_tiles = ((a.M + BM - 1) / BM) * n_tiles_n * a.ksplit;
     const int k_blocks = a.K / BK;
+    // tile -> (row block, column block, K split)
+    auto decode = [&](int tile, int &m_blk, int &n_blk, int &kb0, int &kb1) {
+        const int ks = tile % a.ksplit, mn = tile / a.ksplit;
+        m_blk = mn / n_tiles_n;
+        n_blk = mn % n_tiles_n;
+        kb0 = ks * a.kb_per;
+        kb1 = min(k_blocks, kb0 + a.kb_per);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -173,12 +185,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             int stage = 0;
             uint32_t phase = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
-                const int m_blk = tile / n_tiles_n, n_blk = tile % n_tiles_n;
+                int m_blk, n_blk, kb0, kb1;
+                decode(tile, m_blk, n_blk, kb0, kb1);
                 const int n_glob = n_blk * BN;
                 const int seg = n_glob / a.E;
                 const int n_loc = n_glob - seg * a.E;
                 const CUtensorMap *tw = seg == 0 ? &tm_w0 : (seg == 1 ? &tm_w1 : &tm_w2);
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err)) break;
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, kStageBytes);
@@ -204,8 +217,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1u, abort_flag, a.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                int m_blk, n_blk, kb0, kb1;
+                decode(tile, m_blk, n_blk, kb0, kb1);
                 bool ok = true;
-                for (int kb = 0; kb < k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, a.err)) {
                         ok = false;
                         break;
@@ -217,7 +232,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                     for (int k = 0; k < BK / 16; ++k) {
                         // +32 bytes along K inside the swizzle atom = +2 in the address field
                         mma_f16kind(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc<TIn>(),
-                                    (kb > 0 || k > 0) ? 1u : 0u);
+                                    (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&empty[stage]));
                     if (++stage == kStages) {
@@ -251,12 +266,36 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             if (et == 0) bulk_wait_read1();  // the store that last read this buffer is done
             if (epi_sync_or(!ok)) break;     // one decision for all 128 threads
             tc_fence_after();
-            const int m_blk = tile / n_tiles_n, n_blk = tile % n_tiles_n;
+            int m_blk, n_blk, kb0, kb1;
+            decode(tile, m_blk, n_blk, kb0, kb1);
             const int n_glob = n_blk * BN;
+            const bool live = m_blk * BM + r < a.M;
+            if constexpr (std::is_same<TOut, float>::value) {
+                // fp32 partial of this K split, stored straight from registers
+                float *dst = (float *)a.out + (long long)(tile % a.ksplit) * a.part_stride +
+                             (long long)(m_blk * BM + r) * a.ldy + n_glob;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), v);
+                    if (live) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<uint4 *>(dst + c * 32 + 4 * q) =
+                                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&acc_empty[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                continue;
+            } else {
             const int seg = n_glob / a.E;
             const int n_loc = n_glob - seg * a.E;
             const __nv_bfloat16 *bias = a.bias[seg];
-            const bool live = m_blk * BM + r < a.M;
             uint8_t *sb = staging + buf * kOutTileBytes;
             bool range_bad = false;
 #pragma unroll 1
@@ -301,6 +340,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 acc = 0;
                 acc_phase ^= 1u;
             }
+            }  // 16-bit output
         }
         if (et == 0) bulk_wait_all();  // the CTA's shared memory must outlive its stores
     }
@@ -377,6 +417,9 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     a.ldy = ldy;
     a.err = device_error_word();
     if (!a.err) return PMHA_ERR_CUDA;
+    a.ksplit = 1;
+    a.kb_per = a.K / BK;
+    a.part_stride = 0;
 
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
     if (in_bf16 && out == TcType::F16) kern = k_gemm_tc<__nv_bfloat16, __half>;
@@ -398,6 +441,80 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     const int grid = std::min(n_tiles, num_sms());
     StageTimer timer(stage, stream);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw[0], mw[1], mw[2], my, a);
+    count_launch();
+    PMHA_CUDA_TRY(cudaGetLastError());
+    return PMHA_OK;
+}
+
+pmha_status gemm_tc_general(TcType in, TcType out, const void *X, int64_t ldx, int64_t M, int64_t K, const void *W,
+                            int64_t ldw, int64_t N, void *Y, int64_t ldy, int64_t ksplit, const char *stage,
+                            cudaStream_t stream)
+{
+    if (M <= 0) return PMHA_OK;
+    if (K % BK || N % BN || K <= 0 || N <= 0 || M > (int64_t)0x7fffffff - BM) {
+        set_error("gemm_tc_general: K must be a multiple of %d and N of %d", BK, BN);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    if (((uintptr_t)X & 15) || ((uintptr_t)W & 15) || ((uintptr_t)Y & 15) || (ldx * 2) % 16 || (ldw * 2) % 16 ||
+        (ldy * (out == TcType::F32 ? 4 : 2)) % 16) {
+        set_error("gemm_tc_general: operands must be 16-byte aligned with 16-byte row pitches");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (in == TcType::F32) {
+        set_error("gemm_tc_general: 16-bit operands only");
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    const bool in_bf16 = in == TcType::BF16;
+    CUtensorMap mx, mw, my;
+    if (!make_map(&mx, X, M, K, in_bf16, ldx) || !make_map(&mw, W, N, K, in_bf16, ldw)) {
+        set_error("gemm_tc_general: cuTensorMapEncodeTiled failed for X or W");
+        return PMHA_ERR_CUDA;
+    }
+    if (out != TcType::F32) {
+        if (!make_map(&my, Y, M, N, out == TcType::BF16, ldy)) {
+            set_error("gemm_tc_general: cuTensorMapEncodeTiled failed for Y");
+            return PMHA_ERR_CUDA;
+        }
+    } else {
+        my = mx;  // unused: float partials are stored without TMA
+    }
+    const int k_blocks = (int)(K / BK);
+    if (out != TcType::F32) ksplit = 1;
+    ksplit = std::max<int64_t>(1, std::min<int64_t>(ksplit, k_blocks));
+    const int kb_per = (int)((k_blocks + ksplit - 1) / ksplit);
+    ksplit = (k_blocks + kb_per - 1) / kb_per;  // every split gets at least one K block
+    TcArgs a;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.E = (int)N;  // one weight matrix
+    for (int i = 0; i < 3; ++i) a.bias[i] = nullptr;
+    a.out = Y;
+    a.ldy = ldy;
+    a.err = device_error_word();
+    if (!a.err) return PMHA_ERR_CUDA;
+    a.ksplit = (int)ksplit;
+    a.kb_per = kb_per;
+    a.part_stride = M * ldy;
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
+    if (out == TcType::F32) kern = in_bf16 ? k_gemm_tc<__nv_bfloat16, float> : k_gemm_tc<__half, float>;
+    else if (in_bf16) kern = out == TcType::F16 ? k_gemm_tc<__nv_bfloat16, __half> : k_gemm_tc<__nv_bfloat16, __nv_bfloat16>;
+    else kern = out == TcType::BF16 ? k_gemm_tc<__half, __nv_bfloat16> : k_gemm_tc<__half, __half>;
+    static std::mutex mu;
+    static std::set<std::pair<int, void *>> configured;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!configured.count({dev, (void *)kern})) {
+            PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+            configured.insert({dev, (void *)kern});
+        }
+    }
+    const int n_tiles = (int)(((M + BM - 1) / BM) * (N / BN) * ksplit);
+    const int grid = std::min(n_tiles, num_sms());
+    StageTimer timer(stage, stream);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw, mw, mw, my, a);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;

@@ -136,6 +136,14 @@ bool edge_supported(int64_t E, int64_t H, TcType t);
 pmha_status edge_attention(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
 pmha_status split_merge(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
 
+// Y (M x N) = X (M x K, pitch ldx) . W^T (W: N x K, pitch ldw) on the tensor
+// cores, one weight matrix, no bias, 16-bit operands of one type; out F16 or
+// BF16 (Y pitch ldy), or F32: K split in up to ksplit parts, part i stored at
+// Y + i * M * ldy (the caller sums them). K % 64 == 0, N % 128 == 0.
+pmha_status gemm_tc_general(TcType in, TcType out, const void *X, int64_t ldx, int64_t M, int64_t K, const void *W,
+                            int64_t ldw, int64_t N, void *Y, int64_t ldy, int64_t ksplit, const char *stage,
+                            cudaStream_t stream);
+
 // ---------------------------------------------------------------- backward
 struct BwdAttnArgs {
     const void *q;         // projected q rows (B, L) of pitch q_ld, intermediate type
@@ -164,6 +172,26 @@ pmha_status bwd_gemm_nn(TcType ta, TcType tb, TcType tc, const void *A, int64_t 
 pmha_status bwd_gemm_tn(TcType ta, TcType tb, const void *A, int64_t lda, const void *B, int64_t ldb, int64_t M,
                         int64_t K, int64_t N, float *dW, float *db, float *scratch, int64_t chunks, cudaStream_t s);
 pmha_status bwd_convert(const float *in, int64_t n, TcType out_t, void *out, cudaStream_t s);
+// Steps 5 and 1 of the backward pass: dmixed, out_proj's and the
+// projections' weight and bias gradients, the input gradients. Tensor cores
+// for bf16 layers with embed_dim % 128 == 0, else CUDA cores.
+struct BwdGemmArgs {
+    TcType pt, it;              // layer (parameter) type, intermediate type
+    int64_t B, L, S, E;
+    const void *dout, *mixed;   // (B, L, E) layer type, intermediate type
+    const void *w[4];           // wq, wk, wv, wo (E, E) layer type
+    const void *in[3];          // query, key, value (layer type)
+    const float *dy[3];         // dq, dk, dv (fp32)
+    void *gx[3];                // input gradients (layer type) or null; shared for shared inputs
+    float *gw[4], *gb[4];       // parameter gradients (q, k, v, o) or null
+    void *dmixed;               // out: (B, L, E) intermediate type
+    float *dx32;                // (max(B L, B S), E) fp32 accumulator (CUDA-core path)
+    void *scratch;              // bwd_gemm_scratch_bytes()
+    int64_t chunks;             // row chunks of the CUDA-core column sums
+};
+size_t bwd_gemm_scratch_bytes(int64_t B, int64_t L, int64_t S, int64_t E, TcType pt);
+pmha_status bwd_step5(const BwdGemmArgs &g, cudaStream_t s);
+pmha_status bwd_step1(const BwdGemmArgs &g, cudaStream_t s);
 
 // ---------------------------------------------------------------- dense graphs
 struct DenseInputs {
