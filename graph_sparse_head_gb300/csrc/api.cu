@@ -675,8 +675,8 @@ pmha_status pmha_edge_weights(const pmha_graph *g, const pmha_params *p, const v
 size_t pmha_backward_workspace_size(const pmha_graph *g, const pmha_params *p, int64_t batch)
 {
     if (check_params(g, p, batch) != PMHA_OK) return 0;
-    int cpl, lph;
-    if (!bwd_shape(p->embed_dim, p->num_heads, &cpl, &lph)) return 0;
+    int cpl, lpe;
+    if (!bwd_shape(p->embed_dim, p->num_heads, &cpl, &lpe, inter_type(p->dtype))) return 0;
     return bwd_layout(g, p, batch).total;
 }
 
@@ -697,8 +697,8 @@ pmha_status pmha_backward(const pmha_graph *g, const pmha_params *p, const void 
         set_error("embed_dim %lld gives rows that are not a multiple of 16 bytes", (long long)E);
         return PMHA_ERR_UNSUPPORTED;
     }
-    int cpl, lph;
-    if (!bwd_shape(E, H, &cpl, &lph)) {
+    int cpl, lpe;
+    if (!bwd_shape(E, H, &cpl, &lpe, inter_type(p->dtype))) {
         set_error("pmha_backward: no kernel for embed_dim %lld, num_heads %lld", (long long)E, (long long)H);
         return PMHA_ERR_UNSUPPORTED;
     }

@@ -108,25 +108,110 @@ __device__ __forceinline__ float head_sum(float x)
     return x;
 }
 
-// dq: one warp per (sample, unit of the per-target view). Lane owns CPL
-// channels; the warp's lanes past E idle in the arithmetic but shuffle.
-template <typename T, int CPL, int LPH>
-__global__ void __launch_bounds__(256) k_bwd_dq(WalkArgs a)
+#ifndef PMHA_BWD_PF
+#define PMHA_BWD_PF 1
+#endif
+#ifndef PMHA_BWD_WARPS
+#define PMHA_BWD_WARPS 4
+#endif
+constexpr int kBwdWarps = PMHA_BWD_WARPS;  // warps per block of the per-edge kernels
+constexpr int kPF = PMHA_BWD_PF;           // edges ahead in flight per slot (raw rows in registers)
+
+// A lane's CPL channels of one row, loaded as raw words (one vector load)
+// and converted to float only when used, so a prefetch does not wait.
+template <typename T, int CPL>
+struct RawRow {
+    static constexpr int kBytes = CPL * (int)sizeof(T);
+    static constexpr int kWords = kBytes >= 4 ? kBytes / 4 : 1;
+    uint32_t w[kWords];
+    __device__ __forceinline__ void load(const T *p, bool act)
+    {
+        if (!act) {
+#pragma unroll
+            for (int i = 0; i < kWords; ++i) w[i] = 0u;
+            return;
+        }
+        if constexpr (kBytes % 16 == 0) {
+#pragma unroll
+            for (int i = 0; i < kBytes / 16; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(reinterpret_cast<const char *>(p) + 16 * i);
+                w[4 * i] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+            }
+        } else if constexpr (kBytes == 8) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(p);
+            w[0] = v.x;
+            w[1] = v.y;
+        } else if constexpr (kBytes == 4) {
+            w[0] = *reinterpret_cast<const uint32_t *>(p);
+        } else {
+            w[0] = *reinterpret_cast<const unsigned short *>(p);
+        }
+    }
+    __device__ __forceinline__ float at(int c) const
+    {
+        if constexpr (sizeof(T) == 4) {
+            return __uint_as_float(w[c]);
+        } else {
+            const unsigned short h = (unsigned short)(w[c >> 1] >> ((c & 1) * 16));
+            return to_f(*reinterpret_cast<const T *>(&h));
+        }
+    }
+};
+
+// Sum over the lph lanes of one head (aligned groups inside a slot).
+__device__ __forceinline__ float head_sum_rt(float x, int lph)
 {
-    const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= (long long)a.B * a.n_units) return;
-    const int b = (int)(gw / a.n_units), u = (int)(gw - (long long)b * a.n_units);
+    for (int o = 1; o < lph; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// The per-edge backward kernels. Like the forward's streaming kernel, a
+// "slot" of LPE = E / CPL lanes owns one sample (a lane owns CPL channels),
+// and the P = 32 / LPE slots of a warp walk the same unit of the view for P
+// consecutive samples: the graph is shared, so their walks are identical.
+// The unit's other-end indices are staged in shared memory; the rows of the
+// next kPF edges are in flight in a register ring of raw words.
+//
+// dq: the per-target view; per edge it gathers k_s and v_s.
+template <typename T, int CPL, int LPE>
+__global__ void __launch_bounds__(kBwdWarps * 32) k_bwd_dq(WalkArgs a)
+{
+    constexpr int P = 32 / LPE;
+    __shared__ int sidx[kBwdWarps][kUnitEdges];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int slot = lane / LPE, grp = lane % LPE;
+    const long long gw = (long long)blockIdx.x * kBwdWarps + wib;
+    const long long groups = (a.B + P - 1) / P;
+    if (gw >= groups * a.n_units) return;
+    const int u = (int)(gw % a.n_units);
+    const int b0 = (int)(gw / a.n_units) * P;
+    const int b = min(b0 + slot, a.B - 1);
+    const bool live_slot = b0 + slot < a.B;
     const int e0 = u * kUnitEdges;
     const int e1 = (int)min((long long)e0 + kUnitEdges, a.nnz);
-    const int c0 = lane * CPL;
-    const bool act = c0 < a.E;
-    const int d = a.E / a.H, head = act ? c0 / d : 0;
+    const int c0 = grp * CPL;
+    const int d = a.E / a.H, head = c0 / d, lph = d / CPL > 1 ? d / CPL : 1;
     const T *Q = (const T *)a.q + (long long)b * a.L * a.q_ld;
     const T *G = (const T *)a.g + (long long)b * a.L * a.E;
     const T *K = (const T *)a.k + (long long)b * a.S * a.kv_ld;
     const T *V = (const T *)a.v + (long long)b * a.S * a.kv_ld;
     const uint8_t *kpm = a.kpm ? a.kpm + (long long)b * a.S : nullptr;
+    for (int p = e0 + lane; p < e1; p += 32) sidx[wib][p - e0] = a.idx[p];
+    __syncwarp();
+
+    RawRow<T, CPL> kr[kPF], vr[kPF];
+    auto fetch = [&](RawRow<T, CPL> &kd, RawRow<T, CPL> &vd, int p) {
+        if (p < e1) {
+            const int s = sidx[wib][p - e0];
+            kd.load(K + (long long)s * a.kv_ld + c0, true);
+            vd.load(V + (long long)s * a.kv_ld + c0, true);
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kPF; ++j) fetch(kr[j], vr[j], e0 + j);
 
     int t = a.unit_first[u];
     const bool first_started_here = a.row_ptr[t] == e0;
@@ -134,10 +219,13 @@ __global__ void __launch_bounds__(256) k_bwd_dq(WalkArgs a)
     int bound = a.row_ptr[t + 1];
     float q[CPL], gv[CPL], acc[CPL], m = 0.f, inv_l = 0.f, Dt = 0.f;
     auto load_row = [&]() {
+        RawRow<T, CPL> rq, rg;
+        rq.load(Q + (long long)t * a.q_ld + c0, true);
+        rg.load(G + (long long)t * a.E + c0, true);
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-            q[c] = act ? to_f(Q[(long long)t * a.q_ld + c0 + c]) : 0.f;
-            gv[c] = act ? to_f(G[(long long)t * a.E + c0 + c]) : 0.f;
+            q[c] = rq.at(c);
+            gv[c] = rg.at(c);
             acc[c] = 0.f;
         }
         const long long st = ((long long)b * a.L + t) * a.H + head;
@@ -148,61 +236,75 @@ __global__ void __launch_bounds__(256) k_bwd_dq(WalkArgs a)
     };
     auto finish = [&]() {
         const bool complete = (is_first ? first_started_here : true) && bound <= e1;
-        if (!act) return;
-        if (complete) {
-            float *o = a.out0 + ((long long)b * a.L + t) * a.E + c0;
+        if (!live_slot) return;
+        float *o = complete ? a.out0 + ((long long)b * a.L + t) * a.E + c0
+                            : a.part + ((long long)b * 2 * a.n_units + 2 * u + (is_first ? 0 : 1)) * a.E + c0;
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) o[c] = __fmul_rn(acc[c], a.inv_sqrt_d);
-        } else {
-            float *o = a.part + ((long long)b * 2 * a.n_units + 2 * u + (is_first ? 0 : 1)) * a.E + c0;
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) o[c] = __fmul_rn(acc[c], a.inv_sqrt_d);
-        }
+        for (int c = 0; c < CPL; ++c) o[c] = __fmul_rn(acc[c], a.inv_sqrt_d);
     };
     load_row();
-    for (int p = e0; p < e1; ++p) {
-        if (p >= bound) {
-            finish();
-            is_first = false;
-            do {
-                ++t;
-                bound = a.row_ptr[t + 1];
-            } while (bound <= p);
-            load_row();
-        }
-        const int s = a.idx[p];
-        if (kpm && kpm[s]) continue;  // a dropped key has no weight
-        float kk[CPL], vv[CPL], d1 = 0.f, d2 = 0.f;
+    for (int base = e0; base < e1; base += kPF) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            kk[c] = act ? to_f(K[(long long)s * a.kv_ld + c0 + c]) : 0.f;
-            vv[c] = act ? to_f(V[(long long)s * a.kv_ld + c0 + c]) : 0.f;
-            d1 = __fmaf_rn(q[c], kk[c], d1);
-            d2 = __fmaf_rn(gv[c], vv[c], d2);
-        }
-        d1 = head_sum<LPH>(d1);
-        d2 = head_sum<LPH>(d2);
-        const float w = __fmul_rn(ex2f(__fsub_rn(__fmul_rn(d1, a.score_scale), m)), inv_l);
-        const float ds = __fmul_rn(w, __fsub_rn(d2, Dt));
+        for (int j = 0; j < kPF; ++j) {
+            const int p = base + j;
+            if (p >= e1) break;
+            if (p >= bound) {
+                finish();
+                is_first = false;
+                do {
+                    ++t;
+                    bound = a.row_ptr[t + 1];
+                } while (bound <= p);
+                load_row();
+            }
+            const int s = sidx[wib][p - e0];
+            float kk[CPL], vv[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[c] = __fmaf_rn(ds, kk[c], acc[c]);
+            for (int c = 0; c < CPL; ++c) {
+                kk[c] = kr[j].at(c);
+                vv[c] = vr[j].at(c);
+            }
+            fetch(kr[j], vr[j], p + kPF);
+            float d1 = 0.f, d2 = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                d1 = __fmaf_rn(q[c], kk[c], d1);
+                d2 = __fmaf_rn(gv[c], vv[c], d2);
+            }
+            d1 = head_sum_rt(d1, lph);
+            d2 = head_sum_rt(d2, lph);
+            // a dropped key (key_padding_mask) has weight 0
+            const bool drop = kpm && kpm[s];
+            const float w =
+                (inv_l > 0.f && !drop) ? __fmul_rn(ex2f(__fsub_rn(__fmul_rn(d1, a.score_scale), m)), inv_l) : 0.f;
+            const float ds = __fmul_rn(w, __fsub_rn(d2, Dt));
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[c] = __fmaf_rn(ds, kk[c], acc[c]);
+        }
     }
     finish();
 }
 
-// dk and dv: one warp per (sample, unit of the per-source view).
-template <typename T, int CPL, int LPH>
-__global__ void __launch_bounds__(256) k_bwd_dkv(WalkArgs a)
+// dk and dv: the per-source view; per edge it gathers q_t, dmixed_t and the
+// target's (m, l, D) of the lane's head.
+template <typename T, int CPL, int LPE>
+__global__ void __launch_bounds__(kBwdWarps * 32) k_bwd_dkv(WalkArgs a)
 {
-    const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= (long long)a.B * a.n_units) return;
-    const int b = (int)(gw / a.n_units), u = (int)(gw - (long long)b * a.n_units);
+    constexpr int P = 32 / LPE;
+    __shared__ int sidx[kBwdWarps][kUnitEdges];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int slot = lane / LPE, grp = lane % LPE;
+    const long long gw = (long long)blockIdx.x * kBwdWarps + wib;
+    const long long groups = (a.B + P - 1) / P;
+    if (gw >= groups * a.n_units) return;
+    const int u = (int)(gw % a.n_units);
+    const int b0 = (int)(gw / a.n_units) * P;
+    const int b = min(b0 + slot, a.B - 1);
+    const bool live_slot = b0 + slot < a.B;
     const int e0 = u * kUnitEdges;
     const int e1 = (int)min((long long)e0 + kUnitEdges, a.nnz);
-    const int c0 = lane * CPL;
-    const bool act = c0 < a.E;
-    const int d = a.E / a.H, head = act ? c0 / d : 0;
+    const int c0 = grp * CPL;
+    const int d = a.E / a.H, head = c0 / d, lph = d / CPL > 1 ? d / CPL : 1;
     const T *Q = (const T *)a.q + (long long)b * a.L * a.q_ld;
     const T *G = (const T *)a.g + (long long)b * a.L * a.E;
     const T *K = (const T *)a.k + (long long)b * a.S * a.kv_ld;
@@ -210,6 +312,24 @@ __global__ void __launch_bounds__(256) k_bwd_dkv(WalkArgs a)
     const float *ML = a.ml + (long long)b * a.L * a.H * 2;
     const float *DD = a.D + (long long)b * a.L * a.H;
     const uint8_t *kpm = a.kpm ? a.kpm + (long long)b * a.S : nullptr;
+    for (int p = e0 + lane; p < e1; p += 32) sidx[wib][p - e0] = a.idx[p];
+    __syncwarp();
+
+    RawRow<T, CPL> qr[kPF], gr[kPF];
+    float mr[kPF], lr[kPF], dr[kPF];
+    auto fetch = [&](RawRow<T, CPL> &qd, RawRow<T, CPL> &gd, float &md, float &ld, float &dd, int p) {
+        if (p < e1) {
+            const int t = sidx[wib][p - e0];
+            qd.load(Q + (long long)t * a.q_ld + c0, true);
+            gd.load(G + (long long)t * a.E + c0, true);
+            const long long st = (long long)t * a.H + head;
+            md = ML[2 * st];
+            ld = ML[2 * st + 1];
+            dd = DD[st];
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kPF; ++j) fetch(qr[j], gr[j], mr[j], lr[j], dr[j], e0 + j);
 
     int s = a.unit_first[u];
     const bool first_started_here = a.row_ptr[s] == e0;
@@ -219,17 +339,20 @@ __global__ void __launch_bounds__(256) k_bwd_dkv(WalkArgs a)
     float kk[CPL], vv[CPL], ak[CPL], av[CPL];
     auto load_row = [&]() {
         dropped = kpm && kpm[s];
+        RawRow<T, CPL> rk, rv;
+        rk.load(K + (long long)s * a.kv_ld + c0, true);
+        rv.load(V + (long long)s * a.kv_ld + c0, true);
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-            kk[c] = act ? to_f(K[(long long)s * a.kv_ld + c0 + c]) : 0.f;
-            vv[c] = act ? to_f(V[(long long)s * a.kv_ld + c0 + c]) : 0.f;
+            kk[c] = rk.at(c);
+            vv[c] = rv.at(c);
             ak[c] = 0.f;
             av[c] = 0.f;
         }
     };
     auto finish = [&]() {
         const bool complete = (is_first ? first_started_here : true) && bound <= e1;
-        if (!act) return;
+        if (!live_slot) return;
         float *ok, *ov;
         if (complete) {
             ok = a.out0 + ((long long)b * a.S + s) * a.E + c0;
@@ -245,36 +368,46 @@ __global__ void __launch_bounds__(256) k_bwd_dkv(WalkArgs a)
         }
     };
     load_row();
-    for (int p = e0; p < e1; ++p) {
-        if (p >= bound) {
-            finish();
-            is_first = false;
-            do {
-                ++s;
-                bound = a.row_ptr[s + 1];
-            } while (bound <= p);
-            load_row();
-        }
-        if (dropped) continue;  // every edge of a dropped key has weight 0
-        const int t = a.idx[p];
-        const long long st = (long long)t * a.H + head;
-        const float m = ML[2 * st], l = ML[2 * st + 1], Dt = DD[st];
-        float qq[CPL], gg[CPL], d1 = 0.f, d2 = 0.f;
+    for (int base = e0; base < e1; base += kPF) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            qq[c] = act ? to_f(Q[(long long)t * a.q_ld + c0 + c]) : 0.f;
-            gg[c] = act ? to_f(G[(long long)t * a.E + c0 + c]) : 0.f;
-            d1 = __fmaf_rn(qq[c], kk[c], d1);
-            d2 = __fmaf_rn(gg[c], vv[c], d2);
-        }
-        d1 = head_sum<LPH>(d1);
-        d2 = head_sum<LPH>(d2);
-        const float w = l > 0.f ? __fmul_rn(ex2f(__fsub_rn(__fmul_rn(d1, a.score_scale), m)), __frcp_rn(l)) : 0.f;
-        const float ds = __fmul_rn(w, __fsub_rn(d2, Dt));
+        for (int j = 0; j < kPF; ++j) {
+            const int p = base + j;
+            if (p >= e1) break;
+            if (p >= bound) {
+                finish();
+                is_first = false;
+                do {
+                    ++s;
+                    bound = a.row_ptr[s + 1];
+                } while (bound <= p);
+                load_row();
+            }
+            float qq[CPL], gg[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            ak[c] = __fmaf_rn(ds, qq[c], ak[c]);
-            av[c] = __fmaf_rn(w, gg[c], av[c]);
+            for (int c = 0; c < CPL; ++c) {
+                qq[c] = qr[j].at(c);
+                gg[c] = gr[j].at(c);
+            }
+            const float m = mr[j], l = lr[j], Dt = dr[j];
+            fetch(qr[j], gr[j], mr[j], lr[j], dr[j], p + kPF);
+            float d1 = 0.f, d2 = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                d1 = __fmaf_rn(qq[c], kk[c], d1);
+                d2 = __fmaf_rn(gg[c], vv[c], d2);
+            }
+            d1 = head_sum_rt(d1, lph);
+            d2 = head_sum_rt(d2, lph);
+            // every edge of a dropped key (key_padding_mask) has weight 0
+            const float w = (l > 0.f && !dropped)
+                                ? __fmul_rn(ex2f(__fsub_rn(__fmul_rn(d1, a.score_scale), m)), __frcp_rn(l))
+                                : 0.f;
+            const float ds = __fmul_rn(w, __fsub_rn(d2, Dt));
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                ak[c] = __fmaf_rn(ds, qq[c], ak[c]);
+                av[c] = __fmaf_rn(w, gg[c], av[c]);
+            }
         }
     }
     finish();
@@ -510,14 +643,15 @@ __global__ void k_rows_f16(const float *__restrict__ in, long long rows, int E, 
 inline unsigned blocks(long long n, int t) { return (unsigned)((n + t - 1) / t); }
 
 template <typename T, int CPL>
-bool launch_walks_lph(int lph, const WalkArgs &dq, const WalkArgs &dkv, cudaStream_t s)
+bool launch_walks_lpe(int lpe, const WalkArgs &dq, const WalkArgs &dkv, cudaStream_t s)
 {
-    const unsigned grid = blocks((long long)dq.B * dq.n_units, 8);
-    switch (lph) {
+    const long long groups = (dq.B + 32 / lpe - 1) / (32 / lpe);
+    const unsigned grid = blocks(groups * dq.n_units, kBwdWarps);
+    switch (lpe) {
 #define PMHA_WALK(L)                                                    \
     case L:                                                             \
-        k_bwd_dq<T, CPL, L><<<grid, 256, 0, s>>>(dq);                   \
-        k_bwd_dkv<T, CPL, L><<<grid, 256, 0, s>>>(dkv);                 \
+        k_bwd_dq<T, CPL, L><<<grid, kBwdWarps * 32, 0, s>>>(dq);        \
+        k_bwd_dkv<T, CPL, L><<<grid, kBwdWarps * 32, 0, s>>>(dkv);      \
         return true;
         PMHA_WALK(1) PMHA_WALK(2) PMHA_WALK(4) PMHA_WALK(8) PMHA_WALK(16) PMHA_WALK(32)
 #undef PMHA_WALK
@@ -526,33 +660,37 @@ bool launch_walks_lph(int lph, const WalkArgs &dq, const WalkArgs &dkv, cudaStre
 }
 
 template <typename T>
-bool launch_walks(int cpl, int lph, const WalkArgs &dq, const WalkArgs &dkv, cudaStream_t s)
+bool launch_walks(int cpl, int lpe, const WalkArgs &dq, const WalkArgs &dkv, cudaStream_t s)
 {
     switch (cpl) {
-    case 1: return launch_walks_lph<T, 1>(lph, dq, dkv, s);
-    case 2: return launch_walks_lph<T, 2>(lph, dq, dkv, s);
-    case 4: return launch_walks_lph<T, 4>(lph, dq, dkv, s);
-    case 8: return launch_walks_lph<T, 8>(lph, dq, dkv, s);
-    case 16: return launch_walks_lph<T, 16>(lph, dq, dkv, s);
+    case 1: return launch_walks_lpe<T, 1>(lpe, dq, dkv, s);
+    case 2: return launch_walks_lpe<T, 2>(lpe, dq, dkv, s);
+    case 4: return launch_walks_lpe<T, 4>(lpe, dq, dkv, s);
+    case 8: return launch_walks_lpe<T, 8>(lpe, dq, dkv, s);
+    case 16: return launch_walks_lpe<T, 16>(lpe, dq, dkv, s);
     default: return false;
     }
 }
 
 }  // namespace
 
-// Channels per lane and lanes per head of the per-edge backward kernels.
-bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lph)
+// Channels per lane (CPL) and lanes per sample (LPE = E / CPL) of the
+// per-edge backward kernels: CPL the largest power of two up to 16 (fp16) or
+// 8 (fp32) that divides the head size, LPE a power of two up to 32.
+bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lpe, TcType t)
 {
-    if (H < 1 || E % H || E > 512) return false;
-    const int64_t c = E >= 32 ? E / 32 : 1;
-    if ((c & (c - 1)) || E % c) return false;
-    if (E >= 32 && E % 32) return false;
-    const int64_t d = E / H;
-    if (d % c) return false;
-    const int64_t l = d / c;
+    if (H < 1 || E % H) return false;
+#ifndef PMHA_BWD_CMAX
+#define PMHA_BWD_CMAX 16
+#endif
+    const int64_t d = E / H, cmax = t == TcType::F16 ? PMHA_BWD_CMAX : 8;
+    int64_t c = 1;
+    while (c * 2 <= cmax && d % (c * 2) == 0) c *= 2;
+    if (E % c) return false;
+    const int64_t l = E / c;
     if (l < 1 || l > 32 || (l & (l - 1))) return false;
     *cpl = (int)c;
-    *lph = (int)l;
+    *lpe = (int)l;
     return true;
 }
 
@@ -573,8 +711,8 @@ pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t 
 
 pmha_status bwd_attention(TcType t, const pmha_graph *g, const BwdAttnArgs &x, cudaStream_t s)
 {
-    int cpl, lph;
-    if (!bwd_shape(x.E, x.H, &cpl, &lph)) {
+    int cpl, lpe;
+    if (!bwd_shape(x.E, x.H, &cpl, &lpe, t)) {
         set_error("backward: no kernel for embed_dim %lld, num_heads %lld", (long long)x.E, (long long)x.H);
         return PMHA_ERR_UNSUPPORTED;
     }
@@ -614,8 +752,8 @@ pmha_status bwd_attention(TcType t, const pmha_graph *g, const BwdAttnArgs &x, c
     dkv.part = x.part_dkv;
     if (x.B * g->n_units > 0) {
         StageTimer timer("bwd_edges", s);
-        const bool ok = t == TcType::F16 ? launch_walks<__half>(cpl, lph, dq, dkv, s)
-                                         : launch_walks<float>(cpl, lph, dq, dkv, s);
+        const bool ok = t == TcType::F16 ? launch_walks<__half>(cpl, lpe, dq, dkv, s)
+                                         : launch_walks<float>(cpl, lpe, dq, dkv, s);
         if (!ok) {
             set_error("backward: no kernel for %d channels per lane", cpl);
             return PMHA_ERR_UNSUPPORTED;

@@ -159,8 +159,9 @@ struct BwdAttnArgs {
     float *part_dkv;       // (B, 2 n_units, 2E)
     int64_t B, E, H;
 };
-// Lane shape of the per-edge backward kernels (false: no kernel).
-bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lph);
+// Lane shape of the per-edge backward kernels for intermediate type t
+// (channels per lane, lanes per sample; false: no kernel).
+bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lpe, TcType t);
 pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t rows, int64_t E, int64_t H, float *D,
                        cudaStream_t s);
 // Steps 2-4 backward: dq over the per-target view, dk and dv over the per-source view.
