@@ -55,3 +55,23 @@ def test_full_bipartite_sampled_rows_and_weights():
     pmha.pmha_device_status()
     assert torch.equal(w, w2)
     g.destroy()
+
+
+def test_full_skewed_with_padding_mask_every_element():
+    # the benchmark's key_padding_mask variant: samples padded at the end
+    c = Case.workload(3)
+    kpm = synth.padding_mask(np.random.default_rng(7), c.B, c.S)
+    g, params, out, w = c.run(DEV, "none", kpm=kpm)
+    ref_out, _ = c.oracle(need_weights=False, kpm=kpm)
+    assert_close("workload 3 masked output", out.float().cpu().numpy(), ref_out, c.dt)
+    g.destroy()
+
+
+@pytest.mark.parametrize("wid", [3, 4, 5])
+def test_full_graph_backward_two_samples(wid):
+    # the workload's full graph and widths, two samples: every gradient element
+    from tests.test_gpu_backward import _check, _run
+    c = Case.workload(wid, batch=2)
+    g, got, ref, tensors = _run(c)
+    _check(got, ref, tensors, c.dt)
+    g.destroy()
