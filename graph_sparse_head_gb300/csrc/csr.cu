@@ -45,6 +45,7 @@ struct Summary {
     int nnz_total;
     int n_merge;
     int max_deg;
+    int n_empty;  // rows without edges
 };
 
 __device__ __forceinline__ int warp_inclusive_sum(int v)
@@ -378,6 +379,7 @@ __global__ void k_merge_flags(const int32_t *__restrict__ row_ptr, int L, int *_
     const int b = row_ptr[t], e = row_ptr[t + 1], deg = e - b;
     flag[t] = (deg == 0 || b / kUnitEdges != (e - 1) / kUnitEdges) ? 1 : 0;
     atomicMax(&sum->max_deg, deg);
+    if (deg == 0) atomicAdd(&sum->n_empty, 1);
 }
 
 __global__ void k_merge_write(const int *__restrict__ flag, const int *__restrict__ off, int L,
@@ -385,6 +387,14 @@ __global__ void k_merge_write(const int *__restrict__ flag, const int *__restric
 {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t < L && flag[t]) merge_t[off[t]] = t;
+}
+
+// Index of each target in the merge list (-1 when it is not there).
+__global__ void k_merge_pos(const int *__restrict__ flag, const int *__restrict__ off, int L,
+                            int32_t *__restrict__ merge_pos)
+{
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < L) merge_pos[t] = flag[t] ? off[t] : -1;
 }
 
 // Keys of the by-source view: for CSR position p (target t, source s),
@@ -456,7 +466,8 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     size_t off_tge = off_perm + align((size_t)cap * 4);
     size_t off_units = off_tge + align((size_t)cap * 4);
     size_t off_merge = off_units + align((size_t)max_units * 4);
-    size_t off_srp = off_merge + align((size_t)L * 4);
+    size_t off_mpos = off_merge + align((size_t)L * 4);
+    size_t off_srp = off_mpos + align((size_t)L * 4);
     size_t off_tbs = off_srp + align((size_t)(S + 1) * 4);
     size_t off_ufs = off_tbs + align((size_t)cap * 4);
     size_t off_ms = off_ufs + align((size_t)max_units * 4);
@@ -504,6 +515,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     g->tgt_of_edge = (int32_t *)(gm + off_tge);
     g->unit_first_t = (int32_t *)(gm + off_units);
     g->merge_t = (int32_t *)(gm + off_merge);
+    g->merge_pos = (int32_t *)(gm + off_mpos);
     g->src_row_ptr = (int32_t *)(gm + off_srp);
     g->tgt_by_src = (int32_t *)(gm + off_tbs);
     g->unit_first_s = (int32_t *)(gm + off_ufs);
@@ -549,7 +561,8 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         count_launch(4);
         exclusive_scan(c1, c2, (int)L, &dsum->n_merge, scan_tmp, stream);
         k_merge_write<<<blocks_for(L, TB), TB, 0, stream>>>(c1, c2, (int)L, g->merge_t);
-        count_launch();
+        k_merge_pos<<<blocks_for(L, TB), TB, 0, stream>>>(c1, c2, (int)L, g->merge_pos);
+        count_launch(2);
         if ((ce = cudaGetLastError()) != cudaSuccess) break;
         // the by-source view (for the backward pass): sort (source, target) keys
         if ((ce = cudaMemsetAsync(dsum_src, 0, sizeof(Summary), stream)) != cudaSuccess) break;
@@ -592,6 +605,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         g->max_deg = host_sum->max_deg;
         g->n_units = (g->nnz + kUnitEdges - 1) / kUnitEdges;
         g->n_merge = host_sum->n_merge;
+        g->n_empty = host_sum->n_empty;
         g->n_merge_s = host_sum[1].n_merge;
         g->max_out_deg = host_sum[1].max_deg;
         // A graph with at least a quarter of all (target, source) pairs may run

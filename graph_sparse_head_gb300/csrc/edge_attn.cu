@@ -28,7 +28,7 @@ template <typename T, bool WV, int CH>
 __global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge_t, long long n_merge,
                                                const int32_t *__restrict__ row_ptr, const float *__restrict__ part,
                                                long long n_units, int B, int L, int E, int H, int d, void *mixed,
-                                               float *ml)
+                                               float *ml, bool empty_only)
 {
     __shared__ float sm_m[8][32], sm_l[8][32];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge
     const int stride = 2 * H + E;
     T *mrow = WV ? (T *)mixed + ((long long)b * L + t) * E : nullptr;
     float *mlrow = ml ? ml + ((long long)b * L + t) * H * 2 : nullptr;
+    if (empty_only && beg != end) return;  // crossing targets were merged by the edge kernel
     if (beg == end) {
         if constexpr (WV) {
             for (int c = lane; c < E; c += 32) {
@@ -190,6 +191,9 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.perm = g->perm;
     k.unit_first_t = g->unit_first_t;
     k.kpm = a.kpm;
+    k.counters = a.counters;
+    k.merge_pos = g->merge_pos;
+    k.n_merge = g->n_merge;
     k.n_units = g->n_units;
     k.nnz = g->nnz;
     k.B = (int)a.B;
@@ -201,6 +205,7 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.score_scale = a.score_scale;
     const long long slots = a.B * g->n_units;
     if (slots == 0) return PMHA_OK;
+    if (g->n_merge > 0 && !a.kpm) PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(a.B * g->n_merge) * 4, s));
     StageTimer timer(a.with_values ? "edge_attn" : "edge_scores", s);
     const pmha_status st = dt == TcType::F16 ? stream::launch_f16(cpl, lpe, a.with_values, k, slots, s)
                                              : stream::launch_f32(cpl, lpe, a.with_values, k, slots, s);
@@ -215,7 +220,7 @@ template <typename T, bool WV, int CH>
 void launch_merge(const pmha_graph *g, const EdgeArgs &a, unsigned blocks, cudaStream_t s)
 {
     k_merge<T, WV, CH><<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, a.part, g->n_units, (int)a.B,
-                                              (int)g->L, (int)a.E, (int)a.H, (int)(a.E / a.H), a.mixed, a.ml);
+                                              (int)g->L, (int)a.E, (int)a.H, (int)(a.E / a.H), a.mixed, a.ml, a.kpm == nullptr);
 }
 template <typename T, bool WV>
 bool launch_merge_ch(int E, const pmha_graph *g, const EdgeArgs &a, unsigned blocks, cudaStream_t s)
@@ -231,9 +236,13 @@ bool launch_merge_ch(int E, const pmha_graph *g, const EdgeArgs &a, unsigned blo
 }
 }  // namespace
 
+// Without a key_padding_mask, targets that cross a unit boundary are merged
+// inside the edge kernel (by the slot that writes their last piece) and this
+// launch only gives the targets without edges their zero mix and (m, l) =
+// (-inf, 0); with a mask it merges the crossing targets too.
 pmha_status split_merge(TcType dt, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s)
 {
-    if (g->n_merge == 0) return PMHA_OK;
+    if (g->n_merge == 0 || (g->n_empty == 0 && !a.kpm)) return PMHA_OK;
     const long long warps = a.B * g->n_merge;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
     StageTimer timer("split_merge", s);

@@ -60,6 +60,9 @@ struct Args {
     const int32_t *perm;
     const int32_t *unit_first_t;
     const uint8_t *kpm;  // (B, S) key_padding_mask, nonzero = key dropped; or null
+    int *counters;             // (B, n_merge) pieces written per crossing target (zero at launch)
+    const int32_t *merge_pos;  // L, index of a target in the merge list
+    long long n_merge;
     long long n_units, nnz;
     int B, L, S, E, H, d;
     float score_scale;
@@ -351,6 +354,52 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
 #pragma unroll
     for (int j = 0; j < NP; ++j) acc2[j] = 0ull;
 
+    // Combine the partial states (m, l, acc) of target t's pieces, unit order:
+    // M = max m_i, L = sum l_i 2^(m_i - M), acc = sum acc_i 2^(m_i - M); an
+    // empty piece (every key dropped) has m = -inf, l = 0 and adds nothing.
+    auto merge_pieces = [&](int beg, int u0, int n_pieces) {
+        const long long stride = 2 * a.H + a.E;
+        const float *base = a.part + (long long)b * 2 * a.n_units * stride;
+        auto piece = [&](int i) -> const float * {
+            const int sid = 2 * (u0 + i) + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
+            return base + (long long)sid * stride;
+        };
+        float Mh = -INFINITY;
+        for (int i = 0; i < n_pieces; ++i) Mh = fmaxf(Mh, piece(i)[head]);
+        const float mo = Mh == -INFINITY ? 0.f : Mh;
+        float Lh = 0.f;
+        for (int i = 0; i < n_pieces; ++i) {
+            const float *pp = piece(i);
+            Lh = __fadd_rn(Lh, __fmul_rn(pp[a.H + head], ex2(__fsub_rn(pp[head], mo))));
+        }
+        if (a.ml && head_leader) {
+            float *q = a.ml + (((long long)b * a.L + t) * a.H + head) * 2;
+            q[0] = Mh;
+            q[1] = Lh;
+        }
+        if constexpr (WV) {
+            f2 macc[NP];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) macc[j] = 0ull;
+            for (int i = 0; i < n_pieces; ++i) {
+                const float *pp = piece(i);
+                const float w = ex2(__fsub_rn(pp[head], mo));
+                const f2 w2 = pk(w, w);
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const float2 v = reinterpret_cast<const float2 *>(pp + 2 * a.H + c0)[j];
+                    macc[j] = ffma2(pk(v.x, v.y), w2, macc[j]);
+                }
+            }
+            const float inv = Lh > 0.f ? __frcp_rn(Lh) : 0.f;
+            const f2 inv2 = pk(inv, inv);
+            f2 o[NP];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) o[j] = fmul2(macc[j], inv2);
+            store_row<T, CPL>((T *)a.mixed + ((long long)b * a.L + t) * a.E + c0, o);
+        }
+    };
+
     // finish target t in this unit: a complete target writes its result, a
     // target crossing a unit boundary its partial state
     auto finish = [&]() {
@@ -379,6 +428,24 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
             if constexpr (WV) {
 #pragma unroll
                 for (int j = 0; j < NP; ++j) reinterpret_cast<float2 *>(p + 2 * a.H + c0)[j] = upk(acc2[j]);
+            }
+            // Without a key_padding_mask, the slot that writes a target's last
+            // piece merges all its pieces: each writer publishes its piece
+            // (fence) and counts it; the one that completes the count reads
+            // every piece in piece order. (With a mask the kernel is short of
+            // registers; the separate merge kernel combines the pieces.)
+            if constexpr (!KPM) {
+            __threadfence();
+            __syncwarp(smask);
+            const int beg = a.row_ptr[t], end = a.row_ptr[t + 1];
+            const int u0 = beg / kUnitEdges, n_pieces = (end - 1) / kUnitEdges - u0 + 1;
+            int prev = 0;
+            if (grp == 0) prev = atomicAdd(a.counters + (long long)b * a.n_merge + a.merge_pos[t], 1);
+            prev = __shfl_sync(smask, prev, 0, LPE);
+            if (prev == n_pieces - 1) {
+                __threadfence();
+                merge_pieces(beg, u0, n_pieces);
+            }
             }
         }
     };

@@ -40,6 +40,8 @@ struct pmha_graph {
     int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
     int32_t *unit_first_t = nullptr;  // n_units, target of each unit's first position
     int32_t *merge_t = nullptr;       // n_merge, targets to merge (crossing a unit boundary, or without edges)
+    int32_t *merge_pos = nullptr;     // L, index of each target in merge_t, or -1
+    int64_t n_empty = 0;              // targets without edges
     // The same edges by source (for the backward pass): positions sorted by
     // (source, target); units of kUnitEdges positions; sources to merge.
     int32_t *src_row_ptr = nullptr;   // S + 1
@@ -126,6 +128,7 @@ struct EdgeArgs {
     float *part;          // (B, 2 n_units, 2H + E): per slot m[H], l[H], acc[E] of a crossing target
     float *ml;            // (B, L, H, 2): running max (log2 units) and sum per target/head
     float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
+    int *counters;        // (B, n_merge) pieces written per crossing target; zeroed before the edge kernel
     const uint8_t *kpm;   // (B, S) key_padding_mask, nonzero = key dropped, or null
     int64_t B, L, S, E, H, nnz;
     float score_scale;    // log2(e) / sqrt(d)
