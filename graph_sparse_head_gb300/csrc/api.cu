@@ -228,6 +228,10 @@ pmha_status project(pmha_dtype dt, const void *X, int64_t M, int64_t E, const Ge
 {
     if (dt == PMHA_BF16 && gemm_tc_supported(E))
         return gemm_tc(TcType::BF16, TcType::F16, X, M, E, seg, Y, ldy, stage, s);
+    if (seg.cvt_n > 0) {
+        const pmha_status st = convert_bf16_to_f16(seg.cvt_src, seg.cvt_dst, seg.cvt_n, s);
+        if (st != PMHA_OK) return st;
+    }
     return gemm_simt(param_type(dt), param_type(dt), inter_type(dt), X, M, E, seg, Y, ldy, stage, s);
 }
 
@@ -246,11 +250,21 @@ GemmSegments segs(const void *w0, const void *b0, const void *w1 = nullptr, cons
 }
 
 // Steps 1-4 (and the weights); with_values = false stops after the scores.
+// A non-null wo16 receives the fp16 copy of Wo that out_proj on the tensor
+// cores needs; the first projection GEMM writes it as a side job.
 pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
                    const void *value, const uint8_t *kpm, int64_t B, pmha_wmode wmode, float *weights, char *ws, const Layout &lay,
                    bool with_values, cudaStream_t s, const void **mixed_out, float *ml_keep = nullptr,
-                   bool allow_dense = true, EdgeArgs *args_out = nullptr)
+                   bool allow_dense = true, EdgeArgs *args_out = nullptr, void *wo16 = nullptr)
 {
+    auto with_wo = [&](GemmSegments sg) {
+        if (wo16) {
+            sg.cvt_src = p->wo;
+            sg.cvt_dst = wo16;
+            sg.cvt_n = p->embed_dim * p->embed_dim;
+        }
+        return sg;
+    };
     const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
     const size_t es = type_size(inter_type(p->dtype));
     char *qkv = ws + lay.qkv;
@@ -260,10 +274,10 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     const int width = with_values ? 3 : 2;
     if (same_qkv) {
         // one GEMM: rows [Q | K | V] (or [Q | K])
-        st = with_values ? project(p->dtype, query, B * L, E, segs(p->wq, p->bq, p->wk, p->bk, p->wv, p->bv), qkv,
-                                   3 * E, "proj_qkv", s)
-                         : project(p->dtype, query, B * L, E, segs(p->wq, p->bq, p->wk, p->bk), qkv, 2 * E, "proj_qk",
-                                   s);
+        st = with_values ? project(p->dtype, query, B * L, E,
+                                   with_wo(segs(p->wq, p->bq, p->wk, p->bk, p->wv, p->bv)), qkv, 3 * E, "proj_qkv", s)
+                         : project(p->dtype, query, B * L, E, with_wo(segs(p->wq, p->bq, p->wk, p->bk)), qkv, 2 * E,
+                                   "proj_qk", s);
         if (st != PMHA_OK) return st;
         a.q = qkv;
         a.q_ld = width * E;
@@ -272,7 +286,7 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     } else {
         char *kvbuf = qkv + (size_t)(B * L * E) * es;
         const int64_t kv_w = with_values ? 2 * E : E;
-        st = project(p->dtype, query, B * L, E, segs(p->wq, p->bq), qkv, E, "proj_q", s);
+        st = project(p->dtype, query, B * L, E, with_wo(segs(p->wq, p->bq)), qkv, E, "proj_q", s);
         if (st != PMHA_OK) return st;
         if (with_values && key == value) {
             st = project(p->dtype, key, B * S, E, segs(p->wk, p->bk, p->wv, p->bv), kvbuf, kv_w, "proj_kv", s);
@@ -386,16 +400,16 @@ pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void
     }
     char *ws = (char *)workspace;
     const void *mixed = nullptr;
-    st = attend(g, p, query, key, value, kpm, B, wmode, weights, ws, lay, true, s, &mixed);
+    // both MMA operands of out_proj on the tensor cores must share one type:
+    // step 1's GEMM (same condition) leaves an fp16 copy of Wo in wo16
+    const bool tc_out = out_proj_on_tensor_cores(p);
+    void *wo16 = tc_out ? ws + lay.wo16 : nullptr;
+    st = attend(g, p, query, key, value, kpm, B, wmode, weights, ws, lay, true, s, &mixed, nullptr, true, nullptr, wo16);
     if (st != PMHA_OK) return st;
     // step 5: out_proj over the joined heads, mixed (intermediate type) -> output (layer dtype)
     const int64_t E = p->embed_dim;
-    if (out_proj_on_tensor_cores(p)) {
-        // both MMA operands must share one type: use an fp16 copy of Wo
-        void *wo16 = ws + lay.wo16;
-        if ((st = convert_bf16_to_f16(p->wo, wo16, E * E, s)) != PMHA_OK) return st;
+    if (tc_out)
         return gemm_tc(TcType::F16, TcType::BF16, mixed, B * g->L, E, segs(wo16, p->bo), output, E, "out_proj", s);
-    }
     return gemm_simt(inter_type(p->dtype), param_type(p->dtype), param_type(p->dtype), mixed, B * g->L, E,
                      segs(p->wo, p->bo), output, E, "out_proj", s);
 }

@@ -58,26 +58,58 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 // ---------------------------------------------------------------- D = dot(dmixed, mixed) per (row, head)
-// One warp per row: lane l takes channels l, l + 32, ...; each head's sum is
-// added over its channels in channel order through shared memory.
+// One thread per (row, head): the head's d channels of both rows come in as
+// 16-byte vectors (consecutive threads read consecutive heads, so a warp
+// reads whole rows); products are rounded and summed in channel order.
+template <typename T>
+__device__ __forceinline__ void widen16(const uint4 &u, float (&f)[16 / sizeof(T)]);
+template <>
+__device__ __forceinline__ void widen16<__half>(const uint4 &u, float (&f)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        f[2 * i] = x.x;
+        f[2 * i + 1] = x.y;
+    }
+}
+template <>
+__device__ __forceinline__ void widen16<float>(const uint4 &u, float (&f)[4])
+{
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) k_rowdot(const T *__restrict__ dmixed, const T *__restrict__ mixed,
                                                 long long rows, int E, int H, float *__restrict__ D)
 {
-    __shared__ float prod[8][512];
-    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-    const long long r = (long long)blockIdx.x * 8 + wib;
-    if (r >= rows) return;
-    const T *g = dmixed + r * E;
-    const T *o = mixed + r * E;
-    for (int c = lane; c < E; c += 32) prod[wib][c] = __fmul_rn(to_f(g[c]), to_f(o[c]));
-    __syncwarp();
+    constexpr int PER = 16 / (int)sizeof(T);  // channels per vector
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // row * H + head
+    if (i >= rows * H) return;
     const int d = E / H;
-    for (int h = lane; h < H; h += 32) {
-        float acc = 0.f;
-        for (int c = 0; c < d; ++c) acc = __fadd_rn(acc, prod[wib][h * d + c]);
-        D[r * H + h] = acc;
+    const long long r = i / H;
+    const int h = (int)(i - r * H);
+    const T *gs = dmixed + r * E + (long long)h * d, *os = mixed + r * E + (long long)h * d;
+    float acc = 0.f;
+    if (d % PER) {  // heads narrower than a vector (float32 heads of 1 or 2 channels)
+        for (int c = 0; c < d; ++c) acc = __fadd_rn(acc, __fmul_rn(to_f(gs[c]), to_f(os[c])));
+        D[i] = acc;
+        return;
     }
+    const uint4 *g = reinterpret_cast<const uint4 *>(gs);
+    const uint4 *o = reinterpret_cast<const uint4 *>(os);
+    for (int v = 0; v < d / PER; ++v) {
+        float fg[PER], fo[PER];
+        widen16<T>(__ldg(g + v), fg);
+        widen16<T>(__ldg(o + v), fo);
+#pragma unroll
+        for (int c = 0; c < PER; ++c) acc = __fadd_rn(acc, __fmul_rn(fg[c], fo[c]));
+    }
+    D[i] = acc;
 }
 
 struct WalkArgs {
@@ -699,11 +731,11 @@ pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t 
 {
     StageTimer timer("bwd_rowdot", s);
     if (t == TcType::F16)
-        k_rowdot<__half><<<blocks(rows, 8), 256, 0, s>>>((const __half *)dmixed, (const __half *)mixed, rows, (int)E,
-                                                         (int)H, D);
+        k_rowdot<__half><<<blocks(rows * H, 256), 256, 0, s>>>((const __half *)dmixed, (const __half *)mixed, rows,
+                                                              (int)E, (int)H, D);
     else
-        k_rowdot<float><<<blocks(rows, 8), 256, 0, s>>>((const float *)dmixed, (const float *)mixed, rows, (int)E,
-                                                        (int)H, D);
+        k_rowdot<float><<<blocks(rows * H, 256), 256, 0, s>>>((const float *)dmixed, (const float *)mixed, rows,
+                                                             (int)E, (int)H, D);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;

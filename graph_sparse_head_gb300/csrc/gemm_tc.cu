@@ -15,10 +15,12 @@
 //             128-byte swizzle, into a 4-stage shared-memory ring
 //   warp 1    allocates 256 TMEM columns (two 128 x 128 fp32 accumulators)
 //             and issues tcgen05.mma (M=128, N=128, K=16) from one thread
-//   warps 2-5 epilogue: tcgen05.ld 32 columns at a time (warp w reads TMEM
-//             lanes 32*(w%4) .. +31), + bias, rounded to the output type,
-//             written to a 128-byte-swizzled shared tile that one thread
-//             stores with TMA (two tiles in flight)
+//   warps 2-  epilogue, kEpi groups of 4 warps; group g drains the tiles
+//             whose accumulator is g (a CTA's tiles alternate between the
+//             two): tcgen05.ld 32 columns at a time (warp w reads TMEM lanes
+//             32*(w%4) .. +31), + bias (staged in shared memory once per
+//             tile), rounded to the output type, written to a
+//             128-byte-swizzled shared tile that one thread stores with TMA
 // Tiles are visited m-major with the N tiles of one row block adjacent, so
 // CTAs that share an X tile run together and the re-reads hit L2.
 //
@@ -40,15 +42,24 @@ namespace {
 using namespace tcu;
 
 constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int kStages = 4;
+#ifndef PMHA_GEMM_STAGES
+#define PMHA_GEMM_STAGES 4
+#endif
+constexpr int kStages = PMHA_GEMM_STAGES;
 constexpr int kTileABytes = BM * BK * 2;
 constexpr int kTileBBytes = BN * BK * 2;
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
-constexpr int kThreads = 192;
+#ifndef PMHA_GEMM_EPI_GROUPS
+#define PMHA_GEMM_EPI_GROUPS 2
+#endif
+constexpr int kEpi = PMHA_GEMM_EPI_GROUPS;  // epilogue warpgroups (1 or 2)
+static_assert(kEpi == 1 || kEpi == 2, "one or two epilogue groups");
+constexpr int kThreads = 64 + 128 * kEpi;
 constexpr int kTmemCols = 2 * BN;
 constexpr int kOutBoxBytes = BM * 128;             // 128 rows x 64 16-bit columns, 128-byte swizzle
 constexpr int kOutTileBytes = 2 * kOutBoxBytes;     // one 128 x 128 output tile
-constexpr int kSmemBytes = kStages * kStageBytes + 2 * kOutTileBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kBiasBytes = kEpi * BN * 4;  // fp32 bias of the tile, per group
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kOutTileBytes + kBiasBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B of one 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), both
@@ -70,6 +81,10 @@ struct TcArgs {
     // split ks = t % ksplit and writes its partial at out + ks * part_stride
     int ksplit, kb_per;
     long long part_stride;
+    // side job: bf16 -> fp16 copy of cvt_n values (out of range sets kErrRangeBit)
+    const __nv_bfloat16 *cvt_src;
+    __half *cvt_dst;
+    int cvt_n;
 };
 
 // Two fp32 values to one 32-bit word of the output type. fp16 outputs also
@@ -100,19 +115,20 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// barrier 1 over the 128 epilogue threads
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// named barrier 1 + g over the 128 threads of epilogue group g
+__device__ __forceinline__ void epi_sync(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); }
 // same barrier, returning whether any of the 128 threads passed `pred`
-__device__ __forceinline__ bool epi_sync_or(bool pred)
+__device__ __forceinline__ bool epi_sync_or(int g, bool pred)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)pred)
+        : "r"((uint32_t)pred), "r"(1 + g)
         : "memory");
     return r != 0;
 }
@@ -127,7 +143,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *tiles = smem;
     uint8_t *staging = smem + kStages * kStageBytes;  // two output tiles
-    uint64_t *bars = (uint64_t *)(staging + 2 * kOutTileBytes);
+    float *bias_s = (float *)(staging + 2 * kOutTileBytes);  // [kEpi][BN]
+    uint64_t *bars = (uint64_t *)(staging + 2 * kOutTileBytes + kBiasBytes);
     uint64_t *full = bars;                    // [kStages]
     uint64_t *empty = bars + kStages;         // [kStages]
     uint64_t *acc_full = bars + 2 * kStages;  // [2]
@@ -180,7 +197,18 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        if (lane == 0) {
+        if (lane != 0) {
+            // ---------------- idle lanes of the producer warp: this CTA's share of the side conversion
+            const int per = (a.cvt_n + (int)gridDim.x - 1) / (int)gridDim.x;
+            const int end = min(a.cvt_n, ((int)blockIdx.x + 1) * per);
+            bool bad = false;
+            for (int i = (int)blockIdx.x * per + lane - 1; i < end; i += 31) {
+                const float v = __bfloat162float(a.cvt_src[i]);
+                bad |= !(fabsf(v) <= 65504.f);
+                a.cvt_dst[i] = __float2half_rn(v);
+            }
+            if (bad) atomicOr(a.err, kErrRangeBit);
+        } else {
             // ---------------- TMA producer
             int stage = 0;
             uint32_t phase = 0;
@@ -253,22 +281,39 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             mbar_wait(smem_u32(mma_done), 0, (volatile int *)&dummy, a.err);
         }
     } else {
-        // ---------------- epilogue, 128 threads: TMEM -> registers (+ bias, rounding)
-        // -> swizzled shared tile -> TMA tensor store, double-buffered
+        // ---------------- epilogue, kEpi groups of 128 threads: TMEM -> registers
+        // (+ bias, rounding) -> swizzled shared tile -> TMA tensor store. The
+        // CTA's i-th tile uses accumulator i % 2 and goes to group i % kEpi;
+        // the two staging tiles alternate within one group or are one per group.
         const int quarter = warp & 3;
-        const int et = threadIdx.x - 64;  // 0..127
+        const int g = (warp - 2) >> 2;          // epilogue group
+        const int et = threadIdx.x - 64 - 128 * g;  // 0..127 within the group
         const int r = quarter * 32 + lane;  // tile row of this thread
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        int buf = 0;
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        float *bias_g = bias_s + g * BN;
+        for (int i = g;; i += kEpi) {
+            const int tile = blockIdx.x + i * gridDim.x;
+            if (tile >= n_tiles) break;
+            const int acc = i & 1;
+            const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
+            const int buf = kEpi == 2 ? g : acc;
             const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err);
-            if (et == 0) bulk_wait_read1();  // the store that last read this buffer is done
-            if (epi_sync_or(!ok)) break;     // one decision for all 128 threads
-            tc_fence_after();
+            // the store that last read this group's staging tile is done
+            if (et == 0) {
+                if constexpr (kEpi == 2) bulk_wait_read0();
+                else bulk_wait_read1();
+            }
             int m_blk, n_blk, kb0, kb1;
             decode(tile, m_blk, n_blk, kb0, kb1);
             const int n_glob = n_blk * BN;
+            const int seg = n_glob / a.E;
+            const int n_loc = n_glob - seg * a.E;
+            const __nv_bfloat16 *bias = a.bias[seg];
+            if constexpr (!std::is_same<TOut, float>::value) {
+                // the readers of the previous tile's bias passed the barrier before its store
+                bias_g[et] = bias ? __bfloat162float(bias[n_loc + et]) : 0.f;
+            }
+            if (epi_sync_or(g, !ok)) break;  // one decision for all 128 threads
+            tc_fence_after();
             const bool live = m_blk * BM + r < a.M;
             if constexpr (std::is_same<TOut, float>::value) {
                 // fp32 partial of this K split, stored straight from registers
@@ -287,29 +332,21 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 }
                 tc_fence_before();
                 mbar_arrive(smem_u32(&acc_empty[acc]));
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
                 continue;
             } else {
-            const int seg = n_glob / a.E;
-            const int n_loc = n_glob - seg * a.E;
-            const __nv_bfloat16 *bias = a.bias[seg];
             uint8_t *sb = staging + buf * kOutTileBytes;
             bool range_bad = false;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), v);
+            // columns [32c, 32c + 32) of the accumulator: + bias, rounded, into the staging tile
+            auto emit = [&](int c, const uint32_t (&v)[32]) {
                 uint32_t packed[16];
                 bool bad = false;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     float v0 = __uint_as_float(v[2 * j]), v1 = __uint_as_float(v[2 * j + 1]);
                     if (bias) {
-                        v0 = __fadd_rn(v0, __bfloat162float(bias[n_loc + c * 32 + 2 * j]));
-                        v1 = __fadd_rn(v1, __bfloat162float(bias[n_loc + c * 32 + 2 * j + 1]));
+                        const float2 bb = *reinterpret_cast<const float2 *>(bias_g + c * 32 + 2 * j);
+                        v0 = __fadd_rn(v0, bb.x);
+                        v1 = __fadd_rn(v1, bb.y);
                     }
                     packed[j] = pack2<TOut>(v0, v1, bad);
                 }
@@ -322,6 +359,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                     *reinterpret_cast<uint4 *>(rowp + ((u ^ (r & 7)) << 4)) =
                         make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 }
+            };
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_row + (uint32_t)(c * 32), v);
+                emit(c, v);
             }
             if (range_bad) atomicOr(a.err, kErrRangeBit);
             // the accumulator has been read: hand it back to the MMA warp
@@ -329,16 +373,11 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             mbar_arrive(smem_u32(&acc_empty[acc]));
             // staged tile -> global (rows past M are clipped by the tensor map)
             fence_async_shared();
-            epi_sync();
+            epi_sync(g);
             if (et == 0) {
                 tma_store_2d(&tm_y, smem_u32(sb), n_glob, m_blk * BM);
                 tma_store_2d(&tm_y, smem_u32(sb + kOutBoxBytes), n_glob + 64, m_blk * BM);
                 bulk_commit();
-            }
-            buf ^= 1;
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
             }
             }  // 16-bit output
         }
@@ -420,6 +459,13 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     a.ksplit = 1;
     a.kb_per = a.K / BK;
     a.part_stride = 0;
+    a.cvt_src = (const __nv_bfloat16 *)seg.cvt_src;
+    a.cvt_dst = (__half *)seg.cvt_dst;
+    a.cvt_n = seg.cvt_src && seg.cvt_dst ? (int)seg.cvt_n : 0;
+    if (seg.cvt_n > 0x7fffffff) {
+        set_error("gemm_tc: side conversion of %lld values exceeds the 32-bit index", (long long)seg.cvt_n);
+        return PMHA_ERR_UNSUPPORTED;
+    }
 
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
     if (in_bf16 && out == TcType::F16) kern = k_gemm_tc<__nv_bfloat16, __half>;
@@ -496,6 +542,9 @@ pmha_status gemm_tc_general(TcType in, TcType out, const void *X, int64_t ldx, i
     a.ksplit = (int)ksplit;
     a.kb_per = kb_per;
     a.part_stride = M * ldy;
+    a.cvt_src = nullptr;
+    a.cvt_dst = nullptr;
+    a.cvt_n = 0;
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
     if (out == TcType::F32) kern = in_bf16 ? k_gemm_tc<__nv_bfloat16, float> : k_gemm_tc<__half, float>;
     else if (in_bf16) kern = out == TcType::F16 ? k_gemm_tc<__nv_bfloat16, __half> : k_gemm_tc<__nv_bfloat16, __nv_bfloat16>;

@@ -100,6 +100,11 @@ struct GemmSegments {
     const void *w[3];
     const void *b[3];
     int n_seg;
+    // optional side job of the tensor-core kernel: convert cvt_n bf16 values
+    // at cvt_src to fp16 at cvt_dst (out_proj's weight, while step 1 runs)
+    const void *cvt_src = nullptr;
+    void *cvt_dst = nullptr;
+    int64_t cvt_n = 0;
 };
 // Element types on the projection path. Layers stored in bf16 keep their
 // intermediates (q, k, v, mixed) in fp16; float32 layers stay float32.
