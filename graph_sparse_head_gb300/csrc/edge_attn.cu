@@ -65,12 +65,14 @@ __global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge
     };
     if (lane < H) {
         float mh = -INFINITY;
+#pragma unroll 4  // several independent loads in flight
         for (int i = 0; i < n_pieces; ++i) mh = fmaxf(mh, piece(i)[lane]);
         // A piece whose keys were all dropped has m = -inf and l = 0, and
         // ex2.approx(-inf) is +0, so it adds nothing; when every piece is
         // empty (M = -inf) the offset 0 stands in for M and avoids -inf - -inf.
         const float mo = mh == -INFINITY ? 0.f : mh;
         float lh = 0.f;
+#pragma unroll 4
         for (int i = 0; i < n_pieces; ++i) {
             const float *p = piece(i);
             lh = __fadd_rn(lh, __fmul_rn(p[H + lane], ex2(__fsub_rn(p[lane], mo))));
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge
             const int ch = lane + 32 * k;
             hd[k] = ch < E ? ch / d : 0;
         }
+#pragma unroll 2
         for (int i = 0; i < n_pieces; ++i) {
             const float *p = piece(i);
 #pragma unroll

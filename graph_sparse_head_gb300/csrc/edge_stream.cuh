@@ -262,8 +262,9 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     };
     int iw = 0;
     int cw0 = ldcol(0), cw1 = ldcol(1), cw2 = ldcol(2);
-    // edges j and j + 1 (j even) in one commit group; both lie in one window
-    auto issue2 = [&](int j) {
+    // edges j and j + 1 (j even) in one commit group, into ring stages sj and
+    // sj + 1 (sj = j mod kRing, even since kRing is); both lie in one window
+    auto issue2 = [&](int j, int sj) {
         if (j >= (iw + 1) * LPE) {
             ++iw;
             cw0 = cw1;
@@ -274,20 +275,21 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
         const int s1 = __shfl_sync(smask, cw0, (j + 1) & (LPE - 1), LPE);
         if (j < n) {
             const char *row = KVb + (long long)s0 * row_bytes;
-            const uint32_t dst = sbase + (uint32_t)((j % kRing) * STAGE);
+            const uint32_t dst = sbase + (uint32_t)(sj * STAGE);
             cp_async<CB>(dst, row);
             if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
         }
         if (j + 1 < n) {
             const char *row = KVb + (long long)s1 * row_bytes;
-            const uint32_t dst = sbase + (uint32_t)(((j + 1) % kRing) * STAGE);
+            const uint32_t dst = sbase + (uint32_t)((sj + 1) * STAGE);
             cp_async<CB>(dst, row);
             if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
         }
         cp_async_commit();
     };
+    static_assert(kDepth % 2 == 0, "edges go two per step");
 #pragma unroll
-    for (int j = 0; j < kDepth; j += 2) issue2(j);
+    for (int j = 0; j < kDepth; j += 2) issue2(j, j);
 
     // ---- given-order edge ids for the score write-out
     int pw = 0, perm_cur = 0, perm_nxt = 0;
@@ -364,26 +366,22 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
             const int sid = 2 * (u0 + i) + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
             return base + (long long)sid * stride;
         };
+        // two passes over the pieces, loads unrolled so that several are in
+        // flight: the maximum, then L and acc together (each summed in piece order)
         float Mh = -INFINITY;
+#pragma unroll 4
         for (int i = 0; i < n_pieces; ++i) Mh = fmaxf(Mh, piece(i)[head]);
         const float mo = Mh == -INFINITY ? 0.f : Mh;
         float Lh = 0.f;
+        f2 macc[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) macc[j] = 0ull;
+#pragma unroll 2
         for (int i = 0; i < n_pieces; ++i) {
             const float *pp = piece(i);
-            Lh = __fadd_rn(Lh, __fmul_rn(pp[a.H + head], ex2(__fsub_rn(pp[head], mo))));
-        }
-        if (a.ml && head_leader) {
-            float *q = a.ml + (((long long)b * a.L + t) * a.H + head) * 2;
-            q[0] = Mh;
-            q[1] = Lh;
-        }
-        if constexpr (WV) {
-            f2 macc[NP];
-#pragma unroll
-            for (int j = 0; j < NP; ++j) macc[j] = 0ull;
-            for (int i = 0; i < n_pieces; ++i) {
-                const float *pp = piece(i);
-                const float w = ex2(__fsub_rn(pp[head], mo));
+            const float w = ex2(__fsub_rn(pp[head], mo));
+            Lh = __fadd_rn(Lh, __fmul_rn(pp[a.H + head], w));
+            if constexpr (WV) {
                 const f2 w2 = pk(w, w);
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
@@ -391,6 +389,13 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
                     macc[j] = ffma2(pk(v.x, v.y), w2, macc[j]);
                 }
             }
+        }
+        if (a.ml && head_leader) {
+            float *q = a.ml + (((long long)b * a.L + t) * a.H + head) * 2;
+            q[0] = Mh;
+            q[1] = Lh;
+        }
+        if constexpr (WV) {
             const float inv = Lh > 0.f ? __frcp_rn(Lh) : 0.f;
             const f2 inv2 = pk(inv, inv);
             f2 o[NP];
@@ -492,11 +497,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
 #pragma unroll
         for (int i = 0; i < NP; ++i) acc2[i] = fmul2(acc2[i], s2);
     };
-    // one edge through the online softmax (used at target boundaries)
-    auto one = [&](int j, const Raw<CB> &kr, const Raw<CB> &vr) {
+    // one edge through the online softmax (used at target boundaries); its
+    // v row is read from stage address vst once the score is known
+    auto one = [&](int j, const Raw<CB> &kr, uint32_t vst) {
         const int pos = e0 + j;
         if (pos >= bound) advance(pos);
         float dot = score(kr);
+        Raw<CB> vr;
+        if constexpr (WV) vr = lds_raw<CB>(vst);
         if constexpr (KPM)
             if (masked(j)) dot = -INFINITY;
         if constexpr (WS) {
@@ -516,23 +524,31 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
         m = m_new;
     };
 
+    // rs = j mod kRing, stepped by 2 with a wrap (no division in the loop);
+    // edge j + kDepth goes to stage (rs + kDepth) mod kRing = the stage read
+    // one step earlier
+    int rs = 0;
     for (int j = 0; j < n; j += 2) {
         cp_async_wait<kDepth / 2 - 1>();
-        const uint32_t st0 = sbase + (uint32_t)((j % kRing) * STAGE);
-        const uint32_t st1 = sbase + (uint32_t)(((j + 1) % kRing) * STAGE);
+        const uint32_t st0 = sbase + (uint32_t)(rs * STAGE);
+        const uint32_t st1 = st0 + (uint32_t)STAGE;
         const Raw<CB> kr0 = lds_raw<CB>(st0);
         const Raw<CB> kr1 = lds_raw<CB>(st1);
-        Raw<CB> vr0, vr1;
-        if constexpr (WV) {
-            vr0 = lds_raw<CB>(st0 + 32 * CB);
-            vr1 = lds_raw<CB>(st1 + 32 * CB);
-        }
-        issue2(j + kDepth);
+        // the v rows are read after the scores (fewer live registers; the
+        // softmax covers the load latency). Stages st0 and st1 are refilled
+        // only by the next step's issue2.
+        issue2(j + kDepth, rs == 0 ? kRing - 2 : rs - 2);
+        rs = rs + 2 == kRing ? 0 : rs + 2;
 
         const int pos = e0 + j;
         if (j + 1 < n && pos + 1 < bound) {
             // both edges belong to t: two independent scores, one rescale
             float d0 = score(kr0), d1 = score(kr1);
+            Raw<CB> vr0, vr1;
+            if constexpr (WV) {
+                vr0 = lds_raw<CB>(st0 + 32 * CB);
+                vr1 = lds_raw<CB>(st1 + 32 * CB);
+            }
             if constexpr (KPM) {
                 if (masked(j)) d0 = -INFINITY;
                 if (masked(j + 1)) d1 = -INFINITY;
@@ -557,8 +573,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
             }
             m = m_new;
         } else {
-            one(j, kr0, vr0);
-            if (j + 1 < n) one(j + 1, kr1, vr1);
+            one(j, kr0, st0 + 32 * CB);
+            if (j + 1 < n) one(j + 1, kr1, st1 + 32 * CB);
         }
     }
     cp_async_wait<0>();
