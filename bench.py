@@ -37,6 +37,7 @@ WORKLOAD_ID = 3  # default: the skewed n = 20,000 workload (--workload picks ano
 METRIC = "edge·head·sample scores/s and layer fwd µs at n=20k; % HBM / tensor roofline"
 UNIT = "scores/s"
 FLUSH_BYTES = 512 << 20
+E2E_STREAMS = 3  # end-to-end leg: steps in flight (own workspace, output and stream each)
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -401,20 +402,21 @@ def bench_ours(args):
                 "stages_avg_us": {k: 1e3 * v[1] / max(v[0], 1) for k, v in b_prof.items()}}
 
     # ---- end to end through the C ABI with host buffers (pinned), per step:
-    # copy the step's tokens in, run, copy the output back. Steps alternate
-    # between two streams, each with its own workspace and output buffer, so
-    # one step's copies overlap the other's kernels (as a serving loop would);
-    # the serial figure (one stream) is reported beside it.
+    # copy the step's tokens in, run, copy the output back. Steps rotate over
+    # E2E_STREAMS streams, each with its own workspace and output buffer, so
+    # one step's copies overlap other steps' kernels (as a serving loop with
+    # several requests in flight would); the serial figure (one stream) is
+    # reported beside it.
     xh = torch.from_numpy(xq_np).to(torch.bfloat16).pin_memory()
     kvh = xh if self_attn else torch.from_numpy(xkv_np).to(torch.bfloat16).pin_memory()
-    streams = [stream, torch.cuda.Stream(device=dev)]
-    outs = [torch.empty_like(xh).pin_memory() for _ in range(2)]
+    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(E2E_STREAMS - 1)]
+    outs = [torch.empty_like(xh).pin_memory() for _ in range(E2E_STREAMS)]
     ws_need = pmha.pmha_forward_host_workspace_size(graph, params, B, "none")
-    wss = [torch.empty(ws_need, dtype=torch.uint8, device=dev) for _ in range(2)]
+    wss = [torch.empty(ws_need, dtype=torch.uint8, device=dev) for _ in range(E2E_STREAMS)]
     e2e_steps = max(4, min(args.steps, 20))
 
     def host_step(i):
-        k = i % 2
+        k = i % E2E_STREAMS
         pmha.pmha_forward_host(graph, params, xh, kvh, kvh, outs[k], "none", workspace=wss[k], stream=streams[k])
 
     for i in range(4):
@@ -428,14 +430,17 @@ def bench_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
-    # overlapped: two streams, the whole run timed from the first copy to the last result
-    e0, e1, side = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    # overlapped: the whole run timed from the first copy to the last result
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(streams[0])
-    streams[1].wait_event(e0)
+    for st_ in streams[1:]:
+        st_.wait_event(e0)
     for i in range(e2e_steps):
         host_step(i)
-    side.record(streams[1])
-    streams[0].wait_event(side)
+    for st_ in streams[1:]:
+        ev = torch.cuda.Event()
+        ev.record(st_)
+        streams[0].wait_event(ev)
     e1.record(streams[0])
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
@@ -498,7 +503,7 @@ def bench_ours(args):
                        "parallelism": f"replicas x{world}, own batch per rank, no collective"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "serial_ms_per_step": e2e_serial_ms,
-                    "api": "pmha_forward_host (pinned host buffers), steps alternating over two streams"},
+                    "api": f"pmha_forward_host (pinned host buffers), steps rotating over {E2E_STREAMS} streams"},
             "gpu_launches": launches,
             "roofline": roof,
             "stages": stages,

@@ -296,22 +296,25 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const int acc = i & 1;
             const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
             const int buf = kEpi == 2 ? g : acc;
-            const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err);
-            // the store that last read this group's staging tile is done
-            if (et == 0) {
-                if constexpr (kEpi == 2) bulk_wait_read0();
-                else bulk_wait_read1();
-            }
             int m_blk, n_blk, kb0, kb1;
             decode(tile, m_blk, n_blk, kb0, kb1);
             const int n_glob = n_blk * BN;
             const int seg = n_glob / a.E;
             const int n_loc = n_glob - seg * a.E;
             const __nv_bfloat16 *bias = a.bias[seg];
-            if constexpr (!std::is_same<TOut, float>::value) {
-                // the readers of the previous tile's bias passed the barrier before its store
-                bias_g[et] = bias ? __bfloat162float(bias[n_loc + et]) : 0.f;
+            // this thread's bias value, loaded before the accumulator wait so
+            // that the wait covers the load
+            float bias_v = 0.f;
+            if constexpr (!std::is_same<TOut, float>::value)
+                if (bias) bias_v = __bfloat162float(bias[n_loc + et]);
+            const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err);
+            // the store that last read this group's staging tile is done
+            if (et == 0) {
+                if constexpr (kEpi == 2) bulk_wait_read0();
+                else bulk_wait_read1();
             }
+            // the readers of the previous tile's bias passed the barrier before its store
+            if constexpr (!std::is_same<TOut, float>::value) bias_g[et] = bias_v;
             if (epi_sync_or(g, !ok)) break;  // one decision for all 128 threads
             tc_fence_after();
             const bool live = m_blk * BM + r < a.M;

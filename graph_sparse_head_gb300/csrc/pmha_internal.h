@@ -23,7 +23,10 @@ namespace pmha {
 // slot 2u + 1 for its last.
 // --------------------------------------------------------------------------
 
-constexpr int kUnitEdges = 256;
+#ifndef PMHA_UNIT_EDGES
+#define PMHA_UNIT_EDGES 160
+#endif
+constexpr int kUnitEdges = PMHA_UNIT_EDGES;
 
 }  // namespace pmha
 
