@@ -342,14 +342,14 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
             EdgeArgs w = a;
             w.with_values = false;
             if ((st = edge_attention(it, g, w, s)) != PMHA_OK) return st;
-            if ((st = split_merge(it, g, w, s)) != PMHA_OK) return st;
+            if ((st = empty_targets(it, g, w, s)) != PMHA_OK) return st;
             if ((st = weights_finalize(g, w, wmode, weights, s)) != PMHA_OK) return st;
         }
         if (mixed_out) *mixed_out = a.mixed;
         return PMHA_OK;
     }
     if ((st = edge_attention(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
-    if ((st = split_merge(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
+    if ((st = empty_targets(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
     if (wmode != PMHA_WEIGHTS_NONE)
         if ((st = weights_finalize(g, a, wmode, weights, s)) != PMHA_OK) return st;
     if (mixed_out) *mixed_out = a.mixed;

@@ -16,8 +16,8 @@
 //   checks    adjacent equal keys -> duplicate
 //   view      row_ptr by binary search; col, perm, target of each edge id
 //   plan      first target of every unit of kUnitEdges positions; list of
-//             targets the merge kernel finishes (crossing a unit boundary,
-//             or without edges)
+//             targets crossing a unit boundary (their pieces are merged by
+//             the edge kernel) or without edges, with their positions in it
 // followed by a single device-to-host copy of a summary and one synchronize.
 #include <algorithm>
 #include <vector>

@@ -17,104 +17,30 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// One warp per (sample, merge-list target). Targets without edges get zeros
-// and (m, l) = (-inf, 0); others combine their partial states:
-// M = max m_i, L = sum l_i 2^(m_i - M), acc = sum acc_i 2^(m_i - M).
-// Pass 1: lane h owns head h and walks the pieces in order. Pass 2: lane l
-// owns channels l, l + 32, ... (CH of them) and walks the pieces in order.
-// Both orders are fixed, so results are deterministic, and pass 1 is the
-// same code with and without values.
-template <typename T, bool WV, int CH>
-__global__ void __launch_bounds__(256) k_merge(const int32_t *__restrict__ merge_t, long long n_merge,
-                                               const int32_t *__restrict__ row_ptr, const float *__restrict__ part,
-                                               long long n_units, int B, int L, int E, int H, int d, void *mixed,
-                                               float *ml, bool empty_only)
+// Targets without edges (paragraph after the Notes steps: they mix to
+// zeros): one warp per (sample, merge-list target) writes the zero mix and
+// (m, l) = (-inf, 0) for the targets without edges and skips the others
+// (targets that cross a unit boundary, merged by the edge kernel itself).
+template <typename T, bool WV>
+__global__ void __launch_bounds__(256) k_empty_targets(const int32_t *__restrict__ merge_t, long long n_merge,
+                                                       const int32_t *__restrict__ row_ptr, int B, int L, int E,
+                                                       int H, void *mixed, float *ml)
 {
-    __shared__ float sm_m[8][32], sm_l[8][32];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const long long gw = (long long)blockIdx.x * 8 + wib;
     if (gw >= (long long)B * n_merge) return;
     const int b = (int)(gw / n_merge);
     const int t = merge_t[gw - (long long)b * n_merge];
-    const int beg = row_ptr[t], end = row_ptr[t + 1];
-    const int stride = 2 * H + E;
-    T *mrow = WV ? (T *)mixed + ((long long)b * L + t) * E : nullptr;
-    float *mlrow = ml ? ml + ((long long)b * L + t) * H * 2 : nullptr;
-    if (empty_only && beg != end) return;  // crossing targets were merged by the edge kernel
-    if (beg == end) {
-        if constexpr (WV) {
-            for (int c = lane; c < E; c += 32) {
-                if constexpr (sizeof(T) == 2) reinterpret_cast<__half *>(mrow)[c] = __float2half_rn(0.f);
-                else reinterpret_cast<float *>(mrow)[c] = 0.f;
-            }
-        }
-        if (mlrow)
-            for (int h = lane; h < H; h += 32) {
-                mlrow[2 * h] = -INFINITY;
-                mlrow[2 * h + 1] = 0.f;
-            }
-        return;
-    }
-    const int u0 = beg / kUnitEdges, u1 = (end - 1) / kUnitEdges;
-    const int n_pieces = u1 - u0 + 1;
-    // piece i lives in unit u0 + i: slot 2u for the unit's first target, else 2u + 1
-    const float *base = part + (long long)b * 2 * n_units * stride;
-    auto piece = [&](int i) -> const float * {
-        const int slot_id = 2 * (u0 + i) + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
-        return base + (long long)slot_id * stride;
-    };
-    if (lane < H) {
-        float mh = -INFINITY;
-#pragma unroll 4  // several independent loads in flight
-        for (int i = 0; i < n_pieces; ++i) mh = fmaxf(mh, piece(i)[lane]);
-        // A piece whose keys were all dropped has m = -inf and l = 0, and
-        // ex2.approx(-inf) is +0, so it adds nothing; when every piece is
-        // empty (M = -inf) the offset 0 stands in for M and avoids -inf - -inf.
-        const float mo = mh == -INFINITY ? 0.f : mh;
-        float lh = 0.f;
-#pragma unroll 4
-        for (int i = 0; i < n_pieces; ++i) {
-            const float *p = piece(i);
-            lh = __fadd_rn(lh, __fmul_rn(p[H + lane], ex2(__fsub_rn(p[lane], mo))));
-        }
-        sm_m[wib][lane] = mo;
-        sm_l[wib][lane] = lh;
-        if (mlrow) {
-            mlrow[2 * lane] = mh;
-            mlrow[2 * lane + 1] = lh;
-        }
-    }
-    __syncwarp();
+    if (row_ptr[t] != row_ptr[t + 1]) return;
     if constexpr (WV) {
-        float acc[CH];
-        int hd[CH];
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            acc[k] = 0.f;
-            const int ch = lane + 32 * k;
-            hd[k] = ch < E ? ch / d : 0;
-        }
-#pragma unroll 2
-        for (int i = 0; i < n_pieces; ++i) {
-            const float *p = piece(i);
-#pragma unroll
-            for (int k = 0; k < CH; ++k) {
-                const int ch = lane + 32 * k;
-                if (ch < E) {
-                    const float w = ex2(__fsub_rn(p[hd[k]], sm_m[wib][hd[k]]));
-                    acc[k] = __fmaf_rn(p[2 * H + ch], w, acc[k]);
-                }
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            const int ch = lane + 32 * k;
-            if (ch < E) {
-                const float lh = sm_l[wib][hd[k]];
-                const float v = __fmul_rn(acc[k], lh > 0.f ? __frcp_rn(lh) : 0.f);
-                if constexpr (sizeof(T) == 2) reinterpret_cast<__half *>(mrow)[ch] = __float2half_rn(v);
-                else reinterpret_cast<float *>(mrow)[ch] = v;
-            }
+        T *mrow = (T *)mixed + ((long long)b * L + t) * E;
+        for (int c = lane; c < E; c += 32) mrow[c] = T(0.f);
+    }
+    if (ml) {
+        float *mlrow = ml + ((long long)b * L + t) * H * 2;
+        for (int h = lane; h < H; h += 32) {
+            mlrow[2 * h] = -INFINITY;
+            mlrow[2 * h + 1] = 0.f;
         }
     }
 }
@@ -208,7 +134,8 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.score_scale = a.score_scale;
     const long long slots = a.B * g->n_units;
     if (slots == 0) return PMHA_OK;
-    if (g->n_merge > 0 && !a.kpm) PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(a.B * g->n_merge) * 4, s));
+    // arrival counts of the pieces of crossing targets (the edge kernel merges them)
+    if (g->n_merge > 0) PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(a.B * g->n_merge) * 4, s));
     StageTimer timer(a.with_values ? "edge_attn" : "edge_scores", s);
     const pmha_status st = dt == TcType::F16 ? stream::launch_f16(cpl, lpe, a.with_values, k, slots, s)
                                              : stream::launch_f32(cpl, lpe, a.with_values, k, slots, s);
@@ -218,51 +145,25 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     return PMHA_OK;
 }
 
-namespace {
-template <typename T, bool WV, int CH>
-void launch_merge(const pmha_graph *g, const EdgeArgs &a, unsigned blocks, cudaStream_t s)
+// Targets that cross a unit boundary are merged inside the edge kernel (by
+// the slot that writes their last piece); this launch only gives the targets
+// without edges their zero mix and (m, l) = (-inf, 0).
+pmha_status empty_targets(TcType dt, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s)
 {
-    k_merge<T, WV, CH><<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, a.part, g->n_units, (int)a.B,
-                                              (int)g->L, (int)a.E, (int)a.H, (int)(a.E / a.H), a.mixed, a.ml, a.kpm == nullptr);
-}
-template <typename T, bool WV>
-bool launch_merge_ch(int E, const pmha_graph *g, const EdgeArgs &a, unsigned blocks, cudaStream_t s)
-{
-    const int ch = (E + 31) / 32;
-    if (ch <= 1) launch_merge<T, WV, 1>(g, a, blocks, s);
-    else if (ch <= 2) launch_merge<T, WV, 2>(g, a, blocks, s);
-    else if (ch <= 4) launch_merge<T, WV, 4>(g, a, blocks, s);
-    else if (ch <= 8) launch_merge<T, WV, 8>(g, a, blocks, s);
-    else if (ch <= 16) launch_merge<T, WV, 16>(g, a, blocks, s);
-    else return false;
-    return true;
-}
-}  // namespace
-
-// Without a key_padding_mask, targets that cross a unit boundary are merged
-// inside the edge kernel (by the slot that writes their last piece) and this
-// launch only gives the targets without edges their zero mix and (m, l) =
-// (-inf, 0); with a mask it merges the crossing targets too.
-pmha_status split_merge(TcType dt, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s)
-{
-    if (g->n_merge == 0 || (g->n_empty == 0 && !a.kpm)) return PMHA_OK;
+    if (g->n_merge == 0 || g->n_empty == 0) return PMHA_OK;
     const long long warps = a.B * g->n_merge;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
-    StageTimer timer("split_merge", s);
-    if (a.H > 32) {
-        set_error("split_merge: at most 32 heads");
-        return PMHA_ERR_UNSUPPORTED;
-    }
-    bool ok;
-    if (dt == TcType::F16)
-        ok = a.with_values ? launch_merge_ch<__half, true>((int)a.E, g, a, blocks, s)
-                           : launch_merge_ch<__half, false>((int)a.E, g, a, blocks, s);
-    else
-        ok = a.with_values ? launch_merge_ch<float, true>((int)a.E, g, a, blocks, s)
-                           : launch_merge_ch<float, false>((int)a.E, g, a, blocks, s);
-    if (!ok) {
-        set_error("split_merge: embed_dim %lld is wider than 512", (long long)a.E);
-        return PMHA_ERR_UNSUPPORTED;
+    StageTimer timer("empty_targets", s);
+    auto go = [&](auto kern) {
+        kern<<<blocks, 256, 0, s>>>(g->merge_t, g->n_merge, g->row_ptr, (int)a.B, (int)g->L, (int)a.E, (int)a.H,
+                                    a.mixed, a.ml);
+    };
+    if (dt == TcType::F16) {
+        if (a.with_values) go(k_empty_targets<__half, true>);
+        else go(k_empty_targets<__half, false>);
+    } else {
+        if (a.with_values) go(k_empty_targets<float, true>);
+        else go(k_empty_targets<float, false>);
     }
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());

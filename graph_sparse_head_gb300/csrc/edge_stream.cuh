@@ -8,10 +8,10 @@
 // lanes that own one row of channels, a lane owning CPL consecutive channels
 // (one whole head when the head has at most 16 channels). A warp runs the
 // same unit for 32 / LPE samples side by side, so its slots never diverge.
-// Every slot does the same gather work whatever the in-degrees, and no
-// target needs atomics: a target inside one unit is finished there, a target
-// crossing a unit boundary leaves partial softmax states that the merge
-// kernel combines.
+// Every slot does the same gather work whatever the in-degrees: a target
+// inside one unit is finished there; a target crossing a unit boundary leaves
+// partial softmax states, and the slot that writes its last piece (counted
+// with one atomic per sample and target) combines them in unit order.
 //
 // Per edge, a lane gathers its chunks of the source's k and v rows through
 // cp.async into a per-lane ring of shared-memory stages, kDepth edges ahead
@@ -434,12 +434,10 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
 #pragma unroll
                 for (int j = 0; j < NP; ++j) reinterpret_cast<float2 *>(p + 2 * a.H + c0)[j] = upk(acc2[j]);
             }
-            // Without a key_padding_mask, the slot that writes a target's last
-            // piece merges all its pieces: each writer publishes its piece
-            // (fence) and counts it; the one that completes the count reads
-            // every piece in piece order. (With a mask the kernel is short of
-            // registers; the separate merge kernel combines the pieces.)
-            if constexpr (!KPM) {
+            // The slot that writes a target's last piece merges all its
+            // pieces: each writer publishes its piece (fence) and counts it;
+            // the one that completes the count reads every piece in piece order.
+            {
             __threadfence();
             __syncwarp(smask);
             const int beg = a.row_ptr[t], end = a.row_ptr[t + 1];

@@ -17,10 +17,10 @@ namespace pmha {
 // Work plan: the CSR positions [0, nnz) of one sample are cut into units of
 // kUnitEdges consecutive positions. A unit walks the targets its positions
 // belong to, in order. A target whose edges all lie in one unit is finished
-// there; a target that crosses a unit boundary (and a target with no edge)
-// is finished by the merge kernel, from partial softmax states that the
-// units write to two slots per unit: slot 2u for the unit's first target,
-// slot 2u + 1 for its last.
+// there; a target that crosses a unit boundary is finished by the slot that
+// writes its last piece, from partial softmax states that the units write to
+// two slots per unit: slot 2u for the unit's first target, slot 2u + 1 for
+// its last. Targets with no edge get their zero mix from a small kernel.
 // --------------------------------------------------------------------------
 
 #ifndef PMHA_UNIT_EDGES
@@ -35,7 +35,7 @@ struct pmha_graph {
     int64_t nnz_given = 0, nnz = 0;   // nnz counts appended self-loops
     int64_t max_deg = 0;
     int64_t n_units = 0;              // units per sample, ceil(nnz / kUnitEdges)
-    int64_t n_merge = 0;              // targets finished by the merge kernel
+    int64_t n_merge = 0;              // targets crossing a unit boundary or without edges
     int device = 0;
     int32_t *row_ptr = nullptr;       // L + 1
     int32_t *col = nullptr;           // nnz, source per CSR position
@@ -145,7 +145,7 @@ struct EdgeArgs {
 // `t` is the intermediate type (F16 or F32) of q, k, v and mixed.
 bool edge_supported(int64_t E, int64_t H, TcType t);
 pmha_status edge_attention(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
-pmha_status split_merge(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
+pmha_status empty_targets(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);
 
 // Y (M x N) = X (M x K, pitch ldx) . W^T (W: N x K, pitch ldw) on the tensor
 // cores, one weight matrix, no bias, 16-bit operands of one type; out F16 or
