@@ -134,6 +134,10 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.score_scale = a.score_scale;
     const long long slots = a.B * g->n_units;
     if (slots == 0) return PMHA_OK;
+    if (a.v_off != a.E) {  // the kernel copies a row's k and v bytes as one run
+        set_error("edge attention: v must follow k in the projected rows");
+        return PMHA_ERR_UNSUPPORTED;
+    }
     // arrival counts of the pieces of crossing targets (the edge kernel merges them)
     if (g->n_merge > 0) PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(a.B * g->n_merge) * 4, s));
     StageTimer timer(a.with_values ? "edge_attn" : "edge_scores", s);

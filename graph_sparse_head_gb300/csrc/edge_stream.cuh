@@ -42,6 +42,9 @@ namespace stream {
 #ifndef PMHA_STREAM_WARPS
 #define PMHA_STREAM_WARPS 2
 #endif
+#ifndef PMHA_STREAM_LINE_COPY
+#define PMHA_STREAM_LINE_COPY 1
+#endif
 constexpr int kWarps = PMHA_STREAM_WARPS;  // warps per block
 constexpr int kDepth = PMHA_STREAM_DEPTH;  // edges in flight per slot (even: two per step)
 constexpr int kRing = kDepth + 2;          // stages: a stage is refilled one step after it was read
@@ -237,6 +240,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     if (gw >= groups * a.n_units) return;
     const int u = (int)(gw % a.n_units);
     const int b = (int)(gw / a.n_units) * P + slot;
+    const unsigned live = __ballot_sync(0xffffffffu, b < a.B);  // lanes of the slots that run
     if (b >= a.B) return;  // the whole slot leaves together
     const int e0 = u * kUnitEdges;
     const int n = (int)min((long long)kUnitEdges, a.nnz - e0);
@@ -248,6 +252,24 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     const bool head_leader = (grp & (lph - 1)) == 0;
 
     const uint32_t sbase = smem_u32(smem_dyn) + (uint32_t)(warp * kRing * STAGE + lane * CB);
+    // Row copies by the whole slot: the k|v bytes of a row (v right after k)
+    // are cut into 16-byte chunks and lane grp copies chunks q * LPE + grp, so
+    // every cp.async instruction reads whole 32-byte sectors (a lane copying
+    // only its own 32 bytes reads half sectors, twice). A chunk lands where
+    // its consumer lane reads it, so each wait is followed by a warp barrier.
+    constexpr bool kLineCopy = PMHA_STREAM_LINE_COPY && CB >= 16;
+    constexpr int RK = LPE * CB;  // bytes of a row's k part (= E elements)
+    const uint32_t sslot = smem_u32(smem_dyn) + (uint32_t)(warp * kRing * STAGE + slot * LPE * CB);
+    const char *KVs = (const char *)a.kv + (long long)b * a.S * a.kv_ld * (long long)sizeof(T);
+    auto copy_row = [&](uint32_t dst, const char *row) {
+#pragma unroll
+        for (int q = 0; q < NR * CB / 16; ++q) {
+            const int c = q * LPE + grp;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * c + (q >= CB / 16 ? 32 * CB - RK : 0)),
+                         "l"(row + 16 * c)
+                         : "memory");
+        }
+    };
     const char *KVb = (const char *)a.kv + ((long long)b * a.S * a.kv_ld + c0) * (long long)sizeof(T);
     const long long row_bytes = a.kv_ld * (long long)sizeof(T);
     const long long v_bytes = a.v_off * (long long)sizeof(T);
@@ -273,17 +295,22 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
         }
         const int s0 = __shfl_sync(smask, cw0, j & (LPE - 1), LPE);
         const int s1 = __shfl_sync(smask, cw0, (j + 1) & (LPE - 1), LPE);
-        if (j < n) {
-            const char *row = KVb + (long long)s0 * row_bytes;
-            const uint32_t dst = sbase + (uint32_t)(sj * STAGE);
-            cp_async<CB>(dst, row);
-            if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
-        }
-        if (j + 1 < n) {
-            const char *row = KVb + (long long)s1 * row_bytes;
-            const uint32_t dst = sbase + (uint32_t)((sj + 1) * STAGE);
-            cp_async<CB>(dst, row);
-            if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
+        if constexpr (kLineCopy) {
+            if (j < n) copy_row(sslot + (uint32_t)(sj * STAGE), KVs + (long long)s0 * row_bytes);
+            if (j + 1 < n) copy_row(sslot + (uint32_t)((sj + 1) * STAGE), KVs + (long long)s1 * row_bytes);
+        } else {
+            if (j < n) {
+                const char *row = KVb + (long long)s0 * row_bytes;
+                const uint32_t dst = sbase + (uint32_t)(sj * STAGE);
+                cp_async<CB>(dst, row);
+                if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
+            }
+            if (j + 1 < n) {
+                const char *row = KVb + (long long)s1 * row_bytes;
+                const uint32_t dst = sbase + (uint32_t)((sj + 1) * STAGE);
+                cp_async<CB>(dst, row);
+                if constexpr (WV) cp_async<CB>(dst + 32 * CB, row + v_bytes);
+            }
         }
         cp_async_commit();
     };
@@ -528,6 +555,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     int rs = 0;
     for (int j = 0; j < n; j += 2) {
         cp_async_wait<kDepth / 2 - 1>();
+        if constexpr (kLineCopy) __syncwarp(live);  // the other lanes' chunks of these rows
         const uint32_t st0 = sbase + (uint32_t)(rs * STAGE);
         const uint32_t st1 = st0 + (uint32_t)STAGE;
         const Raw<CB> kr0 = lds_raw<CB>(st0);
