@@ -184,7 +184,7 @@ pmha_status check_params(const pmha_graph *g, const pmha_params *p, int64_t batc
 }
 
 struct Layout {
-    size_t qkv = 0, mixed = 0, part = 0, ml = 0, scores = 0, wo16 = 0, vt = 0, counters = 0, total = 0;
+    size_t qkv = 0, mixed = 0, part = 0, ml = 0, scores = 0, wo16 = 0, vt = 0, counters = 0, kpm_bits = 0, total = 0;
 };
 
 bool out_proj_on_tensor_cores(const pmha_params *p)
@@ -218,6 +218,8 @@ Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode w
     if (with_values && dense_supported(g, E, H, inter_type(p->dtype))) o += align256(dense_vt_bytes(g, B, E));
     l.counters = o;
     o += align256((size_t)(B * g->n_merge) * 4);
+    l.kpm_bits = o;  // a key_padding_mask per CSR position, when one is given
+    o += align256((size_t)(B * ((g->nnz + 31) / 32)) * 4);
     l.total = o;
     return l;
 }
@@ -319,6 +321,7 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.with_values = with_values;
     a.kpm = kpm;
     a.counters = (int *)(ws + lay.counters);
+    a.kpm_bits = (uint32_t *)(ws + lay.kpm_bits);
     const TcType it = inter_type(p->dtype);
     if (args_out) *args_out = a;
     if (allow_dense && with_values && dense_supported(g, E, H, it)) {

@@ -45,6 +45,26 @@ __global__ void __launch_bounds__(256) k_empty_targets(const int32_t *__restrict
     }
 }
 
+// key_padding_mask per CSR position: warp w reads the sources of positions
+// 32 w .. 32 w + 31 once and, for every sample b, sets bit p of word (b, w)
+// when the source at position 32 w + p is dropped in b.
+__global__ void __launch_bounds__(256) k_kpm_bits(const int32_t *__restrict__ col, long long nnz,
+                                                  const uint8_t *__restrict__ kpm, int S, int B, long long n_kw,
+                                                  uint32_t *__restrict__ bits)
+{
+    const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= n_kw) return;  // whole warps
+    const long long pos = w * 32 + lane;
+    const int src = pos < nnz ? col[pos] : -1;
+#pragma unroll 4
+    for (int b = 0; b < B; ++b) {
+        const bool drop = src >= 0 && kpm[(long long)b * S + src] != 0;
+        const unsigned word = __ballot_sync(0xffffffffu, drop);
+        if (lane == 0) bits[(long long)b * n_kw + w] = word;
+    }
+}
+
 // weights[b, e, h] = 2^(s - m) / l for the target of edge e; averaged over
 // heads when out has one entry per edge. Runs in place when out == scores
 // (per-head layout: each thread reads its H scores before writing them).
@@ -120,6 +140,8 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.perm = g->perm;
     k.unit_first_t = g->unit_first_t;
     k.kpm = a.kpm;
+    k.kpm_bits = a.kpm_bits;
+    k.n_kw = (g->nnz + 31) / 32;
     k.counters = a.counters;
     k.merge_pos = g->merge_pos;
     k.n_merge = g->n_merge;
@@ -137,6 +159,13 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     if (a.v_off != a.E) {  // the kernel copies a row's k and v bytes as one run
         set_error("edge attention: v must follow k in the projected rows");
         return PMHA_ERR_UNSUPPORTED;
+    }
+    if (a.kpm) {
+        // the mask per CSR position, as bits
+        StageTimer bits_timer("kpm_bits", s);
+        k_kpm_bits<<<(unsigned)((k.n_kw + 7) / 8), 256, 0, s>>>(g->col, g->nnz, a.kpm, (int)g->S, (int)a.B, k.n_kw,
+                                                               a.kpm_bits);
+        count_launch();
     }
     // arrival counts of the pieces of crossing targets (the edge kernel merges them)
     if (g->n_merge > 0) PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(a.B * g->n_merge) * 4, s));

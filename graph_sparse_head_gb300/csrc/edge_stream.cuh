@@ -63,6 +63,8 @@ struct Args {
     const int32_t *perm;
     const int32_t *unit_first_t;
     const uint8_t *kpm;  // (B, S) key_padding_mask, nonzero = key dropped; or null
+    const uint32_t *kpm_bits;  // (B, n_kw) the mask per CSR position, 32 positions a word
+    long long n_kw;
     int *counters;             // (B, n_merge) pieces written per crossing target (zero at launch)
     const int32_t *merge_pos;  // L, index of a target in the merge list
     long long n_merge;
@@ -334,21 +336,20 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
         return __shfl_sync(smask, perm_cur, j & (LPE - 1), LPE);
     };
 
-    // ---- key_padding_mask of the sources, one window of LPE positions ahead
-    // (lane grp holds the flag of position w * LPE + grp)
-    const uint8_t *kpm_b = KPM ? a.kpm + (long long)b * a.S : nullptr;
-    auto ldmask = [&](int w) -> int {
-        const int p = w * LPE + grp;
-        return (KPM && p < n) ? (int)kpm_b[colu[p]] : 0;
-    };
-    int mw = 0, km_cur = ldmask(0), km_nxt = ldmask(1);
-    auto masked = [&](int j) -> bool {  // j never decreases
-        if (j >= (mw + 1) * LPE) {
-            ++mw;
-            km_cur = km_nxt;
-            km_nxt = ldmask(mw + 1);
+    // ---- key_padding_mask per CSR position (one bit each, 32 positions a
+    // word, the next word prefetched): every lane holds the same word
+    const uint32_t *kb = KPM ? a.kpm_bits + (long long)b * a.n_kw : nullptr;
+    auto ldword = [&](int w) -> uint32_t { return (KPM && w < a.n_kw) ? kb[w] : 0u; };
+    int kwi = e0 >> 5;
+    uint32_t kw_cur = ldword(kwi), kw_nxt = ldword(kwi + 1);
+    auto masked = [&](int j) -> bool {  // j never decreases, by at most 32 per call
+        const int pos = e0 + j;
+        if ((pos >> 5) != kwi) {
+            ++kwi;
+            kw_cur = kw_nxt;
+            kw_nxt = ldword(kwi + 1);
         }
-        return __shfl_sync(smask, km_cur, j & (LPE - 1), LPE) != 0;
+        return (kw_cur >> (pos & 31)) & 1u;
     };
 
     // ---- target bounds: lane grp holds row_ptr[tw + grp + 1], the end of target tw + grp

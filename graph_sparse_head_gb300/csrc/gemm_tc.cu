@@ -52,14 +52,17 @@ constexpr int kStageBytes = kTileABytes + kTileBBytes;
 #ifndef PMHA_GEMM_EPI_GROUPS
 #define PMHA_GEMM_EPI_GROUPS 2
 #endif
-constexpr int kEpi = PMHA_GEMM_EPI_GROUPS;  // epilogue warpgroups (1 or 2)
-static_assert(kEpi == 1 || kEpi == 2, "one or two epilogue groups");
+constexpr int kEpi = PMHA_GEMM_EPI_GROUPS;  // epilogue warpgroups (1 to 3)
+static_assert(kEpi >= 1 && kEpi <= 3, "one to three epilogue groups");
+constexpr int kAcc = kEpi == 1 ? 2 : kEpi;   // TMEM accumulators (one per group, or two for one group)
+constexpr int kBufs = kEpi == 1 ? 2 : kEpi;  // staging tiles (one per group, or two for one group)
 constexpr int kThreads = 64 + 128 * kEpi;
-constexpr int kTmemCols = 2 * BN;
+constexpr int kTmemCols = kAcc * BN <= 256 ? 256 : 512;  // a power of two
 constexpr int kOutBoxBytes = BM * 128;             // 128 rows x 64 16-bit columns, 128-byte swizzle
 constexpr int kOutTileBytes = 2 * kOutBoxBytes;     // one 128 x 128 output tile
 constexpr int kBiasBytes = kEpi * BN * 4;  // fp32 bias of the tile, per group
-constexpr int kSmemBytes = kStages * kStageBytes + 2 * kOutTileBytes + kBiasBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kSmemBytes = kStages * kStageBytes + kBufs * kOutTileBytes + kBiasBytes + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B of one 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), both
@@ -143,13 +146,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *tiles = smem;
     uint8_t *staging = smem + kStages * kStageBytes;  // two output tiles
-    float *bias_s = (float *)(staging + 2 * kOutTileBytes);  // [kEpi][BN]
-    uint64_t *bars = (uint64_t *)(staging + 2 * kOutTileBytes + kBiasBytes);
+    float *bias_s = (float *)(staging + kBufs * kOutTileBytes);  // [kEpi][BN]
+    uint64_t *bars = (uint64_t *)(staging + kBufs * kOutTileBytes + kBiasBytes);
     uint64_t *full = bars;                    // [kStages]
     uint64_t *empty = bars + kStages;         // [kStages]
-    uint64_t *acc_full = bars + 2 * kStages;  // [2]
-    uint64_t *acc_empty = acc_full + 2;       // [2]
-    uint64_t *mma_done = acc_empty + 2;       // [1]
+    uint64_t *acc_full = bars + 2 * kStages;  // [kAcc]
+    uint64_t *acc_empty = acc_full + kAcc;    // [kAcc]
+    uint64_t *mma_done = acc_empty + kAcc;    // [1]
     uint32_t *tmem_holder = (uint32_t *)(mma_done + 1);
     volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
     int *issued = (int *)(tmem_holder + 2);  // [kStages]: TMA phases armed per stage
@@ -173,7 +176,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             mbar_init(smem_u32(&empty[s]), 1);
             issued[s] = 0;
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kAcc; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
             mbar_init(smem_u32(&acc_empty[i]), 128);
         }
@@ -270,7 +273,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&acc_full[acc]));
-                if (++acc == 2) {
+                if (++acc == kAcc) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -293,9 +296,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         for (int i = g;; i += kEpi) {
             const int tile = blockIdx.x + i * gridDim.x;
             if (tile >= n_tiles) break;
-            const int acc = i & 1;
-            const uint32_t acc_phase = (uint32_t)(i >> 1) & 1u;
-            const int buf = kEpi == 2 ? g : acc;
+            const int acc = i % kAcc;
+            const uint32_t acc_phase = (uint32_t)(i / kAcc) & 1u;
+            const int buf = kEpi == 1 ? acc : g;
             int m_blk, n_blk, kb0, kb1;
             decode(tile, m_blk, n_blk, kb0, kb1);
             const int n_glob = n_blk * BN;
@@ -310,7 +313,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err);
             // the store that last read this group's staging tile is done
             if (et == 0) {
-                if constexpr (kEpi == 2) bulk_wait_read0();
+                if constexpr (kEpi >= 2) bulk_wait_read0();
                 else bulk_wait_read1();
             }
             // the readers of the previous tile's bias passed the barrier before its store

@@ -138,6 +138,7 @@ struct EdgeArgs {
     float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
     int *counters;        // (B, n_merge) pieces written per crossing target; zeroed before the edge kernel
     const uint8_t *kpm;   // (B, S) key_padding_mask, nonzero = key dropped, or null
+    uint32_t *kpm_bits;   // (B, ceil(nnz / 32)) scratch: bit p of word w = key of CSR position 32 w + p dropped
     int64_t B, L, S, E, H, nnz;
     float score_scale;    // log2(e) / sqrt(d)
     bool with_values;     // false: scores and (m, l) only
