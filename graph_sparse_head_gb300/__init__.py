@@ -25,6 +25,7 @@ from ._lib import (PMHA_BF16, PMHA_F32, PMHA_WEIGHTS_AVG, PMHA_WEIGHTS_NONE, PMH
 
 __all__ = [
     "Graph", "Params", "PackedMultiheadAttention", "PmhaError", "pmha_build_csr", "pmha_graph_info",
+    "pmha_graph_split_info",
     "pmha_graph_export", "pmha_forward", "pmha_forward_host", "pmha_edge_weights",
     "pmha_forward_workspace_size", "pmha_edge_weights_workspace_size", "pmha_forward_host_workspace_size",
     "pmha_device_status", "pmha_profile_enable", "pmha_profile_read", "pmha_launch_count",
@@ -144,6 +145,14 @@ def pmha_build_csr(source_index: torch.Tensor, target_index: torch.Tensor, query
 def pmha_graph_info(graph: Graph) -> dict:
     return {"nnz": graph.nnz, "query_features": graph.query_features, "key_features": graph.key_features,
             "max_in_degree": graph.max_in_degree}
+
+
+def pmha_graph_split_info(graph: Graph) -> dict:
+    """How the build split the targets: heavy targets (tensor-core path) and the light edges."""
+    n, th, ln = (ctypes.c_int64() for _ in range(3))
+    _lib.check(_lib.load().pmha_graph_split_info(graph.handle, ctypes.byref(n), ctypes.byref(th), ctypes.byref(ln)),
+               "pmha_graph_split_info")
+    return {"n_heavy": n.value, "heavy_min_degree": th.value, "light_nnz": ln.value}
 
 
 def pmha_graph_export(graph: Graph, stream=None):

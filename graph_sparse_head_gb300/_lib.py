@@ -40,6 +40,7 @@ _I64P = ctypes.POINTER(ctypes.c_int64)
 SIGNATURES = {
     "pmha_build_csr": (ctypes.c_int, [_vp, _vp, _i64, _i64, _i64, ctypes.c_int, _vp, ctypes.POINTER(_vp)]),
     "pmha_graph_info": (ctypes.c_int, [_vp, _I64P, _I64P, _I64P, _I64P]),
+    "pmha_graph_split_info": (ctypes.c_int, [_vp, _I64P, _I64P, _I64P]),
     "pmha_graph_export": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp]),
     "pmha_graph_destroy": (None, [_vp]),
     "pmha_forward_workspace_size": (_sz, [_vp, _P, _i64, ctypes.c_int]),

@@ -10,6 +10,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -184,8 +185,24 @@ pmha_status check_params(const pmha_graph *g, const pmha_params *p, int64_t batc
 }
 
 struct Layout {
-    size_t qkv = 0, mixed = 0, part = 0, ml = 0, scores = 0, wo16 = 0, vt = 0, counters = 0, kpm_bits = 0, total = 0;
+    size_t qkv = 0, mixed = 0, part = 0, ml = 0, scores = 0, wo16 = 0, vt = 0, counters = 0, kpm_bits = 0, heavy = 0,
+           total = 0;
 };
+
+// In-degree from which a target runs on the tensor-core path (graphs are
+// split when they are built): PMHA_HEAVY_MIN_DEGREE, default 0 (no split,
+// every target on the per-edge kernel, which is the faster of the two on
+// the measured workloads).
+int64_t heavy_min_degree()
+{
+    const char *e = getenv("PMHA_HEAVY_MIN_DEGREE");
+    if (e && *e) {
+        char *end = nullptr;
+        const long long v = strtoll(e, &end, 10);
+        if (end && *end == '\0' && v >= 0) return (int64_t)v;
+    }
+    return 0;
+}
 
 bool out_proj_on_tensor_cores(const pmha_params *p)
 {
@@ -216,10 +233,14 @@ Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode w
     if (with_values && out_proj_on_tensor_cores(p)) o += align256((size_t)(E * E) * 2);
     l.vt = o;
     if (with_values && dense_supported(g, E, H, inter_type(p->dtype))) o += align256(dense_vt_bytes(g, B, E));
-    l.counters = o;
-    o += align256((size_t)(B * g->n_merge) * 4);
+    l.counters = o;  // the light part of a split graph has its own merge list
+    o += align256((size_t)(B * std::max(g->n_merge, g->light ? g->light->n_merge : (int64_t)0)) * 4);
     l.kpm_bits = o;  // a key_padding_mask per CSR position, when one is given
     o += align256((size_t)(B * ((g->nnz + 31) / 32)) * 4);
+    l.heavy = o;  // the heavy-target path's qt images and per-head mixes
+    if (with_values && wmode == PMHA_WEIGHTS_NONE && p->dtype == PMHA_BF16 &&
+        heavy_supported(g, E, H, inter_type(p->dtype)))
+        o += align256(heavy_workspace_bytes(g, B));
     l.total = o;
     return l;
 }
@@ -348,6 +369,28 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
             if ((st = empty_targets(it, g, w, s)) != PMHA_OK) return st;
             if ((st = weights_finalize(g, w, wmode, weights, s)) != PMHA_OK) return st;
         }
+        if (mixed_out) *mixed_out = a.mixed;
+        return PMHA_OK;
+    }
+    if (with_values && wmode == PMHA_WEIGHTS_NONE && !kpm && !ml_keep && !args_out && key == value &&
+        p->dtype == PMHA_BF16 && heavy_supported(g, E, H, it)) {
+        // heavy targets on the tensor cores, the others on the per-edge kernel
+        // over the light part of the graph (whose empty targets include the
+        // heavy ones: their zero rows are overwritten by the heavy path)
+        if ((st = edge_attention(it, g->light, a, s)) != PMHA_OK) return st;
+        if ((st = empty_targets(it, g->light, a, s)) != PMHA_OK) return st;
+        HeavyInputs hin;
+        hin.q = a.q;
+        hin.q_ld = a.q_ld;
+        hin.x = key;
+        hin.wk = p->wk;
+        hin.wv = p->wv;
+        hin.bv = p->bv;
+        hin.mixed = a.mixed;
+        hin.workspace = ws + lay.heavy;
+        hin.B = B;
+        hin.H = H;
+        if ((st = heavy_attention(g, hin, s)) != PMHA_OK) return st;
         if (mixed_out) *mixed_out = a.mixed;
         return PMHA_OK;
     }
@@ -508,8 +551,14 @@ pmha_status pmha_build_csr(const int64_t *source_index, const int64_t *target_in
             return PMHA_ERR_INVALID_ARG;
         }
     }
-    return build_csr(source_index, target_index, nnz, query_features, key_features, add_self_loops != 0,
-                     (cudaStream_t)stream, out);
+    pmha_status st = build_csr(source_index, target_index, nnz, query_features, key_features, add_self_loops != 0,
+                               (cudaStream_t)stream, out);
+    if (st != PMHA_OK) return st;
+    if ((st = split_heavy(*out, heavy_min_degree(), (cudaStream_t)stream)) != PMHA_OK) {
+        destroy_graph(*out);
+        *out = nullptr;
+    }
+    return st;
 }
 
 pmha_status pmha_graph_info(const pmha_graph *g, int64_t *nnz_total, int64_t *L, int64_t *S, int64_t *max_deg)
@@ -522,6 +571,18 @@ pmha_status pmha_graph_info(const pmha_graph *g, int64_t *nnz_total, int64_t *L,
     if (L) *L = g->L;
     if (S) *S = g->S;
     if (max_deg) *max_deg = g->max_deg;
+    return PMHA_OK;
+}
+
+pmha_status pmha_graph_split_info(const pmha_graph *g, int64_t *n_heavy, int64_t *heavy_min_degree, int64_t *light_nnz)
+{
+    if (!g) {
+        set_error("graph is NULL");
+        return PMHA_ERR_INVALID_ARG;
+    }
+    if (n_heavy) *n_heavy = g->light ? g->n_heavy : 0;
+    if (heavy_min_degree) *heavy_min_degree = g->heavy_min_deg;
+    if (light_nnz) *light_nnz = g->light ? g->light->nnz : g->nnz;
     return PMHA_OK;
 }
 
@@ -557,14 +618,7 @@ pmha_status pmha_graph_export_by_source(const pmha_graph *g, int32_t *src_row_pt
 
 void pmha_graph_destroy(pmha_graph *g)
 {
-    if (!g) return;
-    int cur = 0;
-    cudaGetDevice(&cur);
-    if (cur != g->device) cudaSetDevice(g->device);
-    cudaFree(g->mem);
-    if (g->adj) cudaFree(g->adj);
-    if (cur != g->device) cudaSetDevice(cur);
-    delete g;
+    destroy_graph(g);
 }
 
 size_t pmha_forward_workspace_size(const pmha_graph *g, const pmha_params *p, int64_t batch, pmha_wmode wmode)
@@ -829,6 +883,10 @@ pmha_status pmha_device_status(pmha_stream stream)
     if (v != 0) {
         const int zero = 0;
         cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (v & kErrInternalBit) {
+            set_error("a kernel found its launch configuration unusable and did nothing");
+            return PMHA_ERR_CUDA;
+        }
         if (v & kErrTimeoutBit) {
             set_error("a bounded device-side wait gave up");
             return PMHA_ERR_TIMEOUT;

@@ -660,4 +660,91 @@ pmha_status build_csr(const int64_t *src, const int64_t *tgt, int64_t nnz, int64
     return build_typed<unsigned long long>(src, tgt, nnz, L, S, self_loops, stream, out);
 }
 
+void destroy_graph(pmha_graph *g)
+{
+    if (!g) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (cur != g->device) cudaSetDevice(g->device);
+    if (g->light) destroy_graph(g->light);
+    if (g->heavy_info) cudaFree(g->heavy_info);
+    if (g->mem) cudaFree(g->mem);
+    if (g->adj) cudaFree(g->adj);
+    if (cur != g->device) cudaSetDevice(cur);
+    delete g;
+}
+
+// Host-side split (one-time, like the build): the per-target degrees and
+// sources come back to the host, the heavy targets are listed by
+// non-increasing in-degree, and the light targets' edges are built into a
+// graph of their own by the same device pipeline.
+pmha_status split_heavy(pmha_graph *g, int64_t min_deg, cudaStream_t stream)
+{
+    if (min_deg <= 0 || g->dense || g->max_deg < min_deg) return PMHA_OK;
+    const int64_t L = g->L, nnz = g->nnz;
+    std::vector<int32_t> rp((size_t)L + 1), col((size_t)nnz);
+    PMHA_CUDA_TRY(cudaMemcpyAsync(rp.data(), g->row_ptr, (size_t)(L + 1) * 4, cudaMemcpyDeviceToHost, stream));
+    PMHA_CUDA_TRY(cudaMemcpyAsync(col.data(), g->col, (size_t)nnz * 4, cudaMemcpyDeviceToHost, stream));
+    PMHA_CUDA_TRY(cudaStreamSynchronize(stream));
+    std::vector<int32_t> heavy;
+    int64_t n_light = 0;
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t deg = rp[(size_t)t + 1] - rp[(size_t)t];
+        if (deg >= min_deg) heavy.push_back((int32_t)t);
+        else n_light += deg;
+    }
+    if (heavy.empty() || n_light == 0) return PMHA_OK;
+    std::stable_sort(heavy.begin(), heavy.end(), [&](int32_t x, int32_t y) {
+        return rp[(size_t)x + 1] - rp[(size_t)x] > rp[(size_t)y + 1] - rp[(size_t)y];
+    });
+    std::vector<int64_t> lsrc, ltgt;
+    lsrc.reserve((size_t)n_light);
+    ltgt.reserve((size_t)n_light);
+    for (int64_t t = 0; t < L; ++t) {
+        const int32_t b = rp[(size_t)t], e = rp[(size_t)t + 1];
+        if (e - b >= min_deg) continue;
+        for (int32_t p = b; p < e; ++p) {
+            lsrc.push_back(col[(size_t)p]);
+            ltgt.push_back(t);
+        }
+    }
+    std::vector<int4> info(heavy.size());
+    for (size_t i = 0; i < heavy.size(); ++i) {
+        const int32_t t = heavy[i], b = rp[(size_t)t], deg = rp[(size_t)t + 1] - b;
+        info[i] = make_int4(t, b, deg, (deg + 127) / 128);
+    }
+    int64_t *dl = nullptr;
+    int4 *dh = nullptr;
+    PMHA_CUDA_TRY(cudaMalloc(&dl, (size_t)n_light * 16));
+    cudaError_t ce = cudaMalloc(&dh, heavy.size() * sizeof(int4));
+    if (ce != cudaSuccess) {
+        cudaFree(dl);
+        return cuda_fail(ce, "cudaMalloc(heavy targets)");
+    }
+    pmha_graph *light = nullptr;
+    pmha_status st = PMHA_OK;
+    do {
+        if ((ce = cudaMemcpyAsync(dl, lsrc.data(), (size_t)n_light * 8, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+            break;
+        if ((ce = cudaMemcpyAsync(dl + n_light, ltgt.data(), (size_t)n_light * 8, cudaMemcpyHostToDevice, stream)) !=
+            cudaSuccess)
+            break;
+        if ((ce = cudaMemcpyAsync(dh, info.data(), info.size() * sizeof(int4), cudaMemcpyHostToDevice, stream)) !=
+            cudaSuccess)
+            break;
+        st = build_csr(dl, dl + n_light, n_light, L, g->S, false, stream, &light);  // synchronizes
+    } while (0);
+    if (ce != cudaSuccess) st = cuda_fail(ce, "heavy-target split");
+    cudaFree(dl);
+    if (st != PMHA_OK) {
+        cudaFree(dh);
+        return st;
+    }
+    g->light = light;
+    g->heavy_info = dh;
+    g->n_heavy = (int64_t)heavy.size();
+    g->heavy_min_deg = min_deg;
+    return PMHA_OK;
+}
+
 }  // namespace pmha

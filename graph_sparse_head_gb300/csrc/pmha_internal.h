@@ -60,6 +60,15 @@ struct pmha_graph {
     uint32_t *adj = nullptr;          // L * adj_words_per_row words (own allocation), or null
     int64_t adj_words_per_row = 0;
     void *mem = nullptr;              // the single allocation behind the arrays above
+    // Targets with at least heavy_min_deg edges run on the tensor cores
+    // (heavy.cu); the others keep the per-edge kernel, which then walks
+    // `light`: the same L targets and S sources with only the light targets'
+    // edges (heavy targets have none there). No split: light == nullptr.
+    int64_t heavy_min_deg = 0;
+    int64_t n_heavy = 0;
+    int4 *heavy_info = nullptr;       // n_heavy {target, first CSR position, in-degree, 128-edge tiles},
+                                      // in-degree non-increasing (own allocation)
+    pmha_graph *light = nullptr;
 };
 
 namespace pmha {
@@ -78,6 +87,7 @@ pmha_status cuda_fail(cudaError_t e, const char *what);
 int *device_error_word();
 constexpr int kErrTimeoutBit = 1;
 constexpr int kErrRangeBit = 2;
+constexpr int kErrInternalBit = 4;  // a kernel found its launch unusable (e.g. shared memory misaligned) and did nothing
 
 // ---------------------------------------------------------------- profiling
 // Records an event pair around a launch when profiling is on.
@@ -226,6 +236,29 @@ size_t dense_vt_bytes(const pmha_graph *g, int64_t B, int64_t E);
 // Steps 2-4 for every target of a dense graph: V transposed, then the
 // masked-dense tile kernel writes `mixed`.
 pmha_status dense_attention(const pmha_graph *g, const DenseInputs &in, cudaStream_t s);
+// ---------------------------------------------------------------- heavy targets
+struct HeavyInputs {
+    const void *q;        // projected q rows (B, L) fp16 of pitch q_ld
+    int64_t q_ld;
+    const void *x;        // key tokens (B, S, E) bf16: the key and value input (one tensor)
+    const void *wk, *wv;  // (E, E) bf16
+    const void *bv;       // (E) bf16 or null
+    void *mixed;          // (B, L, E) fp16: the heavy targets' rows are written
+    void *workspace;      // heavy_workspace_bytes(g, B), 256-byte aligned
+    int64_t B, H;
+};
+// The tensor-core path for heavy targets applies: the graph was split, fp16
+// intermediates, embed_dim 128, at most 8 heads.
+bool heavy_supported(const pmha_graph *g, int64_t E, int64_t H, TcType t);
+size_t heavy_workspace_bytes(const pmha_graph *g, int64_t B);
+// Steps 2-4 for the heavy targets of g (writes their mixed rows).
+pmha_status heavy_attention(const pmha_graph *g, const HeavyInputs &in, cudaStream_t s);
+// Splits a built graph: targets with at least min_deg edges become heavy,
+// the rest form g->light. No split when min_deg <= 0, the graph is dense,
+// or either side would be empty. Synchronizes the stream.
+pmha_status split_heavy(pmha_graph *g, int64_t min_deg, cudaStream_t stream);
+void destroy_graph(pmha_graph *g);
+
 // weights[b, e(, h)] from raw scores and (m, l); in place when out == scores.
 pmha_status weights_finalize(const pmha_graph *g, const EdgeArgs &a, pmha_wmode mode, float *out,
                              cudaStream_t s);

@@ -119,6 +119,24 @@ pmha_status pmha_build_csr(const int64_t *source_index, const int64_t *target_in
 pmha_status pmha_graph_info(const pmha_graph *graph, int64_t *nnz_total, int64_t *query_features,
                             int64_t *key_features, int64_t *max_in_degree);
 
+/* How pmha_build_csr split the targets for pmha_forward (host outputs, any
+ * may be NULL). Targets with at least heavy_min_degree incoming edges
+ * ("heavy") run on the tensor-core path when pmha_forward computes values
+ * without weights and without a key_padding_mask, for a bf16 layer with
+ * embed_dim 128, at most 8 heads and key == value (the same pointer): their
+ * scores and mix are two dense products per 128 edges over the gathered key
+ * tokens (Notes steps 2-4 rewritten through the step 1 projections:
+ * q.k_s = (Wk^T q).x_s + a per-target constant, sum w v_s = Wv (sum w x_s)
+ * + bv). The other targets keep the per-edge kernel. The threshold is the
+ * value of the environment variable PMHA_HEAVY_MIN_DEGREE when the graph is
+ * built; unset or 0 means no split (the default: on the measured workloads
+ * the per-edge kernel is faster). n_heavy = 0 means no split (no threshold,
+ * no target reaches it, every target does, or the graph is dense);
+ * light_nnz counts the edges of the other targets.
+ * Errors: PMHA_ERR_INVALID_ARG (graph NULL). */
+pmha_status pmha_graph_split_info(const pmha_graph *graph, int64_t *n_heavy, int64_t *heavy_min_degree,
+                                  int64_t *light_nnz);
+
 /* Copy the per-target view into caller device buffers (int32):
  *  row_ptr (L + 1)  edges into target t are positions row_ptr[t] .. row_ptr[t+1]-1,
  *  col (nnz_total)  source index of each position, ascending within a target,

@@ -66,6 +66,7 @@ def test_host_checks_before_device_work(lib):
     assert lib.pmha_edge_weights(None, None, None, None, None, 1, 1, None, None, 0, None) == 1
     assert lib.pmha_forward_workspace_size(None, None, 1, 0) == 0
     assert lib.pmha_graph_info(None, None, None, None, None) == 1
+    assert lib.pmha_graph_split_info(None, None, None, None) == 1
     lib.pmha_graph_destroy(None)
     assert lib.pmha_profile_enable(0) == 0
     assert lib.pmha_launch_count() >= 0
