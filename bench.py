@@ -112,9 +112,9 @@ KERNEL_SOURCES = {
 }
 
 
-def ncu_traffic(stage: str):
+def ncu_traffic(stage: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel; else None."""
+    on the current source of that kernel and on this workload; else None."""
     p = os.path.join(PROFILE_DIR, "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -122,6 +122,8 @@ def ncu_traffic(stage: str):
         d = json.load(f)
     e = d.get(stage)
     if not e or e.get("source_digest") != source_digest(KERNEL_SOURCES[stage]):
+        return None
+    if e.get("workload", "").split(",")[0].strip() != workload:
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -461,19 +463,23 @@ def bench_ours(args):
         avg_s = stages[dom]["avg_us"] / 1e6
         alg = algorithmic_bytes(dom, w, B, nnz)
         fl = stage_flops(dom, w, B)
-        if dom in TENSOR_BOUND and fl is not None:
+        # a GEMM is tensor-bound when its arithmetic intensity passes the ridge
+        # point of the two measured peaks (E = 512), else memory-bound (E = 128)
+        ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        tensor_bound = fl is not None and (dom in TENSOR_BOUND or (alg is not None and fl / alg > ridge))
+        if tensor_bound:
             # timed inside a long loop of steps: the sustained tensor peak
             achieved = fl / avg_s / 1e12
             peak = peaks["bf16_tflops_sustained"]
             roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": ncu_traffic(dom), "algorithmic_flops_per_launch": fl,
+                    "frac": achieved / peak, "traffic": ncu_traffic(dom, w.name), "algorithmic_flops_per_launch": fl,
                     "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
                     "peak_source": f"{peaks['source']} sustained bf16 GEMM (MEASURED_PEAKS.json "
                                    "bf16_tflops_sustained; fp16 runs at the bf16 rate)"}
         elif alg is not None:
             achieved = alg / avg_s / 1e9
             roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom),
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom, w.name),
                     "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
                     "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
     for k, v in stages.items():

@@ -43,16 +43,17 @@ struct DenseLayout {
     static constexpr int DC = D / 64;               // 64-channel chunks of a head
     static constexpr int kQBytes = DC * kTM * 128;   // q tile
     static constexpr int kKBytes = DC * kTN * 128;   // k tile (two stages)
-    static constexpr int kVBytes = 2 * D * 128;      // v^T tile (one stage): 2 chunks of 64 sources
+    static constexpr int kVBytes = 2 * D * 128;      // v^T tile: 2 chunks of 64 sources (two stages)
     static constexpr int kPBytes = 2 * kTM * 128;    // P: 2 chunks of 64 sources
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + 2 * kKBytes;
-    static constexpr int kOffP = kOffV + kVBytes;
+    static constexpr int kOffP = kOffV + 2 * kVBytes;
     static constexpr int kOffWords = kOffP + kPBytes;  // uint32 [2][4] source-validity words
     static constexpr int kOffBars = kOffWords + 32;
-    static constexpr int kSmem = kOffBars + 160 + 1024;  // + alignment slack
+    static constexpr int kSmem = kOffBars + 160;     // the base is 1024-byte aligned (checked)
 };
+static_assert(2 * (DenseLayout<64>::kSmem + 1024) <= 233472, "two CTAs per SM at head_dim 64");
 
 struct DenseArgs {
     int B, L, S, H, n_tiles_t;
@@ -109,6 +110,21 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// a row's reference maximum moves only when a score passes it by more than this (log2 units)
+constexpr float kLazy = 8.f;
 
 // head_dim 64: two CTAs per SM (registers capped at 170 a thread); 128: one
 template <int D>
@@ -117,24 +133,22 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              const __grid_constant__ CUtensorMap tm_vt, DenseArgs a)
 {
     using LY = DenseLayout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem[];
     uint32_t *words = (uint32_t *)(smem + LY::kOffWords);
     uint64_t *bars = (uint64_t *)(smem + LY::kOffBars);
     uint64_t *q_full = bars;         // [1]
     uint64_t *k_full = bars + 1;     // [2]
     uint64_t *k_empty = bars + 3;    // [2]
-    uint64_t *v_full = bars + 5;     // [1]
-    uint64_t *v_empty = bars + 6;    // [1]
-    uint64_t *s_full = bars + 7;     // [1]
-    uint64_t *s_free = bars + 8;     // [1]
-    uint64_t *p_full = bars + 9;     // [1]
-    uint64_t *o_full = bars + 10;    // [1]
-    uint64_t *o_free = bars + 11;    // [1]
-    uint64_t *mma_done = bars + 12;  // [1]
-    uint32_t *tmem_holder = (uint32_t *)(bars + 13);
+    uint64_t *v_full = bars + 5;     // [2]
+    uint64_t *v_empty = bars + 7;    // [2]
+    uint64_t *s_full = bars + 9;     // [1]
+    uint64_t *s_free = bars + 10;    // [1]
+    uint64_t *p_full = bars + 11;    // [1]
+    uint64_t *o_full = bars + 12;    // [1] one phase per P V product
+    uint64_t *mma_done = bars + 13;  // [1]
+    uint32_t *tmem_holder = (uint32_t *)(bars + 14);
     volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
-    int *issued = (int *)(tmem_holder + 2);  // [4]: TMA phases armed (q, k stage 0, k stage 1, v)
+    int *issued = (int *)(tmem_holder + 2);  // [5]: TMA phases armed (q, k stages 0 and 1, v stages 0 and 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int it = blockIdx.x % a.n_tiles_t;
@@ -143,21 +157,26 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int t0 = it * kTM;
     const int n_steps = (a.S + kTN - 1) / kTN;
 
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(a.err, kErrInternalBit);
+        return;
+    }
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(q_full), 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&k_full[s]), 1);
             mbar_init(smem_u32(&k_empty[s]), 1);
         }
-        mbar_init(smem_u32(v_full), 1);
-        mbar_init(smem_u32(v_empty), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&v_full[s]), 1);
+            mbar_init(smem_u32(&v_empty[s]), 1);
+        }
         mbar_init(smem_u32(s_full), 1);
         mbar_init(smem_u32(s_free), 128);
         mbar_init(smem_u32(p_full), 128);
         mbar_init(smem_u32(o_full), 1);
-        mbar_init(smem_u32(o_free), 128);
         mbar_init(smem_u32(mma_done), 1);
-        issued[0] = issued[1] = issued[2] = issued[3] = 0;
+        issued[0] = issued[1] = issued[2] = issued[3] = issued[4] = 0;
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -197,11 +216,12 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             };
             bool ok = load_k(0);
             for (int j = 0; ok && j < n_steps; ++j) {
-                if (!mbar_wait(smem_u32(v_empty), (j & 1) ^ 1u, abort_flag, a.err)) break;
-                const uint32_t fb = smem_u32(v_full);
+                const int vs = j & 1;
+                if (!mbar_wait(smem_u32(&v_empty[vs]), ((j >> 1) & 1) ^ 1u, abort_flag, a.err)) break;
+                const uint32_t fb = smem_u32(&v_full[vs]);
                 mbar_arrive_expect_tx(fb, LY::kVBytes);
-                issued[3] += 1;
-                const uint32_t vdst = smem_u32(smem + LY::kOffV);
+                issued[3 + vs] += 1;
+                const uint32_t vdst = smem_u32(smem + LY::kOffV + vs * LY::kVBytes);
 #pragma unroll
                 for (int kc = 0; kc < 2; ++kc)
                     tma_load_2d(vdst + kc * D * 128, &tm_vt, b * a.S_pad + j * kTN + kc * 64, h * D, fb);
@@ -210,16 +230,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
     } else if (warp == 5) {
         if (lane == 0) {
-            // ---------------- MMA issuer
+            // ---------------- MMA issuer: S(j + 1) as soon as the softmax has read
+            // S(j), then O += P(j) V(j) (O accumulates in tensor memory)
             bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, a.err);
             tc_fence_after();
             const uint32_t qa = smem_u32(smem + LY::kOffQ);
             const uint32_t pa = smem_u32(smem + LY::kOffP);
-            const uint32_t va = smem_u32(smem + LY::kOffV);
-            for (int j = 0; ok && j < n_steps; ++j) {
+            auto issue_s = [&](int j) -> bool {
                 const int s = j & 1;
-                if (!mbar_wait(smem_u32(&k_full[s]), (j >> 1) & 1, abort_flag, a.err)) break;
-                if (j > 0 && !mbar_wait(smem_u32(s_free), (j - 1) & 1, abort_flag, a.err)) break;
+                if (!mbar_wait(smem_u32(&k_full[s]), (j >> 1) & 1, abort_flag, a.err)) return false;
+                if (j > 0 && !mbar_wait(smem_u32(s_free), (j - 1) & 1, abort_flag, a.err)) return false;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(smem + LY::kOffK + s * LY::kKBytes);
 #pragma unroll
@@ -231,19 +251,25 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                                     (c > 0 || k > 0) ? 1u : 0u);
                 mma_commit(smem_u32(s_full));
                 mma_commit(smem_u32(&k_empty[s]));
-                if (!mbar_wait(smem_u32(p_full), j & 1, abort_flag, a.err)) break;
-                if (j > 0 && !mbar_wait(smem_u32(o_free), (j - 1) & 1, abort_flag, a.err)) break;
-                if (!mbar_wait(smem_u32(v_full), j & 1, abort_flag, a.err)) break;
+                return true;
+            };
+            ok = ok && issue_s(0);
+            for (int j = 0; ok && j < n_steps; ++j) {
+                if (j + 1 < n_steps && !(ok = issue_s(j + 1))) break;
+                const int vs = j & 1;
+                if (!(ok = mbar_wait(smem_u32(p_full), j & 1, abort_flag, a.err))) break;
+                if (!(ok = mbar_wait(smem_u32(&v_full[vs]), (j >> 1) & 1, abort_flag, a.err))) break;
                 tc_fence_after();
+                const uint32_t va = smem_u32(smem + LY::kOffV + vs * LY::kVBytes);
 #pragma unroll
                 for (int kc = 0; kc < 2; ++kc)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_f16kind(tmem_o, smem_desc(pa + kc * kTM * 128) + (uint64_t)(2 * k),
                                     smem_desc(va + kc * D * 128) + (uint64_t)(2 * k), idesc_f16(kTM, D),
-                                    (kc > 0 || k > 0) ? 1u : 0u);
+                                    (j > 0 || kc > 0 || k > 0) ? 1u : 0u);
                 mma_commit(smem_u32(o_full));
-                mma_commit(smem_u32(v_empty));
+                mma_commit(smem_u32(&v_empty[vs]));
             }
             // all MMAs issued by this thread have finished once this arrives
             mma_commit(smem_u32(mma_done));
@@ -255,10 +281,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int r = threadIdx.x;  // 0..127
         const int t = t0 + r;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // m: the row's reference (log2 units), raised only when a step's maximum
+        // passes it by more than kLazy; P <= 2^kLazy stays well inside fp16
         float m = -INFINITY, l = 0.f;
-        float o[D];
-#pragma unroll
-        for (int c = 0; c < D; ++c) o[c] = 0.f;
         const uint32_t *adj_row = (a.adj && t < a.L) ? a.adj + (long long)t * a.words_per_row : nullptr;
         uint8_t *P = smem + LY::kOffP;
         bool ok = true;
@@ -308,13 +333,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 if (c + 1 < kTN / 32) tmem_wait_ld();
             }
-            const float m_new = fmaxf(m, __fmul_rn(mx, a.score_scale));
+            const float mxs = __fmul_rn(mx, a.score_scale);
+            const bool move = mxs > m + kLazy;  // also when m is still -inf and the step has a live source
+            const float m_new = move ? mxs : m;
             // ex2.approx(-inf) is +0: masked columns add nothing; the offset 0
-            // stands in for a max that is still -inf (no live source yet)
+            // stands in for a reference that is still -inf (no live source yet)
             const float m_off = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = ex2_approx(__fsub_rn(m, m_off));
-            // pass 2: P = 2^(s * scale - m) in fp16 into the swizzled A tile, and the row sum
+            const float alpha = move ? ex2_approx(__fsub_rn(m, m_off)) : 1.f;
+            // pass 2: P = 2^(s * scale - m) in fp16 (kept in registers) and the row sum
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[kTN / 32][16];
             tmem_ld32_async(tmem_s + lane_off, v0);
             tmem_wait_ld();
 #pragma unroll
@@ -322,7 +350,6 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
                 uint32_t(&nxt)[32] = (c & 1) ? v0 : v1;
                 if (c + 1 < kTN / 32) tmem_ld32_async(tmem_s + lane_off + (uint32_t)((c + 1) * 32), nxt);
-                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float p0 = ex2_approx(__fmaf_rn(__uint_as_float(cur[2 * i]), a.score_scale, -m_off));
@@ -334,60 +361,86 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     sum4[(2 * i) & 3] = __fadd_rn(sum4[(2 * i) & 3], p0);
                     sum4[(2 * i + 1) & 3] = __fadd_rn(sum4[(2 * i + 1) & 3], p1);
                     const __half2 hp = __floats2half2_rn(p0, p1);
-                    pk[i] = *reinterpret_cast<const uint32_t *>(&hp);
+                    pk[c][i] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
-                // columns c*32 .. c*32+31 = chunk c/2, 16-byte units 4*(c%2) .. +3
+                if (c + 1 < kTN / 32) tmem_wait_ld();
+            }
+            // S has been read: the MMA warp may compute S(j + 1)
+            tc_fence_before();
+            mbar_arrive(smem_u32(s_free));
+            if (j > 0) {
+                // P(j - 1) has been consumed and O holds steps 0 .. j-1 once P V(j - 1) is done;
+                // a row whose reference moved rescales its O in tensor memory now, before P V(j)
+                ok = !softmax_vote(!mbar_wait(smem_u32(o_full), (j - 1) & 1, abort_flag, a.err));
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, move)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        const uint32_t oa = tmem_o + lane_off + (uint32_t)(c * 32);
+                        tmem_ld32_async(oa, v0);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v0[i] = __float_as_uint(__fmul_rn(__uint_as_float(v0[i]), alpha));
+                        tmem_st32(oa, v0);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P into the swizzled A tile: columns c*32 .. c*32+31 = chunk c/2, 16-byte units 4*(c%2) .. +3
+#pragma unroll
+            for (int c = 0; c < kTN / 32; ++c) {
                 uint8_t *rowp = P + (c >> 1) * (kTM * 128) + r * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int u = (c & 1) * 4 + q;
                     *reinterpret_cast<uint4 *>(rowp + ((u ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        make_uint4(pk[c][4 * q], pk[c][4 * q + 1], pk[c][4 * q + 2], pk[c][4 * q + 3]);
                 }
-                if (c + 1 < kTN / 32) tmem_wait_ld();
             }
-            // S has been read: the MMA warp may overwrite it; P is ready for the tensor cores
+            // P is ready for the tensor cores (and O rescaled)
             tc_fence_before();
-            mbar_arrive(smem_u32(s_free));
             fence_async_shared();
             mbar_arrive(smem_u32(p_full));
             const float sum = __fadd_rn(__fadd_rn(sum4[0], sum4[1]), __fadd_rn(sum4[2], sum4[3]));
             l = __fadd_rn(__fmul_rn(l, alpha), sum);
             m = m_new;
-
-            ok = !softmax_vote(!mbar_wait(smem_u32(o_full), j & 1, abort_flag, a.err));
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t(&cur)[32] = (c & 1) ? v1 : v0;
-                tmem_ld32_async(tmem_o + lane_off + (uint32_t)(c * 32), cur);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[c * 32 + i] = __fmaf_rn(o[c * 32 + i], alpha, __uint_as_float(cur[i]));
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(o_free));
         }
-        if (ok && t < a.L) {
-            // mixed = O / l (a target without a live source mixes to zeros)
+        if (ok) {
+            // the last P V product completes O
+            ok = !softmax_vote(!mbar_wait(smem_u32(o_full), (n_steps - 1) & 1, abort_flag, a.err));
+            if (ok) tc_fence_after();
+        }
+        if (ok) {
+            // mixed = O / l (a target without a live source mixes to zeros). The
+            // tensor-memory loads are warp-collective: every lane runs them,
+            // only rows of real targets (t < L) store.
             const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
             __half *dst = a.mixed + ((long long)b * a.L + t) * a.E + h * D;
             bool bad = false;
 #pragma unroll
-            for (int c = 0; c < D; c += 8) {
-                uint32_t w[4];
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t ov[32];
+                tmem_ld32_async(tmem_o + lane_off + (uint32_t)(cc * 32), ov);
+                tmem_wait_ld();
+                if (t >= a.L) continue;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float x0 = __fmul_rn(o[c + 2 * i], inv), x1 = __fmul_rn(o[c + 2 * i + 1], inv);
-                    if (!(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f)) bad = true;
-                    const __half2 hv = __floats2half2_rn(x0, x1);
-                    w[i] = *reinterpret_cast<const uint32_t *>(&hv);
+                for (int c = 0; c < 32; c += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float x0 = __fmul_rn(__uint_as_float(ov[c + 2 * i]), inv);
+                        const float x1 = __fmul_rn(__uint_as_float(ov[c + 2 * i + 1]), inv);
+                        if (!(fabsf(x0) <= 65504.f) || !(fabsf(x1) <= 65504.f)) bad = true;
+                        const __half2 hv = __floats2half2_rn(x0, x1);
+                        w[i] = *reinterpret_cast<const uint32_t *>(&hv);
+                    }
+                    *reinterpret_cast<uint4 *>(dst + cc * 32 + c) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                *reinterpret_cast<uint4 *>(dst + c) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             if (bad) atomicOr(a.err, kErrRangeBit);
         }
+        if (warp < 4) tc_fence_before();
     }
 
     __syncthreads();
@@ -399,8 +452,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (issued[1 + s] > 0)
                 mbar_wait(smem_u32(&k_full[s]), (uint32_t)((issued[1 + s] - 1) & 1), (volatile int *)&dummy,
                           a.err);
-        if (issued[3] > 0)
-            mbar_wait(smem_u32(v_full), (uint32_t)((issued[3] - 1) & 1), (volatile int *)&dummy, a.err);
+        for (int s = 0; s < 2; ++s)
+            if (issued[3 + s] > 0)
+                mbar_wait(smem_u32(&v_full[s]), (uint32_t)((issued[3 + s] - 1) & 1), (volatile int *)&dummy,
+                          a.err);
     }
     __syncthreads();
     if (warp == 5) {
