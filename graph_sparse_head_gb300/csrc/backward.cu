@@ -24,6 +24,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "pmha_internal.h"
 
@@ -199,6 +200,14 @@ __device__ __forceinline__ float head_sum_rt(float x, int lph)
     for (int o = 1; o < lph; o <<= 1) x += __shfl_xor_sync(kFull, x, o);
     return x;
 }
+
+}  // namespace
+}  // namespace pmha
+
+#include "bwd_stream.cuh"  // the streaming variants (fp16, 8 or 16 channels per lane)
+
+namespace pmha {
+namespace {
 
 // The per-edge backward kernels. Like the forward's streaming kernel, a
 // "slot" of LPE = E / CPL lanes owns one sample (a lane owns CPL channels),
@@ -678,6 +687,20 @@ template <typename T, int CPL>
 bool launch_walks_lpe(int lpe, const WalkArgs &dq, const WalkArgs &dkv, cudaStream_t s)
 {
     const long long groups = (dq.B + 32 / lpe - 1) / (32 / lpe);
+    if constexpr (std::is_same<T, __half>::value && (CPL == 8 || CPL == 16)) {
+        // rows gathered through a cp.async ring, paired fp32 arithmetic
+        const unsigned grid_s = blocks(groups * dq.n_units, bwds::kWarps);
+        switch (lpe) {
+#define PMHA_WALK_S(L)                                                                   \
+    case L:                                                                              \
+        bwds::k_bwd_dq_s<CPL, L><<<grid_s, bwds::kWarps * 32, 0, s>>>(dq);               \
+        bwds::k_bwd_dkv_s<CPL, L><<<grid_s, bwds::kWarps * 32, 0, s>>>(dkv);             \
+        return true;
+            PMHA_WALK_S(1) PMHA_WALK_S(2) PMHA_WALK_S(4) PMHA_WALK_S(8) PMHA_WALK_S(16) PMHA_WALK_S(32)
+#undef PMHA_WALK_S
+        default: return false;
+        }
+    }
     const unsigned grid = blocks(groups * dq.n_units, kBwdWarps);
     switch (lpe) {
 #define PMHA_WALK(L)                                                    \
