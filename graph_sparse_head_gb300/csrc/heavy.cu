@@ -26,10 +26,13 @@
 //                           S = X qt (fp32 in tensor memory) and, once the
 //                           softmax warps wrote P, Y = X^T P
 //                 warps 2-5 one thread per tile row: scores from tensor
-//                           memory, the tile maximum per head (warp reduce
-//                           + shared memory), P = 2^(s - m) in bf16, the
-//                           running sum l, and the running mix Y read back
-//                           from tensor memory and rescaled in registers
+//                           memory, P = 2^(s - m_ref) in bf16 against a
+//                           reference per (item, head) that moves only when a
+//                           score passes it by more than kLazy (then the mix
+//                           in tensor memory and the sums are rescaled), the
+//                           running sums l; Y accumulates in tensor memory
+//                           over the item's tiles and is read once, during
+//                           the next item's first tile
 //                 An item is one (sample, heavy target); items run in order
 //                 of decreasing in-degree, dealt to the CTAs back and forth.
 //   k_heavy_out   mixed[t] = Wv_h (Y_h / l_h) + bv_h per head, fp16 rows
@@ -40,6 +43,8 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <mutex>
+#include <set>
 #include <vector>
 
 #include "pmha_internal.h"
@@ -742,6 +747,22 @@ __global__ void __launch_bounds__(128) k_heavy_out(const __half *__restrict__ yh
 
 constexpr int kItemsPerBlock = 32;  // items per block of the qt and output kernels
 
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device)
+template <typename K>
+cudaError_t set_smem_once(K kern, int bytes)
+{
+    static std::mutex mu;
+    static std::set<int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count(dev)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert(dev);
+    return e;
+}
+
 }  // namespace
 
 bool heavy_supported(const pmha_graph *g, int64_t E, int64_t H, TcType t)
@@ -783,14 +804,8 @@ pmha_status heavy_attention(const pmha_graph *g, const HeavyInputs &in, cudaStre
         count_launch();
         PMHA_CUDA_TRY(cudaGetLastError());
     }
+    PMHA_CUDA_TRY(set_smem_once(k_heavy_attn, kSmemBytes));
     {
-        static bool attr_set[64] = {false};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            PMHA_CUDA_TRY(cudaFuncSetAttribute(k_heavy_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-            attr_set[dev] = true;
-        }
         HeavyArgs a;
         a.row_ptr = g->row_ptr;
         a.col = g->col;
@@ -807,14 +822,8 @@ pmha_status heavy_attention(const pmha_graph *g, const HeavyInputs &in, cudaStre
         count_launch();
         PMHA_CUDA_TRY(cudaGetLastError());
     }
+    PMHA_CUDA_TRY(set_smem_once(k_heavy_out, kOutSmem));
     {
-        static bool attr_set[64] = {false};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            PMHA_CUDA_TRY(cudaFuncSetAttribute(k_heavy_out, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem));
-            attr_set[dev] = true;
-        }
         StageTimer timer("heavy_out", s);
         k_heavy_out<<<pre_blocks, 128, kOutSmem, s>>>(yh, (const __nv_bfloat16 *)in.wv, (const __nv_bfloat16 *)in.bv,
                                                       g->heavy_info, n_items, (int)in.B, (int)g->L, d, kItemsPerBlock,
