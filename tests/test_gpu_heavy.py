@@ -156,3 +156,42 @@ def test_skewed_workload_full_size_matches_oracle():
     ref, _ = c.oracle(need_weights=False)
     assert_close("workload 3 output (split at 32)", out.float().cpu().numpy(), ref, "bf16")
     g.destroy()
+
+
+def test_split_graph_with_padding_mask_takes_the_per_edge_path():
+    # a key_padding_mask keeps every target on the per-edge kernel: same result as the unsplit graph
+    rng = np.random.default_rng(31)
+    L = S = 2000
+    src, tgt = degree_graph(rng, L, S, mixed_degrees(rng, L, HEAVY))
+    c = Case(src, tgt, L, S, 128, 8, 2, "bf16", seed=32)
+    import synth
+    kpm = synth.padding_mask(rng, c.B, S)
+    g_split, g_plain = build(c), build(c, min_degree=0)
+    _, _, out_s, _ = c.run(DEV, "none", graph=g_split, kpm=kpm)
+    _, _, out_p, _ = c.run(DEV, "none", graph=g_plain, kpm=kpm)
+    assert torch.equal(out_s, out_p)
+    ref, _ = c.oracle(need_weights=False, kpm=kpm)
+    assert_close("masked output", out_s.float().cpu().numpy(), ref, "bf16")
+    g_split.destroy()
+    g_plain.destroy()
+
+
+def test_split_graph_backward_equals_unsplit():
+    # the backward recomputes the forward on the whole graph, split or not
+    import graph_sparse_head_gb300 as pmha
+    rng = np.random.default_rng(41)
+    L = S = 1500
+    src, tgt = degree_graph(rng, L, S, mixed_degrees(rng, L, HEAVY[:8]))
+    c = Case(src, tgt, L, S, 128, 8, 2, "bf16", seed=42)
+    params = pmha.Params.from_arrays(c.params, c.H, torch.bfloat16, DEV)
+    xq, xkv = c.device_inputs(DEV)
+    dout = torch.from_numpy(rng.standard_normal(xq.shape).astype(np.float32)).to(DEV).to(torch.bfloat16)
+    grads = []
+    for g in (build(c), build(c, min_degree=0)):
+        r = pmha.pmha_backward(g, params, xq, xkv, xkv, dout)
+        pmha.pmha_device_status()
+        grads.append({k: v.clone() for k, v in r.items() if v is not None})
+        g.destroy()
+    assert grads[0].keys() == grads[1].keys()
+    for k in grads[0]:
+        assert torch.equal(grads[0][k], grads[1][k]), k
