@@ -31,6 +31,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 #include "pmha_internal.h"
 
 namespace pmha {
@@ -88,15 +90,33 @@ __device__ __forceinline__ float ex2(float x)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// f(std::integral_constant<int, I>) for I = FIRST .. LAST-1, unrolled at compile time
+template <int I, int N, typename F>
+__device__ __forceinline__ void static_for(F &&f)
+{
+    if constexpr (I < N) {
+        f(std::integral_constant<int, I>{});
+        static_for<I + 1, N>(f);
+    }
+}
+
+// One 16-byte cp.async from src + SOFF to dst + DOFF, the offsets as
+// immediates of the address operands (no address arithmetic per chunk).
+template <int DOFF, int SOFF>
+__device__ __forceinline__ void cp_async16_at(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0+%2], [%1+%3], 16;" ::"r"(dst), "l"(src), "n"(DOFF), "n"(SOFF)
+                 : "memory");
+}
+
 template <int CB>
 __device__ __forceinline__ void cp_async(uint32_t dst, const void *src)
 {
     if constexpr (CB >= 16) {
-#pragma unroll
-        for (int i = 0; i < CB / 16; ++i)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * i),
-                         "l"((const char *)src + 16 * i)
-                         : "memory");
+        static_for<0, CB / 16>([&](auto ic) {
+            constexpr int i = decltype(ic)::value;
+            cp_async16_at<16 * i, 16 * i>(dst, src);
+        });
     } else {
         asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(CB) : "memory");
     }
@@ -115,11 +135,12 @@ __device__ __forceinline__ Raw<CB> lds_raw(uint32_t addr)
 {
     Raw<CB> r;
     if constexpr (CB % 16 == 0) {
-#pragma unroll
-        for (int i = 0; i < CB / 16; ++i)
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+        static_for<0, CB / 16>([&](auto ic) {
+            constexpr int i = decltype(ic)::value;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
                          : "=r"(r.w[4 * i]), "=r"(r.w[4 * i + 1]), "=r"(r.w[4 * i + 2]), "=r"(r.w[4 * i + 3])
-                         : "r"(addr + 16 * i));
+                         : "r"(addr), "n"(16 * i));
+        });
     } else if constexpr (CB == 8) {
         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "r"(addr));
     } else {
@@ -264,13 +285,13 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     const uint32_t sslot = smem_u32(smem_dyn) + (uint32_t)(warp * kRing * STAGE + slot * LPE * CB);
     const char *KVs = (const char *)a.kv + (long long)b * a.S * a.kv_ld * (long long)sizeof(T);
     auto copy_row = [&](uint32_t dst, const char *row) {
-#pragma unroll
-        for (int q = 0; q < NR * CB / 16; ++q) {
-            const int c = q * LPE + grp;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * c + (q >= CB / 16 ? 32 * CB - RK : 0)),
-                         "l"(row + 16 * c)
-                         : "memory");
-        }
+        // chunk q * LPE + grp: one base address per row, the chunk offsets as immediates
+        const uint32_t d0 = dst + 16 * grp;
+        const char *s0 = row + 16 * grp;
+        static_for<0, NR * CB / 16>([&](auto qc) {
+            constexpr int q = decltype(qc)::value;
+            cp_async16_at<16 * q * LPE + (q >= CB / 16 ? 32 * CB - RK : 0), 16 * q * LPE>(d0, s0);
+        });
     };
     const char *KVb = (const char *)a.kv + ((long long)b * a.S * a.kv_ld + c0) * (long long)sizeof(T);
     const long long row_bytes = a.kv_ld * (long long)sizeof(T);
