@@ -22,9 +22,13 @@
 // next target's q row are prefetched in registers. When a head spans several lanes, its dot
 // product is a butterfly sum over them, so those lanes hold the same score.
 //
-// The softmax is online, in log2 units: s = (q . k) * log2(e)/sqrt(d) with q
-// pre-scaled in fp32; m = running max, l = running sum of 2^(s - m), acc =
-// running sum of 2^(s - m) v, updated with paired fp32 FMAs. The (m, l)
+// The softmax is online, in log2 units: s = (q . k) * log2(e)/sqrt(d). With
+// fp16 rows the dot product takes mixed-precision FMAs on the packed halves
+// (fp16 products are exact in fp32, so no widening is needed) and is scaled
+// once; fp32 rows use q pre-scaled in fp32 pairs. m is a lazy reference: it
+// moves to a new score only when that score exceeds it by more than kLazy, so
+// most edges skip the rescale of l and acc; l = running sum of 2^(s - m), acc
+// = running sum of 2^(s - m) v, updated with paired fp32 FMAs. The (m, l)
 // arithmetic uses explicit round-to-nearest operations so that it is identical in the variants with and without values; that makes
 // pmha_edge_weights bit-identical to the weights of pmha_forward.
 #pragma once
@@ -47,9 +51,18 @@ namespace stream {
 #ifndef PMHA_STREAM_LINE_COPY
 #define PMHA_STREAM_LINE_COPY 1
 #endif
+#ifndef PMHA_STREAM_MIXED_FMA
+#define PMHA_STREAM_MIXED_FMA 1
+#endif
+#ifndef PMHA_STREAM_LAZY
+#define PMHA_STREAM_LAZY 8
+#endif
 constexpr int kWarps = PMHA_STREAM_WARPS;  // warps per block
 constexpr int kDepth = PMHA_STREAM_DEPTH;  // edges in flight per slot (even: two per step)
 constexpr int kRing = kDepth + 2;          // stages: a stage is refilled one step after it was read
+// The running reference m moves only when a score exceeds it by more than
+// kLazy (log2 units), so 2^(s - m) <= 2^kLazy; 0 moves it at every new maximum.
+constexpr float kLazy = (float)PMHA_STREAM_LAZY;
 
 struct Args {
     const void *q;
@@ -79,6 +92,16 @@ template <typename T, int CPL, bool WV>
 constexpr int smem_bytes()
 {
     return kWarps * kRing * (WV ? 2 : 1) * 32 * CPL * (int)sizeof(T);
+}
+
+// x += a.lo * b.lo, y += a.hi * b.hi for two fp16 pairs, one rounding each
+// (the fp16 product is exact in fp32, so this equals widening then fma.rn.f32)
+__device__ __forceinline__ void fma_h2(float &x, float &y, uint32_t a, uint32_t b)
+{
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+        : "+f"(x), "+f"(y)
+        : "r"(a), "r"(b));
 }
 
 __device__ __forceinline__ float ex2(float x)
@@ -390,12 +413,20 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     const bool first_started_here = a.row_ptr[t] == e0;
     bool is_first = true;
 
-    f2 q2[NP];
+    // fp16 rows: q stays packed and the scores take mixed-precision FMAs (no
+    // widening), scaled once per score; fp32 rows: q pre-scaled in fp32 pairs
+    constexpr bool kMixed = PMHA_STREAM_MIXED_FMA && sizeof(T) == 2;
+    f2 q2[kMixed ? 1 : NP];
+    Raw<CB> qr;
     const f2 sc2 = pk(a.score_scale, a.score_scale);
     auto set_q = [&](const Raw<CB> &r) {
-        widen2<T, CPL>(r, q2);
+        if constexpr (kMixed) {
+            qr = r;
+        } else {
+            widen2<T, CPL>(r, q2);
 #pragma unroll
-        for (int j = 0; j < NP; ++j) q2[j] = fmul2(q2[j], sc2);
+            for (int j = 0; j < NP; ++j) q2[j] = fmul2(q2[j], sc2);
+        }
     };
     set_q(ldg_raw<CB>(Qb + (long long)t * a.q_ld));
     Raw<CB> qnext = ldg_raw<CB>(Qb + (long long)min(t + 1, a.L - 1) * a.q_ld);
@@ -519,17 +550,29 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
     };
     // the head's score of one staged k row (two independent partial sums)
     auto score = [&](const Raw<CB> &kr) -> float {
-        f2 k2[NP];
-        widen2<T, CPL>(kr, k2);
-        f2 da = 0ull, db = 0ull;
+        float dot;
+        if constexpr (kMixed) {
+            float ax = 0.f, ay = 0.f, bx = 0.f, by = 0.f;
 #pragma unroll
-        for (int i = 0; i < NP; i += 2) {
-            da = ffma2(q2[i], k2[i], da);
-            if (i + 1 < NP) db = ffma2(q2[i + 1], k2[i + 1], db);
+            for (int i = 0; i < NP; i += 2) {
+                fma_h2(ax, ay, qr.w[i], kr.w[i]);
+                if (i + 1 < NP) fma_h2(bx, by, qr.w[i + 1], kr.w[i + 1]);
+            }
+            dot = __fadd_rn(__fadd_rn(ax, bx), __fadd_rn(ay, by));
+        } else {
+            f2 k2[NP];
+            widen2<T, CPL>(kr, k2);
+            f2 da = 0ull, db = 0ull;
+#pragma unroll
+            for (int i = 0; i < NP; i += 2) {
+                da = ffma2(q2[i], k2[i], da);
+                if (i + 1 < NP) db = ffma2(q2[i + 1], k2[i + 1], db);
+            }
+            const float2 fa = upk(da), fb = upk(db);
+            dot = __fadd_rn(__fadd_rn(fa.x, fb.x), __fadd_rn(fa.y, fb.y));
         }
-        const float2 fa = upk(da), fb = upk(db);
-        float dot = __fadd_rn(__fadd_rn(fa.x, fb.x), __fadd_rn(fa.y, fb.y));
         for (int o = 1; o < lph; o <<= 1) dot = __fadd_rn(dot, __shfl_xor_sync(smask, dot, o, LPE));
+        if constexpr (kMixed) dot = __fmul_rn(dot, a.score_scale);
         return dot;
     };
     auto mix = [&](const Raw<CB> &vr, float p) {
@@ -543,6 +586,17 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
         const f2 s2 = pk(scale, scale);
 #pragma unroll
         for (int i = 0; i < NP; ++i) acc2[i] = fmul2(acc2[i], s2);
+    };
+    // Move the reference m to mx where mx > m + kLazy (m = -inf: any finite
+    // mx), rescaling l and acc; the vote keeps the branch uniform over the warp.
+    auto lift = [&](float mx) {
+        const bool move = mx > __fadd_rn(m, kLazy);
+        if (__any_sync(live, move)) {
+            const float scale = !move ? 1.f : (m == -INFINITY ? 0.f : ex2(__fsub_rn(m, mx)));
+            l = __fmul_rn(l, scale);
+            if constexpr (WV) rescale(scale);
+            if (move) m = mx;
+        }
     };
     // one edge through the online softmax (used at target boundaries); its
     // v row is read from stage address vst once the score is known
@@ -558,17 +612,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
             const int e = edge_id(j);
             if (head_leader) scores_b[(long long)e * a.H + head] = dot;
         }
-        const float m_new = fmaxf(m, dot);
-        const float scale = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, m_new));
+        lift(dot);
         // ex2.approx(-inf) is +0, so a dropped edge gives p = 0 once some key
-        // is live; before that m_new is -inf and the offset 0 avoids -inf - -inf
-        const float p = ex2(__fsub_rn(dot, (KPM && m_new == -INFINITY) ? 0.f : m_new));
-        l = __fadd_rn(__fmul_rn(l, scale), p);
-        if constexpr (WV) {
-            rescale(scale);
-            mix(vr, p);
-        }
-        m = m_new;
+        // is live; before that m is -inf and the offset 0 avoids -inf - -inf
+        const float p = ex2(__fsub_rn(dot, (KPM && m == -INFINITY) ? 0.f : m));
+        l = __fadd_rn(l, p);
+        if constexpr (WV) mix(vr, p);
     };
 
     // rs = j mod kRing, stepped by 2 with a wrap (no division in the loop);
@@ -608,18 +657,15 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
                     scores_b[(long long)i1 * a.H + head] = d1;
                 }
             }
-            const float m_new = fmaxf(m, fmaxf(d0, d1));
-            const float scale = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, m_new));
-            const float m_off = (KPM && m_new == -INFINITY) ? 0.f : m_new;
+            lift(fmaxf(d0, d1));
+            const float m_off = (KPM && m == -INFINITY) ? 0.f : m;
             const float p0 = ex2(__fsub_rn(d0, m_off));
             const float p1 = ex2(__fsub_rn(d1, m_off));
-            l = __fadd_rn(__fadd_rn(__fmul_rn(l, scale), p0), p1);
+            l = __fadd_rn(__fadd_rn(l, p0), p1);
             if constexpr (WV) {
-                rescale(scale);
                 mix(vr0, p0);
                 mix(vr1, p1);
             }
-            m = m_new;
         } else {
             one(j, kr0, st0 + 32 * CB);
             if (j + 1 < n) one(j + 1, kr1, st1 + 32 * CB);
