@@ -114,6 +114,32 @@ def test_single_source_targets_exact(dt):
     g.destroy()
 
 
+@pytest.mark.parametrize("L,S,nnz,E,H,B,dt,bip,scale,masked", [
+    (300, 300, 9000, 128, 8, 2, "bf16", False, 2.0, False),
+    (60, 600, 15000, 128, 8, 2, "bf16", True, 2.0, False),   # split targets: pieces merged
+    (300, 300, 9000, 128, 8, 2, "bf16", False, 2.0, True),    # with a key_padding_mask
+    (130, 70, 900, 64, 4, 2, "f32", True, 3.0, False),
+    (64, 64, 256, 32, 4, 3, "f32", False, 3.0, False),
+])
+def test_sharp_scores_move_the_softmax_reference(L, S, nnz, E, H, B, dt, bip, scale, masked):
+    # Tokens scaled up so that scores spread over tens of log2 units within one
+    # target: the running softmax reference has to move many times, by more
+    # than its lazy threshold, and the weights are close to one-hot.
+    rng = np.random.default_rng(L + 7 * E)
+    src, tgt = synth.uniform_graph(rng, L, S, nnz, min_in_degree=1)
+    rnd = synth.bf16_round if dt == "bf16" else (lambda x: x.astype(np.float32))
+    xq = rnd(synth.make_tokens(rng, B, L, E, dt) * np.float32(scale))
+    xkv = rnd(synth.make_tokens(rng, B, S, E, dt) * np.float32(scale)) if bip else xq
+    c = Case(src, tgt, L, S, E, H, B, dt, seed=E, bipartite=bip, xq=xq, xkv=xkv)
+    kpm = synth.padding_mask(rng, B, S) if masked else None
+    g, params, out, w = c.run(DEV, "per_head", kpm=kpm)
+    ref_out, ref_w = c.oracle(kpm=kpm)
+    assert np.nanmax(ref_w) > 0.99  # the spread is real: some weights are one-hot
+    assert_close("output", out.float().cpu().numpy(), ref_out, dt)
+    assert_close_weights("weights", w.cpu().numpy(), ref_w, dt)
+    g.destroy()
+
+
 @pytest.mark.parametrize("wid", [2, 4])
 def test_weights_sum_to_one_per_target_and_head(wid):
     c = _small(wid, 2)
