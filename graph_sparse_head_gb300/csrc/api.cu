@@ -63,16 +63,17 @@ int *device_error_word()
 
 int num_sms()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];  // zero-initialised (static storage)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (!n) {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 148;
+        if (n <= 0) n = 148;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 // ---------------------------------------------------------------- profiling
@@ -111,7 +112,11 @@ StageTimer::StageTimer(const char *stage_, cudaStream_t s) : stage(stage_), stre
     r.stage = stage;
     r.start = take_event();
     r.stop = take_event();
-    if (!r.start || !r.stop) return;
+    if (!r.start || !r.stop) {  // keep whichever one was created
+        if (r.start) g_event_pool.push_back(r.start);
+        if (r.stop) g_event_pool.push_back(r.stop);
+        return;
+    }
     cudaEventRecord(r.start, stream);
     slot = (int)g_records.size();
     g_records.push_back(r);
