@@ -144,7 +144,8 @@ struct EdgeArgs {
     int64_t v_off;
     void *mixed;          // (B, L, E) output of the mix (light targets written directly)
     float *part;          // (B, 2 n_units, 2H + E): per slot m[H], l[H], acc[E] of a crossing target
-    float *ml;            // (B, L, H, 2): running max (log2 units) and sum per target/head
+    float *ml;            // (B, L, H, 2): softmax reference m (log2 units, at most 8 below the largest
+                          // score) and l = sum of 2^(s - m), per target/head
     float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
     int *counters;        // (B, n_merge) pieces written per crossing target; zeroed before the edge kernel
     const uint8_t *kpm;   // (B, S) key_padding_mask, nonzero = key dropped, or null
