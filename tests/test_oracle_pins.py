@@ -227,6 +227,75 @@ def test_forward_rows_matches_full_forward():
         assert np.abs(we - w[b, e_ids]).max() < 1e-15
 
 
+def test_key_bias_does_not_change_the_layer():
+    # q_t . (k_s + c) = q_t . k_s + q_t . c: the key bias adds the same amount
+    # to every score of one (target, head), and a softmax over that target's
+    # edges does not see it. Any bk gives the same weights and output.
+    rng = np.random.default_rng(21)
+    L, S, E, H, B = 25, 33, 16, 4, 2
+    p = _params(rng, E)
+    xq = rng.standard_normal((B, L, E))
+    xkv = rng.standard_normal((B, S, E))
+    src, tgt = synth.uniform_graph(rng, L, S, 110, min_in_degree=0)
+    out, w = oracle.forward(xq, xkv, xkv, p, src, tgt, H)
+    p2 = dict(p)
+    p2["bk"] = p["bk"] + 3.0 * rng.standard_normal(E)
+    out2, w2 = oracle.forward(xq, xkv, xkv, p2, src, tgt, H)
+    assert np.abs(w - w2).max() < 1e-12
+    assert np.abs(out - out2).max() < 1e-12
+    # the query bias is not so: it changes the scores edge by edge
+    p3 = dict(p)
+    p3["bq"] = p["bq"] + 3.0 * rng.standard_normal(E)
+    _, w3 = oracle.forward(xq, xkv, xkv, p3, src, tgt, H)
+    assert np.abs(w - w3).max() > 1e-3
+
+
+def test_value_path_is_affine():
+    # With the keys fixed the weights are fixed and sum to 1 over a target's
+    # edges, so out = Wo (Wv sum_e w_e x_s + bv) + bo is affine in the value
+    # tokens: out(v1 + v2) = out(v1) + out(v2) - (Wo bv + bo) for a target with
+    # a source; a target without one outputs bo whatever the values.
+    rng = np.random.default_rng(23)
+    L, S, E, H, B = 20, 28, 16, 2, 2
+    p = _params(rng, E)
+    xq = rng.standard_normal((B, L, E))
+    xk = rng.standard_normal((B, S, E))
+    v1 = rng.standard_normal((B, S, E))
+    v2 = rng.standard_normal((B, S, E))
+    src, tgt = synth.uniform_graph(rng, L, S, 70, min_in_degree=0)
+    o1, w1 = oracle.forward(xq, xk, v1, p, src, tgt, H)
+    o2, _ = oracle.forward(xq, xk, v2, p, src, tgt, H)
+    o12, w12 = oracle.forward(xq, xk, v1 + v2, p, src, tgt, H)
+    assert np.abs(w1 - w12).max() == 0.0  # the weights do not read the values
+    deg = np.bincount(tgt, minlength=L)
+    assert (deg == 0).any() and (deg > 0).any()
+    const = p["wo"].astype(np.float64) @ p["bv"].astype(np.float64) + p["bo"]
+    live = deg > 0
+    assert np.abs(o12[:, live] - (o1[:, live] + o2[:, live] - const)).max() < 1e-12
+    assert np.abs(o12[:, ~live] - p["bo"]).max() == 0.0
+
+
+def test_node_relabelling_permutes_the_output():
+    # Renaming the targets by a permutation pt and the sources by ps (graph
+    # and tokens alike) permutes the output rows by pt and leaves each edge's
+    # weights unchanged.
+    rng = np.random.default_rng(25)
+    L, S, E, H, B = 18, 26, 16, 4, 2
+    p = _params(rng, E)
+    xq = rng.standard_normal((B, L, E))
+    xkv = rng.standard_normal((B, S, E))
+    src, tgt = synth.uniform_graph(rng, L, S, 80, min_in_degree=0)
+    out, w = oracle.forward(xq, xkv, xkv, p, src, tgt, H)
+    pt, ps = rng.permutation(L), rng.permutation(S)  # node t is called pt[t]
+    xq2 = np.empty_like(xq)
+    xq2[:, pt] = xq
+    xkv2 = np.empty_like(xkv)
+    xkv2[:, ps] = xkv
+    out2, w2 = oracle.forward(xq2, xkv2, xkv2, p, ps[src], pt[tgt], H)
+    assert np.abs(out2[:, pt] - out).max() < 1e-13
+    assert np.abs(w2 - w).max() < 1e-15
+
+
 # ------------------------------------------------------------ index work pins
 
 def test_validation_codes():
