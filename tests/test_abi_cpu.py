@@ -21,7 +21,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pmha_[a-z_]+)\s*\(", text)))
 
@@ -73,6 +74,7 @@ def test_host_checks_before_device_work(lib):
 
 
 def test_status_names_cover_the_header():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     for name in re.findall(r"\b(PMHA_(?:OK|ERR_[A-Z_]+))\s*=", text):
         assert name in _lib.STATUS_NAMES.values(), name

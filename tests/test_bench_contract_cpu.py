@@ -1,0 +1,44 @@
+"""bench.py's command line and the JSON line of its reference arm (the fp64
+oracle on the host cores), checked on the CPU: the keys the line must carry,
+their types, and that the arm reports what it ran."""
+import contextlib
+import io
+import json
+
+import pytest
+
+import bench
+
+
+def _run(argv):
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(argv)
+    lines = [l for l in buf.getvalue().splitlines() if l.startswith("{")]
+    assert rc == 0 and len(lines) == 1
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line(monkeypatch):
+    monkeypatch.setattr(bench, "WORKLOAD_ID", bench.WORKLOAD_ID)  # main() sets it; restored afterwards
+    d = _run(["--impl", "reference", "--steps", "2", "--warmup", "3", "--workload", "1"])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == "tiny_f32_n64_E32_H4"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_warmup_below_three_is_refused(monkeypatch):
+    monkeypatch.setattr(bench, "WORKLOAD_ID", bench.WORKLOAD_ID)
+    with pytest.raises(SystemExit):
+        with contextlib.redirect_stderr(io.StringIO()):
+            bench.main(["--impl", "reference", "--steps", "1", "--warmup", "2"])
