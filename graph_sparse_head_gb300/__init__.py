@@ -195,10 +195,36 @@ def pmha_forward_host_workspace_size(graph: Graph, params: Params, batch: int, w
 
 def _workspace(nbytes: int, device, workspace):
     if workspace is not None:
+        if not isinstance(workspace, torch.Tensor) or workspace.device != device or not workspace.is_contiguous():
+            raise ValueError(f"workspace must be a contiguous tensor on {device}")
         if workspace.numel() * workspace.element_size() < nbytes:
             raise ValueError(f"workspace holds fewer than the {nbytes} bytes needed")
         return workspace
     return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def _check_dest(name, t, shape, dtype, device):
+    """A result tensor the caller supplies: exactly `shape` and `dtype`,
+    contiguous, on `device` (None: a host tensor). The kernels write it whole,
+    so anything smaller or strided is refused before a launch."""
+    if not isinstance(t, torch.Tensor) or tuple(t.shape) != tuple(shape) or t.dtype != dtype \
+            or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {tuple(shape)} tensor of {dtype}")
+    if device is None:
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor here")
+    elif t.device != device:
+        raise ValueError(f"{name} must live on {device}")
+
+
+def _check_placement(graph, params, device):
+    """The graph and every parameter tensor on the device of the call."""
+    if graph.device != device:
+        raise ValueError(f"the graph was built on {graph.device}, the call runs on {device}")
+    for n in ("wq", "wk", "wv", "wo", "bq", "bk", "bv", "bo"):
+        t = getattr(params, n)
+        if t is not None and t.device != device:
+            raise ValueError(f"parameter {n} lives on {t.device}, the call runs on {device}")
 
 
 def _check_tokens(name, x, batch, seq, E, dtype, device):
@@ -239,13 +265,19 @@ def pmha_forward(graph: Graph, params: Params, query: torch.Tensor, key: torch.T
     _check_tokens("key", key, B, graph.key_features, E, params.dtype, dev)
     _check_tokens("value", value, B, graph.key_features, E, params.dtype, dev)
     mp = _check_mask(key_padding_mask, B, graph.key_features, True, dev)
+    _check_placement(graph, params, dev)
     p = params.as_struct()
     lib = _lib.load()
     wm = WMODES[wmode]
     if out is None:
         out = torch.empty_like(query)
-    if wm != PMHA_WEIGHTS_NONE and weights is None:
-        weights = torch.empty(_weights_shape(graph, B, H, wmode), dtype=torch.float32, device=dev)
+    else:
+        _check_dest("out", out, (B, graph.query_features, E), params.dtype, dev)
+    if wm != PMHA_WEIGHTS_NONE:
+        if weights is None:
+            weights = torch.empty(_weights_shape(graph, B, H, wmode), dtype=torch.float32, device=dev)
+        else:
+            _check_dest("weights", weights, _weights_shape(graph, B, H, wmode), torch.float32, dev)
     need = lib.pmha_forward_workspace_size(graph.handle, ctypes.byref(p), B, wm)
     if need == 0:
         _lib.check(_lib.PMHA_OK + 1, "pmha_forward_workspace_size")
@@ -267,15 +299,20 @@ def pmha_forward_host(graph: Graph, params: Params, query: torch.Tensor, key: to
     on the stream. Synchronize the stream before reading `out`."""
     B = int(query.shape[0])
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    E = params.embed_dim
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    E, H = params.embed_dim, int(params.num_heads)
     for n, x, seq in (("query", query, graph.query_features), ("key", key, graph.key_features),
                       ("value", value, graph.key_features), ("out", out, graph.query_features)):
         if x.is_cuda or tuple(x.shape) != (B, seq, E) or x.dtype != params.dtype or not x.is_contiguous():
             raise ValueError(f"{n} must be a contiguous host tensor ({B}, {seq}, {E}) of {params.dtype}")
     mp = _check_mask(key_padding_mask, B, graph.key_features, False)
+    _check_placement(graph, params, dev)
+    wm = WMODES[wmode]
+    if wm != PMHA_WEIGHTS_NONE and weights is not None:
+        _check_dest("weights", weights, _weights_shape(graph, B, H, wmode), torch.float32, None)
     p = params.as_struct()
     lib = _lib.load()
-    wm = WMODES[wmode]
     need = lib.pmha_forward_host_workspace_size(graph.handle, ctypes.byref(p), B, wm)
     ws = _workspace(need, dev, workspace)
     with torch.cuda.device(dev):
@@ -299,11 +336,14 @@ def pmha_edge_weights(graph: Graph, params: Params, query: torch.Tensor, key: to
     if wmode not in ("avg", "per_head"):
         raise ValueError("wmode must be 'avg' or 'per_head'")
     mp = _check_mask(key_padding_mask, B, graph.key_features, True, dev)
+    _check_placement(graph, params, dev)
     p = params.as_struct()
     lib = _lib.load()
     wm = WMODES[wmode]
     if weights is None:
         weights = torch.empty(_weights_shape(graph, B, H, wmode), dtype=torch.float32, device=dev)
+    else:
+        _check_dest("weights", weights, _weights_shape(graph, B, H, wmode), torch.float32, dev)
     need = lib.pmha_edge_weights_workspace_size(graph.handle, ctypes.byref(p), B, wm)
     ws = _workspace(need, dev, workspace)
     with torch.cuda.device(dev):
@@ -334,6 +374,7 @@ def pmha_backward(graph: Graph, params: Params, query: torch.Tensor, key: torch.
     _check_tokens("value", value, B, graph.key_features, E, params.dtype, dev)
     _check_tokens("dout", dout, B, graph.query_features, E, params.dtype, dev)
     mp = _check_mask(key_padding_mask, B, graph.key_features, True, dev)
+    _check_placement(graph, params, dev)
     p = params.as_struct()
     lib = _lib.load()
     out = {}
