@@ -226,6 +226,29 @@ def test_argument_errors():
     g.destroy()
 
 
+def test_binding_refuses_mismatched_results_before_launch():
+    import graph_sparse_head_gb300 as pmha
+    c = _small(1, 2)
+    g, params, out, w = c.run(DEV, "per_head")
+    xq, _ = c.device_inputs(DEV)
+    n0 = pmha.pmha_launch_count()
+    bad_calls = [
+        dict(out=torch.empty(2, c.L, c.E - 1, dtype=out.dtype, device=DEV)),          # short rows
+        dict(out=torch.empty(2, c.L, c.E, dtype=torch.float64, device=DEV)),          # dtype
+        dict(out=torch.empty(2, c.E, c.L, dtype=out.dtype, device=DEV).transpose(1, 2)),  # strided
+        dict(weights=torch.empty(2, c.src.size, dtype=torch.float32, device=DEV)),   # avg shape for per_head
+        dict(workspace=torch.empty(1 << 20, dtype=torch.uint8)),                      # host workspace
+    ]
+    for kw in bad_calls:
+        with pytest.raises(ValueError):
+            pmha.pmha_forward(g, params, xq, xq, xq, "per_head", **kw)
+    with pytest.raises(ValueError):
+        pmha.pmha_edge_weights(g, params, xq, xq, "avg", weights=torch.empty(2, c.src.size + 1, device=DEV))
+    assert pmha.pmha_launch_count() == n0  # nothing was launched
+    pmha.pmha_device_status()
+    g.destroy()
+
+
 def test_launch_counter_and_profile():
     import graph_sparse_head_gb300 as pmha
     c = _small(2, 1)
