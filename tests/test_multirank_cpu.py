@@ -33,7 +33,7 @@ def _worker(rank, world, port, out):
 
 def test_two_ranks_own_batches_and_max_time():
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of this (threaded) process
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     (w0, r0, s0, m0), (w1, r1, s1, m1) = out[0], out[1]
     assert (w0, r0, w1, r1) == (2, 0, 2, 1)
