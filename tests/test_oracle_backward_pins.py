@@ -187,6 +187,31 @@ def test_bias_false_has_no_bias_gradients():
     _assert_grads(g, ref, 1e-11, names=("dquery", "dwq", "dwk", "dwv", "dwo"))
 
 
+@pytest.mark.parametrize("masked", [False, True])
+def test_output_and_value_bias_gradients_in_closed_form(masked):
+    # out = mixed Wo^T + bo, so dbo = sum of dout over all (sample, target) and
+    # dmixed = dout Wo. A target with a live key mixes sum_e w_e v_s with
+    # weights summing to 1, so bv reaches it with coefficient 1: dbv = sum of
+    # dmixed over the (sample, target) pairs that have a live key, and a target
+    # without one contributes nothing.
+    rng = np.random.default_rng(31)
+    E, H, L, S, B = 16, 4, 24, 30, 3
+    p = _params(rng, E)
+    src, tgt = synth.uniform_graph(rng, L, S, 90, min_in_degree=0)
+    xq = rng.standard_normal((B, L, E))
+    xkv = rng.standard_normal((B, S, E))
+    kpm = (rng.random((B, S)) < 0.4) if masked else None
+    dout = rng.standard_normal((B, L, E))
+    g = oracle.backward(xq, xkv, xkv, p, src, tgt, H, dout, key_padding_mask=kpm)
+    live = np.zeros((B, L), bool)
+    for e in range(src.size):
+        live[:, tgt[e]] |= True if kpm is None else ~kpm[:, src[e]]
+    assert live.any() and (~live).any()
+    dmixed = dout @ p["wo"].astype(np.float64)
+    assert np.abs(g["dbo"] - dout.sum(axis=(0, 1))).max() < 1e-12
+    assert np.abs(g["dbv"] - dmixed[live].sum(axis=0)).max() < 1e-11
+
+
 def test_linear_backward_matches_numpy():
     rng = np.random.default_rng(1)
     x, w, dy = rng.standard_normal((7, 5)), rng.standard_normal((3, 5)), rng.standard_normal((7, 3))
