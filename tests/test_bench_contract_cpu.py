@@ -42,3 +42,21 @@ def test_warmup_below_three_is_refused(monkeypatch):
     with pytest.raises(SystemExit):
         with contextlib.redirect_stderr(io.StringIO()):
             bench.main(["--impl", "reference", "--steps", "1", "--warmup", "2"])
+
+
+def test_traffic_is_tied_to_the_kernel_source_and_workload(monkeypatch):
+    # The committed DRAM bytes belong to the kernel source they were captured
+    # on: any change to that source, or another workload, gives null.
+    got = bench.ncu_traffic("edge_attn", "skewed_n20000_E128_H8")
+    assert got is not None and got > 0
+    assert bench.ncu_traffic("edge_attn", "grn_n2000_E128_H8") is None
+    monkeypatch.setattr(bench, "source_digest", lambda paths: "0" * 16)
+    assert bench.ncu_traffic("edge_attn", "skewed_n20000_E128_H8") is None
+
+
+def test_algorithmic_bytes_of_the_edge_kernel():
+    # q, k|v and the mixed rows once, plus col and row_ptr (int32), at n=20k
+    w = bench.synth.workload(3)
+    got = bench.algorithmic_bytes("edge_attn", w, 16, 400_000)
+    E, n, B = 128, 20_000, 16
+    assert got == B * n * E * 2 + B * n * 2 * E * 2 + B * n * E * 2 + 400_000 * 4 + (n + 1) * 4
