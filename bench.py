@@ -105,7 +105,8 @@ def source_digest(paths) -> str:
 
 
 KERNEL_SOURCES = {
-    "edge_attn": ["graph_sparse_head_gb300/csrc/edge_stream.cuh", "graph_sparse_head_gb300/csrc/edge_attn_f16.cu"],
+    "edge_attn": ["graph_sparse_head_gb300/csrc/edge_ring.cuh", "graph_sparse_head_gb300/csrc/edge_attn_ring.cu",
+                  "graph_sparse_head_gb300/csrc/edge_stream.cuh"],
     "proj_qkv": ["graph_sparse_head_gb300/csrc/gemm_tc.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
     "out_proj": ["graph_sparse_head_gb300/csrc/gemm_tc.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
     "dense_attn": ["graph_sparse_head_gb300/csrc/dense_attn.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],

@@ -239,7 +239,7 @@ Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode w
     l.vt = o;
     if (with_values && dense_supported(g, E, H, inter_type(p->dtype))) o += align256(dense_vt_bytes(g, B, E));
     l.counters = o;  // the light part of a split graph has its own merge list
-    o += align256((size_t)(B * std::max(g->n_merge, g->light ? g->light->n_merge : (int64_t)0)) * 4);
+    o += align256((size_t)(kCounterHead + B * std::max(g->n_merge, g->light ? g->light->n_merge : (int64_t)0)) * 4);
     l.kpm_bits = o;  // a key_padding_mask per CSR position, when one is given
     o += align256((size_t)(B * ((g->nnz + 31) / 32)) * 4);
     l.heavy = o;  // the heavy-target path's qt images and per-head mixes

@@ -371,6 +371,38 @@ __global__ void k_unit_first(const int32_t *__restrict__ row_ptr, int L, const S
     unit_first_t[u] = lo;
 }
 
+// Work estimate of every unit (its positions plus kSwitchCost per target it
+// touches: a target switch costs the edge kernel about that many edges), as
+// a 16-bit key that sorts the slowest unit first; padding units past the
+// real count get the largest key. vals receive the unit indices.
+#ifndef PMHA_SWITCH_COST
+#define PMHA_SWITCH_COST 4
+#endif
+constexpr int kSwitchCost = PMHA_SWITCH_COST;
+__global__ void k_unit_cost(const int32_t *__restrict__ row_ptr, int L, const Summary *__restrict__ sum,
+                            const int32_t *__restrict__ unit_first_t, int max_units, uint32_t *__restrict__ key,
+                            int *__restrict__ val)
+{
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= max_units) return;
+    const int nnz = sum->nnz_total;
+    const int n_units = (nnz + kUnitEdges - 1) / kUnitEdges;
+    val[u] = u;
+    if (u >= n_units) {
+        key[u] = 0xffffu;
+        return;
+    }
+    const int e0 = u * kUnitEdges, e1 = min(e0 + kUnitEdges, nnz);
+    int lo = 0, hi = L;  // target of position e1 - 1: row_ptr[lo] <= e1 - 1 < row_ptr[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (row_ptr[mid] <= e1 - 1) lo = mid;
+        else hi = mid;
+    }
+    const int cost = (e1 - e0) + kSwitchCost * (lo - unit_first_t[u] + 1);
+    key[u] = 0xfffeu - (uint32_t)min(cost, 0xfffe);
+}
+
 __global__ void k_merge_flags(const int32_t *__restrict__ row_ptr, int L, int *__restrict__ flag,
                               Summary *__restrict__ sum)
 {
@@ -465,7 +497,8 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     size_t off_perm = off_col + align((size_t)cap * 4);
     size_t off_tge = off_perm + align((size_t)cap * 4);
     size_t off_units = off_tge + align((size_t)cap * 4);
-    size_t off_merge = off_units + align((size_t)max_units * 4);
+    size_t off_order = off_units + align((size_t)max_units * 4);
+    size_t off_merge = off_order + align((size_t)max_units * 4);
     size_t off_mpos = off_merge + align((size_t)L * 4);
     size_t off_srp = off_mpos + align((size_t)L * 4);
     size_t off_tbs = off_srp + align((size_t)(S + 1) * 4);
@@ -514,6 +547,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     g->perm = (int32_t *)(gm + off_perm);
     g->tgt_of_edge = (int32_t *)(gm + off_tge);
     g->unit_first_t = (int32_t *)(gm + off_units);
+    g->unit_order = (int32_t *)(gm + off_order);
     g->merge_t = (int32_t *)(gm + off_merge);
     g->merge_pos = (int32_t *)(gm + off_mpos);
     g->src_row_ptr = (int32_t *)(gm + off_srp);
@@ -559,6 +593,19 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         k_unit_first<<<blocks_for(max_units, TB), TB, 0, stream>>>(g->row_ptr, (int)L, dsum, g->unit_first_t);
         k_merge_flags<<<blocks_for(L, TB), TB, 0, stream>>>(g->row_ptr, (int)L, c1, dsum);
         count_launch(4);
+        {
+            // the units by decreasing estimated work, for the edge kernel's queue
+            uint32_t *ck_a = (uint32_t *)keys_a, *ck_b = (uint32_t *)keys_b;
+            k_unit_cost<<<blocks_for(max_units, TB), TB, 0, stream>>>(g->row_ptr, (int)L, dsum, g->unit_first_t,
+                                                                      max_units, ck_a, vals_a);
+            count_launch();
+            uint32_t *ck_s;
+            int *cv_s;
+            radix_sort<uint32_t>(ck_a, vals_a, ck_b, vals_b, max_units, 16, hist, scan_tmp, stream, &ck_s, &cv_s);
+            if ((ce = cudaMemcpyAsync(g->unit_order, cv_s, (size_t)max_units * 4, cudaMemcpyDeviceToDevice,
+                                      stream)) != cudaSuccess)
+                break;
+        }
         exclusive_scan(c1, c2, (int)L, &dsum->n_merge, scan_tmp, stream);
         k_merge_write<<<blocks_for(L, TB), TB, 0, stream>>>(c1, c2, (int)L, g->merge_t);
         k_merge_pos<<<blocks_for(L, TB), TB, 0, stream>>>(c1, c2, (int)L, g->merge_pos);

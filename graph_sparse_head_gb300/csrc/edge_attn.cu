@@ -5,7 +5,11 @@
 // the per-edge weights in the given edge order.
 #include <math.h>
 
-#include "edge_stream.cuh"
+#include "edge_ring.cuh"
+
+#ifndef PMHA_EDGE_RING
+#define PMHA_EDGE_RING 1
+#endif
 
 namespace pmha {
 namespace {
@@ -139,10 +143,12 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.col = g->col;
     k.perm = g->perm;
     k.unit_first_t = g->unit_first_t;
+    k.unit_order = g->unit_order;
+    k.task_counter = (unsigned *)a.counters;  // the first word of the counter region
     k.kpm = a.kpm;
     k.kpm_bits = a.kpm_bits;
     k.n_kw = (g->nnz + 31) / 32;
-    k.counters = a.counters;
+    k.counters = a.counters + kCounterHead;
     k.merge_pos = g->merge_pos;
     k.n_merge = g->n_merge;
     k.n_units = g->n_units;
@@ -167,11 +173,16 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
                                                                a.kpm_bits);
         count_launch();
     }
-    // arrival counts of the pieces of crossing targets (the edge kernel merges them)
-    if (g->n_merge > 0) PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(a.B * g->n_merge) * 4, s));
+    // the ring kernel's task counter and the arrival counts of the pieces of
+    // crossing targets (the edge kernel merges them)
+    PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(kCounterHead + a.B * g->n_merge) * 4, s));
     StageTimer timer(a.with_values ? "edge_attn" : "edge_scores", s);
-    const pmha_status st = dt == TcType::F16 ? stream::launch_f16(cpl, lpe, a.with_values, k, slots, s)
-                                             : stream::launch_f32(cpl, lpe, a.with_values, k, slots, s);
+    // fp16 rows of 16 channels a lane and 8 to 32 lanes: the ring kernel
+    // (edge_ring.cuh); other shapes and float32 layers: the streaming kernel
+    const bool ring = PMHA_EDGE_RING && dt == TcType::F16 && cpl == 16 && lpe >= 8;
+    const pmha_status st = ring ? stream::launch_ring_f16(lpe, a.with_values, k, s)
+                           : dt == TcType::F16 ? stream::launch_f16(cpl, lpe, a.with_values, k, slots, s)
+                                               : stream::launch_f32(cpl, lpe, a.with_values, k, slots, s);
     if (st != PMHA_OK) return st;
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());

@@ -77,6 +77,8 @@ struct Args {
     const int32_t *col;
     const int32_t *perm;
     const int32_t *unit_first_t;
+    const int32_t *unit_order;  // units by decreasing estimated work (the ring kernel's queue order)
+    unsigned *task_counter;     // next task of the ring kernel's queue (zero at launch)
     const uint8_t *kpm;  // (B, S) key_padding_mask, nonzero = key dropped; or null
     const uint32_t *kpm_bits;  // (B, n_kw) the mask per CSR position, 32 positions a word
     long long n_kw;

@@ -42,6 +42,7 @@ struct pmha_graph {
     int32_t *perm = nullptr;          // nnz, given-order edge id per CSR position
     int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
     int32_t *unit_first_t = nullptr;  // n_units, target of each unit's first position
+    int32_t *unit_order = nullptr;    // n_units, the units by decreasing estimated work (ties by index)
     int32_t *merge_t = nullptr;       // n_merge, targets to merge (crossing a unit boundary, or without edges)
     int32_t *merge_pos = nullptr;     // L, index of each target in merge_t, or -1
     int64_t n_empty = 0;              // targets without edges
@@ -147,13 +148,15 @@ struct EdgeArgs {
     float *ml;            // (B, L, H, 2): softmax reference m (log2 units, at most 8 below the largest
                           // score) and l = sum of 2^(s - m), per target/head
     float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
-    int *counters;        // (B, n_merge) pieces written per crossing target; zeroed before the edge kernel
+    int *counters;        // kCounterHead words (a task counter), then (B, n_merge) pieces written per
+                          // crossing target; zeroed by edge_attention before the edge kernel
     const uint8_t *kpm;   // (B, S) key_padding_mask, nonzero = key dropped, or null
     uint32_t *kpm_bits;   // (B, ceil(nnz / 32)) scratch: bit p of word w = key of CSR position 32 w + p dropped
     int64_t B, L, S, E, H, nnz;
     float score_scale;    // log2(e) / sqrt(d)
     bool with_values;     // false: scores and (m, l) only
 };
+constexpr int kCounterHead = 64;  // words before the merge counters (256 bytes)
 // `t` is the intermediate type (F16 or F32) of q, k, v and mixed.
 bool edge_supported(int64_t E, int64_t H, TcType t);
 pmha_status edge_attention(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);

@@ -44,12 +44,17 @@ def test_warmup_below_three_is_refused(monkeypatch):
             bench.main(["--impl", "reference", "--steps", "1", "--warmup", "2"])
 
 
-def test_traffic_is_tied_to_the_kernel_source_and_workload(monkeypatch):
-    # The committed DRAM bytes belong to the kernel source they were captured
-    # on: any change to that source, or another workload, gives null.
-    got = bench.ncu_traffic("edge_attn", "skewed_n20000_E128_H8")
-    assert got is not None and got > 0
+def test_traffic_is_tied_to_the_kernel_source_and_workload(monkeypatch, tmp_path):
+    # DRAM bytes from an ncu summary count only for the kernel source they were
+    # captured on and for their workload: a stale or foreign entry gives null.
+    digest = bench.source_digest(bench.KERNEL_SOURCES["edge_attn"])
+    entry = {"dram_bytes_per_launch": 123456789.0, "source_digest": digest,
+             "workload": "skewed_n20000_E128_H8, B=16"}
+    (tmp_path / "ncu_traffic.json").write_text(json.dumps({"edge_attn": entry}))
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    assert bench.ncu_traffic("edge_attn", "skewed_n20000_E128_H8") == 123456789.0
     assert bench.ncu_traffic("edge_attn", "grn_n2000_E128_H8") is None
+    assert bench.ncu_traffic("out_proj", "skewed_n20000_E128_H8") is None
     monkeypatch.setattr(bench, "source_digest", lambda paths: "0" * 16)
     assert bench.ncu_traffic("edge_attn", "skewed_n20000_E128_H8") is None
 
