@@ -57,6 +57,10 @@ namespace stream {
 #ifndef PMHA_RING_EARLY
 #define PMHA_RING_EARLY 1
 #endif
+#ifndef PMHA_RING_ACQREL
+#define PMHA_RING_ACQREL 1
+#endif
+
 constexpr int kRWarps = PMHA_RING_WARPS;  // warps per block
 constexpr int kRDepth = PMHA_RING_DEPTH;  // edges in flight ahead of the pair being read (even)
 // Early release: a step reads its k and v rows into registers first and
@@ -89,6 +93,18 @@ __device__ __forceinline__ Raw<32> lds_pair(uint32_t a0, uint32_t a1)
                  : "=r"(r.w[4]), "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
                  : "r"(a1));
     return r;
+}
+
+// Orders this thread's prior global writes before its later ones and its
+// later reads after earlier acquires (release and acquire at GPU scope; the
+// pieces of a crossing target are published and read across CTAs with it).
+__device__ __forceinline__ void fence_gpu()
+{
+#if PMHA_RING_ACQREL
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+#else
+    __threadfence();
+#endif
 }
 
 // x += p * v.lo, y += p * v.hi: fp16 operands, fp32 accumulate, one rounding
@@ -367,7 +383,7 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
             // The slot that writes a target's last piece merges all its
             // pieces: each writer publishes its piece (fence) and counts it;
             // the one that completes the count reads every piece in piece order.
-            __threadfence();
+            fence_gpu();
             __syncwarp(kAll);
             const int beg = a.row_ptr[t], end = a.row_ptr[t + 1];
             const int u0 = beg / kUnitEdges, n_pieces = (end - 1) / kUnitEdges - u0 + 1;
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
             if (grp == 0 && own) prev = atomicAdd(a.counters + (long long)b * a.n_merge + a.merge_pos[t], 1);
             prev = __shfl_sync(kAll, prev, slot * LPE);
             if (own && prev == n_pieces - 1) {
-                __threadfence();
+                fence_gpu();
                 merge_pieces(beg, u0, n_pieces);
             }
         }

@@ -24,7 +24,7 @@ namespace pmha {
 // --------------------------------------------------------------------------
 
 #ifndef PMHA_UNIT_EDGES
-#define PMHA_UNIT_EDGES 160
+#define PMHA_UNIT_EDGES 176
 #endif
 constexpr int kUnitEdges = PMHA_UNIT_EDGES;
 

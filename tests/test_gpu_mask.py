@@ -52,7 +52,7 @@ def test_masked_forward_matches_oracle(wid, B, kind):
 
 
 def test_mask_empties_a_whole_unit_of_a_split_target():
-    # complete graph, 1024 sources per target (several units of 160 edges each):
+    # complete graph, 1024 sources per target (several units of edges each):
     # sample 0 drops keys 0..599, so whole units of every target are dropped
     # and the merge combines empty pieces with live ones; sample 1 drops all
     # keys but one, sample 2 drops every key
