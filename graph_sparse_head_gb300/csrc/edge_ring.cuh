@@ -170,14 +170,14 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
 
     // ---- global rows (byte pointers at this lane's first chunk)
     const char *KV0 = (const char *)a.kv + (long long)b * a.S * a.kv_ld * 2 + 16 * grp;
-    const long long kv_row = a.kv_ld * 2;
+    const unsigned kv_row = (unsigned)(a.kv_ld * 2);  // row pitches in bytes (< 2^32)
     const char *Q0 = (const char *)a.q + (long long)b * a.L * a.q_ld * 2 + 16 * grp;
-    const long long q_row = a.q_ld * 2;
+    const unsigned q_row = (unsigned)(a.q_ld * 2);
     float *scores_b = WS ? a.scores + (long long)b * a.nnz * a.H : nullptr;
     const int32_t *colu = a.col + e0;
 
     auto copy_kv = [&](uint32_t st, int s) {
-        const char *src = KV0 + (long long)s * kv_row;
+        const char *src = KV0 + (unsigned long long)(unsigned)s * kv_row;  // one 32 x 32 -> 64-bit multiply-add
         static_for<0, 2 * NR>([&](auto qc) {
             constexpr int q = decltype(qc)::value;
             constexpr int doff = (q / 2) * PART + (q % 2) * (PART / 2);
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
         });
     };
     auto copy_q = [&](uint32_t st, int t) {
-        const char *src = Q0 + (long long)t * q_row;
+        const char *src = Q0 + (unsigned long long)(unsigned)t * q_row;
         cp_async16_at<0, 0>(fill_q + st, src);
         cp_async16_at<PART / 2, 16 * LPE>(fill_q + st, src);
     };
@@ -312,9 +312,13 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
         *reinterpret_cast<uint4 *>(row + 16 * (1 - sw)) = make_uint4(w[4], w[5], w[6], w[7]);
     };
 
-    // Combine the partial states (m, l, acc) of target t's pieces, unit order:
-    // M = max m_i, L = sum l_i 2^(m_i - M), acc = sum acc_i 2^(m_i - M); an
-    // empty piece (every key dropped) has m = -inf, l = 0 and adds nothing.
+    // Combine the partial states (m, l, acc) of target t's pieces in unit
+    // order, in one pass with a running maximum M: a piece with m_i > M first
+    // rescales L and acc by 2^(M - m_i); then L += l_i 2^(m_i - M) and acc +=
+    // acc_i 2^(m_i - M). An empty piece (every key dropped: m = -inf, l = 0)
+    // adds nothing. Pieces are pulled into L1 eight ahead of their use, so the
+    // pass is not a chain of L2 round trips (a target with thousands of edges
+    // has dozens of pieces).
     auto merge_pieces = [&](int beg, int u0, int n_pieces) {
         const long long stride = 2 * a.H + a.E;
         const float *base = a.part + (long long)b * 2 * a.n_units * stride;
@@ -322,19 +326,34 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
             const int sid = 2 * (u0 + i) + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
             return base + (long long)sid * stride;
         };
-        float Mh = -INFINITY;
-#pragma unroll 4
-        for (int i = 0; i < n_pieces; ++i) Mh = fmaxf(Mh, piece(i)[head]);
-        const float mo = Mh == -INFINITY ? 0.f : Mh;
-        float Lh = 0.f;
+        auto pull = [&](int i) {
+            if (i < n_pieces) {
+                const float *pp = piece(i);
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(pp + head));
+                if constexpr (WV) asm volatile("prefetch.global.L1 [%0];" ::"l"(pp + 2 * a.H + c0));
+            }
+        };
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pull(i);
+        float Mh = -INFINITY, Lh = 0.f;
         float macc[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) macc[j] = 0.f;
-#pragma unroll 2
         for (int i = 0; i < n_pieces; ++i) {
+            pull(i + 8);
             const float *pp = piece(i);
-            const float w = ex2(__fsub_rn(pp[head], mo));
-            Lh = __fadd_rn(Lh, __fmul_rn(pp[a.H + head], w));
+            const float mi = pp[head], li = pp[a.H + head];
+            if (mi > Mh) {
+                const float sc = ex2(__fsub_rn(Mh, mi));  // 0 while M is -inf
+                Lh = __fmul_rn(Lh, sc);
+                if constexpr (WV) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) macc[j] = __fmul_rn(macc[j], sc);
+                }
+                Mh = mi;
+            }
+            const float w = mi == -INFINITY ? 0.f : ex2(__fsub_rn(mi, Mh));
+            Lh = __fmaf_rn(li, w, Lh);
             if constexpr (WV) {
                 // a piece row is 2H + E floats: 8-byte aligned for any H
 #pragma unroll
