@@ -8,6 +8,13 @@ steps by writing a 512 MiB buffer (untimed). Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The headline steps run with the library's stage timer off; stage times and
+the dominant kernel's roofline come from a separate pass of the same steps.
+`per_workload` adds every other workload of the pages' shapes (tiny fp32,
+gene-regulatory n=2,000, bipartite 500 -> 20,000 with averaged weights,
+complete n=1,024): layer time, stages, roofline and the oracle on a bounded
+sample (rank 0 only).
+
 Under torchrun each rank runs its own batch (weak scaling, no collective on
 the data path; a barrier and a max over ranks of the step time only).
 --impl reference times the fp64 CPU oracle on the host cores instead (rank 0
@@ -52,17 +59,25 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def algorithmic_bytes(stage: str, w: synth.Workload, B: int, nnz: int) -> float | None:
+def algorithmic_bytes(stage: str, w: synth.Workload, B: int, nnz: int, wmode: str = "none") -> float | None:
     """Compulsory HBM bytes of one launch: every tensor the kernel must touch,
-    read or written once (gathered re-reads served by L2 are not counted)."""
-    E, L, S = w.embed_dim, w.query_features, w.key_features
+    read or written once (gathered re-reads served by L2 are not counted).
+    With weights requested the edge kernel also writes every raw score
+    (B, nnz, H) fp32 and the (m, l) pairs, and a weights pass turns them into
+    weights."""
+    E, L, S, H = w.embed_dim, w.query_features, w.key_features, w.num_heads
     bf = 2
     if stage == "edge_attn":
+        scores = (B * nnz * H * 4 + B * L * H * 8) if wmode != "none" else 0
         return (B * L * E * bf          # q rows
                 + B * S * 2 * E * bf    # k and v rows, each at least once
                 + B * L * E * bf        # mixed, written
                 + nnz * 4               # source index per CSR position
-                + (L + 1) * 4)          # row pointers
+                + (L + 1) * 4           # row pointers
+                + scores)
+    if stage == "weights":
+        out = B * nnz * (H if wmode == "per_head" else 1) * 4
+        return B * nnz * H * 4 + B * L * H * 8 + nnz * 4 + out
     if stage == "dense_attn":
         return B * L * E * bf + B * S * 2 * E * bf + B * L * E * bf  # q, k, v^T once; mixed
     if stage == "transpose_v":
@@ -170,18 +185,45 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, first: int):
-        rows = [l.split(",") for _, l in self.lines[first:]]
+    def query_once(self):
+        """One read-only sample, taken now (for a timed region too short for
+        the sampling interval)."""
+        try:
+            r = subprocess.run(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                "-i", str(self.gpu)], capture_output=True, text=True, timeout=10)
+            if r.returncode == 0 and r.stdout.strip():
+                self.lines.append((time.time(), r.stdout.strip().splitlines()[0]))
+                return True
+        except (OSError, ValueError, subprocess.TimeoutExpired):
+            pass
+        return False
+
+    def summary(self, first: int, last: int | None = None):
+        """Samples [first, last): the timed region. A region that caught none
+        falls back to every sample of the run so far, then to one sample taken
+        now, and says which."""
+        window = "timed region"
+        rows = [l.split(",") for _, l in self.lines[first:last]]
         rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+            window = "whole run (the timed region was shorter than the sampling interval)"
+            rows = [[c.strip() for c in l.split(",")] for _, l in self.lines]
+            rows = [r for r in rows if len(r) >= 9]
+        if not rows and self.query_once():
+            window = "one sample right after the timed region"
+            rows = [[c.strip() for c in self.lines[-1][1].split(",")]]
+            rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "window": "none (nvidia-smi gave no sample)"}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None,
+                "window": window}
 
 
 def dist_env():
@@ -197,13 +239,14 @@ def shard_seed(rank: int) -> int:
     return rank
 
 
-def make_rank_inputs(rank: int, batch: int):
+def make_rank_inputs(rank: int, batch: int, wid: int | None = None):
     """(query tokens, key/value tokens, params); key/value is the query for
     attention within one graph."""
-    w = synth.workload(WORKLOAD_ID)
-    xq, xkv, params = synth.make_inputs(WORKLOAD_ID, batch)
+    wid = WORKLOAD_ID if wid is None else wid
+    w = synth.workload(wid)
+    xq, xkv, params = synth.make_inputs(wid, batch)
     if shard_seed(rank):
-        rng = np.random.default_rng([1000 + WORKLOAD_ID, shard_seed(rank)])
+        rng = np.random.default_rng([1000 + wid, shard_seed(rank)])
         xq = synth.make_tokens(rng, batch, w.query_features, w.embed_dim, w.dtype)
         if xkv is not None:
             xkv = synth.make_tokens(rng, batch, w.key_features, w.embed_dim, w.dtype)
@@ -278,6 +321,138 @@ def bench_reference(args):
     return 0
 
 
+def _timed(torch, stream, flush, steps, fn):
+    """CUDA-event time (ms) of each of `steps` calls of fn on `stream`, with L2
+    flushed (untimed) before each."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (e0, e1) in enumerate(ev):
+        flush.fill_(i & 0xFF)  # evict L2 between steps (not timed)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def _stage_pass(pmha, torch, stream, flush, steps, fn):
+    """Per-stage CUDA-event times from a pass of their own (the library's stage
+    timer records events around each launch, so the headline steps run
+    without it)."""
+    pmha.pmha_profile_enable(True)
+    pmha.pmha_profile_read()
+    try:
+        _timed(torch, stream, flush, steps, fn)
+    finally:
+        pmha.pmha_profile_enable(False)
+    prof = pmha.pmha_profile_read()
+    stages = {k: {"launches": v[0], "total_ms": v[1], "avg_us": 1e3 * v[1] / max(v[0], 1)} for k, v in prof.items()}
+    total = sum(v["total_ms"] for v in stages.values()) or 1.0
+    for v in stages.values():
+        v["share"] = v["total_ms"] / total
+    return stages
+
+
+def _roofline(stages, w, B, nnz, peaks, wmode="none"):
+    """Roofline line of the dominant stage (the one with the largest total
+    time), and per-stage HBM / tensor fractions in place."""
+    for k, v in stages.items():
+        alg = algorithmic_bytes(k, w, B, nnz, wmode)
+        if alg is not None:
+            v["hbm_gbs_algorithmic"] = alg / (v["avg_us"] / 1e6) / 1e9
+            v["hbm_frac"] = v["hbm_gbs_algorithmic"] / peaks["hbm_gbs"]
+        fl = stage_flops(k, w, B)
+        if fl is not None:
+            v["tflops"] = fl / (v["avg_us"] / 1e6) / 1e12
+            v["tensor_frac"] = v["tflops"] / peaks["bf16_tflops"]
+    dom = max(stages, key=lambda k: stages[k]["total_ms"]) if stages else None
+    if dom is None:
+        return None
+    avg_s = stages[dom]["avg_us"] / 1e6
+    alg = algorithmic_bytes(dom, w, B, nnz, wmode)
+    fl = stage_flops(dom, w, B)
+    # a GEMM is tensor-bound when its arithmetic intensity passes the ridge
+    # point of the two measured peaks (E = 512), else memory-bound (E = 128)
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_bound = fl is not None and (dom in TENSOR_BOUND or (alg is not None and fl / alg > ridge))
+    if tensor_bound:
+        # timed inside a long loop of steps: the sustained tensor peak
+        achieved = fl / avg_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": ncu_traffic(dom, w.name), "algorithmic_flops_per_launch": fl,
+                "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
+                "peak_source": f"{peaks['source']} sustained bf16 GEMM (MEASURED_PEAKS.json "
+                               "bf16_tflops_sustained; fp16 runs at the bf16 rate)"}
+    if alg is not None:
+        achieved = alg / avg_s / 1e9
+        return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom, w.name),
+                "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
+                "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+    return None
+
+
+class _Problem:
+    """One workload resident on the device: graph, parameters, tokens, output,
+    weights and workspace buffers, and one forward step."""
+
+    def __init__(self, pmha, torch, dev, wid, rank, stream):
+        self.w = w = synth.workload(wid)
+        self.B = B = w.batch
+        self.src, self.tgt = synth.make_graph(wid)
+        self.xq_np, self.xkv_np, self.prm = make_rank_inputs(rank, B, wid)
+        self.self_attn = self.xkv_np is self.xq_np
+        self.tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.params = pmha.Params.from_arrays(self.prm, w.num_heads, self.tdt, dev)
+        self.graph = pmha.pmha_build_csr(torch.from_numpy(self.src).to(dev), torch.from_numpy(self.tgt).to(dev),
+                                         w.query_features, w.key_features)
+        self.nnz, self.H = self.graph.nnz, w.num_heads
+        self.x = torch.from_numpy(self.xq_np).to(self.tdt).to(dev)
+        self.kv = self.x if self.self_attn else torch.from_numpy(self.xkv_np).to(self.tdt).to(dev)
+        self.out = torch.empty_like(self.x)
+        # the workload's own need_weights (the bipartite map asks for averaged weights)
+        self.wmode = w.weights[0] if w.weights else "none"
+        shape = (B, self.nnz) if self.wmode == "avg" else (B, self.nnz, self.H)
+        self.weights = None if self.wmode == "none" else torch.empty(shape, dtype=torch.float32, device=dev)
+        self.ws = torch.empty(pmha.pmha_forward_workspace_size(self.graph, self.params, B, self.wmode),
+                              dtype=torch.uint8, device=dev)
+        self.pmha, self.stream = pmha, stream
+
+    def step(self, key_padding_mask=None):
+        self.pmha.pmha_forward(self.graph, self.params, self.x, self.kv, self.kv, self.wmode, out=self.out,
+                               weights=self.weights, workspace=self.ws, stream=self.stream,
+                               key_padding_mask=key_padding_mask)
+
+    @property
+    def scores(self):
+        return float(self.B) * self.nnz * self.H
+
+
+def measure_workload(pmha, torch, dev, wid, steps, warmup, flush, stream, peaks, cpu_seconds, rank=0):
+    """Layer forward time, stage times, the dominant kernel's roofline and the
+    oracle on a bounded sample, for one workload (not the headline)."""
+    pr = _Problem(pmha, torch, dev, wid, rank, stream)
+    for _ in range(warmup):
+        pr.step()
+    pmha.pmha_device_status()
+    ms = statistics.mean(_timed(torch, stream, flush, steps, pr.step))
+    stages = _stage_pass(pmha, torch, stream, flush, steps, pr.step)
+    pmha.pmha_device_status()
+    w = pr.w
+    roof = None if wid == 1 else _roofline(stages, w, pr.B, pr.nnz, peaks, pr.wmode)
+    cpu = None
+    if cpu_seconds > 0:
+        cpu = run_cpu_baseline(cpu_seconds, pr.src, pr.tgt, w, pr.xq_np, pr.xkv_np, pr.prm)
+    res = {"workload": w.name, "batch": pr.B, "nnz": pr.nnz, "embed_dim": w.embed_dim, "num_heads": w.num_heads,
+           "dtype": w.dtype, "need_weights": pr.wmode, "steps": steps, "ms_per_step": ms, "layer_fwd_us": ms * 1e3,
+           "value": pr.scores / (ms / 1e3), "unit": UNIT, "stages": stages,
+           "roofline": roof if roof is not None else ("none: a latency-bound correctness case (64 nodes)"
+                                                       if wid == 1 else None),
+           "cpu_baseline": cpu}
+    pr.graph.destroy()
+    return res
+
+
 def bench_ours(args):
     import torch
 
@@ -291,90 +466,61 @@ def bench_ours(args):
         dist.init_process_group("nccl", device_id=dev)
 
     import graph_sparse_head_gb300 as pmha
-    w = synth.workload(WORKLOAD_ID)
-    B = w.batch
-    src, tgt = synth.make_graph(WORKLOAD_ID)
-    xq_np, xkv_np, prm = make_rank_inputs(rank, B)
-    self_attn = xkv_np is xq_np
-    params = pmha.Params.from_arrays(prm, w.num_heads, torch.bfloat16, dev)
-    graph = pmha.pmha_build_csr(torch.from_numpy(src).to(dev), torch.from_numpy(tgt).to(dev),
-                                w.query_features, w.key_features)
-    nnz, H = graph.nnz, w.num_heads
-    x = torch.from_numpy(xq_np).to(torch.bfloat16).to(dev)
-    kv = x if self_attn else torch.from_numpy(xkv_np).to(torch.bfloat16).to(dev)
-    out = torch.empty_like(x)
-    ws = torch.empty(pmha.pmha_forward_workspace_size(graph, params, B, "none"), dtype=torch.uint8, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step():
-        pmha.pmha_forward(graph, params, x, kv, kv, "none", out=out, workspace=ws, stream=stream)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks = load_peaks()
+    pr = _Problem(pmha, torch, dev, WORKLOAD_ID, rank, stream)
+    w, B, nnz, H = pr.w, pr.B, pr.nnz, pr.H
+    graph, params, x, kv, out, ws = pr.graph, pr.params, pr.x, pr.kv, pr.out, pr.ws
+    xq_np, xkv_np, prm, src, tgt, self_attn = pr.xq_np, pr.xkv_np, pr.prm, pr.src, pr.tgt, pr.self_attn
+    step = pr.step
 
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     pmha.pmha_device_status()
 
+    # ---- the headline: K steps, the library's stage timer off
     sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
     first = sampler.mark()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     launches0 = pmha.pmha_launch_count()
-    pmha.pmha_profile_enable(True)
-    pmha.pmha_profile_read()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)  # evict L2 between steps (not timed)
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    step_ms = _timed(torch, stream, flush, args.steps, step)
     wall = time.perf_counter() - wall0
+    launches = pmha.pmha_launch_count() - launches0
+    last = sampler.mark()
     if world > 1:
         torch.distributed.barrier()
-    pmha.pmha_profile_enable(False)
-    prof = pmha.pmha_profile_read()
-    launches = pmha.pmha_launch_count() - launches0
-    clocks = sampler.summary(first)
-    sampler.stop()
     pmha.pmha_device_status()
-
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
     ms = max_over_ranks(ms, world, dev)
-    scores = float(B) * nnz * H
+    scores = pr.scores
     value = world * scores / (ms / 1e3)
+
+    # ---- stage times of the same steps, from a pass of their own
+    stage_steps = max(3, min(args.steps, 50))
+    stages = _stage_pass(pmha, torch, stream, flush, stage_steps, step)
+    pmha.pmha_device_status()
+    roof = _roofline(stages, w, B, nnz, peaks, pr.wmode)
 
     # ---- the same workload with a key_padding_mask: each sample keeps its
     # first n_b ~ U[S/2, S] keys (padding at the end), timed like the steps above
     kpm = torch.from_numpy(synth.padding_mask(np.random.default_rng(7 + rank), B, w.key_features)).to(dev)
     masked_steps = max(3, min(args.steps, 100))
     for _ in range(3):
-        pmha.pmha_forward(graph, params, x, kv, kv, "none", out=out, workspace=ws, stream=stream,
-                          key_padding_mask=kpm)
+        step(kpm)
     pmha.pmha_device_status()
-    pmha.pmha_profile_enable(True)
-    pmha.pmha_profile_read()
-    m_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(masked_steps)]
-    for i, (e_start, e_end) in enumerate(m_ev):
-        flush.fill_(i & 0xFF)
-        e_start.record(stream)
-        pmha.pmha_forward(graph, params, x, kv, kv, "none", out=out, workspace=ws, stream=stream,
-                          key_padding_mask=kpm)
-        e_end.record(stream)
-    torch.cuda.synchronize()
-    pmha.pmha_profile_enable(False)
-    m_prof = pmha.pmha_profile_read()
+    m_ms = max_over_ranks(statistics.mean(_timed(torch, stream, flush, masked_steps, lambda: step(kpm))), world, dev)
+    m_stages = _stage_pass(pmha, torch, stream, flush, min(masked_steps, 20), lambda: step(kpm))
     pmha.pmha_device_status()
-    m_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in m_ev) / masked_steps, world, dev)
-    masked = {"ms_per_step": m_ms, "value": world * float(B) * nnz * H / (m_ms / 1e3), "unit": UNIT,
+    masked = {"ms_per_step": m_ms, "value": world * scores / (m_ms / 1e3), "unit": UNIT,
               "steps": masked_steps, "kept_key_fraction": float(1.0 - kpm.float().mean().item()),
               "mask": "per-sample end padding, n_b ~ U[S/2, S] keys kept (value counts every edge)",
-              "stages_avg_us": {k: 1e3 * v[1] / max(v[0], 1) for k, v in m_prof.items()}}
+              "stages_avg_us": {k: v["avg_us"] for k, v in m_stages.items()}}
 
     # ---- the backward pass (pmha_backward: forward recompute + gradients of
     # inputs, weights and biases) for a seeded dout, timed the same way
@@ -383,26 +529,20 @@ def bench_ours(args):
         g_out = torch.from_numpy(synth.make_tokens(np.random.default_rng(11 + rank), B, w.query_features,
                                                    w.embed_dim, w.dtype)).to(torch.bfloat16).to(dev)
         ws_b = torch.empty(max(1, pmha.pmha_backward_workspace_size(graph, params, B)), dtype=torch.uint8, device=dev)
-        for _ in range(3):
+
+        def back_step():
             pmha.pmha_backward(graph, params, x, kv, kv, g_out, workspace=ws_b, stream=stream)
+
+        for _ in range(3):
+            back_step()
         pmha.pmha_device_status()
         back_steps = max(3, min(args.steps, 30))
-        pmha.pmha_profile_enable(True)
-        pmha.pmha_profile_read()
-        b_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(back_steps)]
-        for i, (e_start, e_end) in enumerate(b_ev):
-            flush.fill_(i & 0xFF)
-            e_start.record(stream)
-            pmha.pmha_backward(graph, params, x, kv, kv, g_out, workspace=ws_b, stream=stream)
-            e_end.record(stream)
-        torch.cuda.synchronize()
-        pmha.pmha_profile_enable(False)
-        b_prof = pmha.pmha_profile_read()
+        b_ms = max_over_ranks(statistics.mean(_timed(torch, stream, flush, back_steps, back_step)), world, dev)
+        b_stages = _stage_pass(pmha, torch, stream, flush, min(back_steps, 10), back_step)
         pmha.pmha_device_status()
-        b_ms = max_over_ranks(sum(e0_.elapsed_time(e1_) for e0_, e1_ in b_ev) / back_steps, world, dev)
-        back = {"ms_per_step": b_ms, "value": world * float(B) * nnz * H / (b_ms / 1e3), "unit": UNIT,
+        back = {"ms_per_step": b_ms, "value": world * scores / (b_ms / 1e3), "unit": UNIT,
                 "steps": back_steps, "what": "pmha_backward: forward recompute, input, weight and bias gradients",
-                "stages_avg_us": {k: 1e3 * v[1] / max(v[0], 1) for k, v in b_prof.items()}}
+                "stages_avg_us": {k: v["avg_us"] for k, v in b_stages.items()}}
 
     # ---- end to end through the C ABI with host buffers (pinned), per step:
     # copy the step's tokens in, run, copy the output back. Steps rotate over
@@ -451,53 +591,25 @@ def bench_ours(args):
     oh = outs[0]
     h2d = xh.numel() * xh.element_size() + (0 if self_attn else kvh.numel() * kvh.element_size())
     d2h = oh.numel() * oh.element_size()
-
-    # ---- roofline of the dominant kernel
-    peaks = load_peaks()
-    stages = {k: {"launches": v[0], "total_ms": v[1], "avg_us": 1e3 * v[1] / max(v[0], 1)} for k, v in prof.items()}
-    total_stage_ms = sum(v["total_ms"] for v in stages.values()) or 1.0
-    for v in stages.values():
-        v["share"] = v["total_ms"] / total_stage_ms
-    dom = max(stages, key=lambda k: stages[k]["total_ms"]) if stages else None
-    roof = None
-    if dom is not None:
-        avg_s = stages[dom]["avg_us"] / 1e6
-        alg = algorithmic_bytes(dom, w, B, nnz)
-        fl = stage_flops(dom, w, B)
-        # a GEMM is tensor-bound when its arithmetic intensity passes the ridge
-        # point of the two measured peaks (E = 512), else memory-bound (E = 128)
-        ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        tensor_bound = fl is not None and (dom in TENSOR_BOUND or (alg is not None and fl / alg > ridge))
-        if tensor_bound:
-            # timed inside a long loop of steps: the sustained tensor peak
-            achieved = fl / avg_s / 1e12
-            peak = peaks["bf16_tflops_sustained"]
-            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": ncu_traffic(dom, w.name), "algorithmic_flops_per_launch": fl,
-                    "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
-                    "peak_source": f"{peaks['source']} sustained bf16 GEMM (MEASURED_PEAKS.json "
-                                   "bf16_tflops_sustained; fp16 runs at the bf16 rate)"}
-        elif alg is not None:
-            achieved = alg / avg_s / 1e9
-            roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom, w.name),
-                    "algorithmic_bytes_per_launch": alg, "avg_launch_us": stages[dom]["avg_us"],
-                    "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
-    for k, v in stages.items():
-        alg = algorithmic_bytes(k, w, B, nnz)
-        if alg is not None:
-            v["hbm_gbs_algorithmic"] = alg / (v["avg_us"] / 1e6) / 1e9
-            v["hbm_frac"] = v["hbm_gbs_algorithmic"] / peaks["hbm_gbs"]
-        fl = stage_flops(k, w, B)
-        if fl is not None:
-            v["tflops"] = fl / (v["avg_us"] / 1e6) / 1e12
-            v["tensor_frac"] = v["tflops"] / peaks["bf16_tflops"]
+    clocks = sampler.summary(first, last)
+    sampler.stop()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
         cpu = run_cpu_baseline(args.cpu_seconds, src, tgt, w, xq_np, xkv_np, prm)
+
+    # ---- every other workload of the pages' shapes, on rank 0
+    per_workload = None
+    if rank == 0 and not args.no_per_workload:
+        per_workload = {}
+        for wid in sorted(synth.WORKLOADS):
+            if wid == WORKLOAD_ID:
+                continue
+            per_workload[synth.workload(wid).name] = measure_workload(
+                pmha, torch, dev, wid, max(3, min(args.steps, 20)), 3, flush, stream, peaks,
+                0.0 if args.no_cpu_baseline else args.cpu_seconds_per_workload)
 
     if rank == 0:
         line = {
@@ -506,6 +618,7 @@ def bench_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "batch": B, "n": w.query_features, "nnz": nnz,
                        "embed_dim": w.embed_dim, "num_heads": H, "max_in_degree": graph.max_in_degree,
+                       "need_weights": pr.wmode,
                        "l2": "flushed between timed steps (512 MiB write, untimed)",
                        "parallelism": f"replicas x{world}, own batch per rank, no collective"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -514,7 +627,10 @@ def bench_ours(args):
             "gpu_launches": launches,
             "roofline": roof,
             "stages": stages,
+            "stage_timing": f"a separate pass of {stage_steps} steps with the stage timer on (L2 flushed "
+                            "between steps); the headline steps run without it",
             "variants": {"key_padding_mask": masked, "backward": back},
+            "per_workload": per_workload,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "wall_s_timed_region": wall,
@@ -536,6 +652,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
+    ap.add_argument("--no-per-workload", action="store_true", help="skip the other workloads' lines")
+    ap.add_argument("--cpu-seconds-per-workload", type=float, default=3.0,
+                    help="budget of the oracle CPU baseline of each other workload")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=sorted(synth.WORKLOADS),
                     help="synthetic workload id (default: the skewed n=20,000 graph the metric is quoted on)")
     args = ap.parse_args(argv)

@@ -254,10 +254,13 @@ def _weights_shape(graph, batch, H, wmode):
 
 def pmha_forward(graph: Graph, params: Params, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
                  wmode: str = "none", out: torch.Tensor | None = None, weights: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None, stream=None, key_padding_mask: torch.Tensor | None = None):
+                 workspace: torch.Tensor | None = None, stream=None, key_padding_mask: torch.Tensor | None = None,
+                 check: bool = False):
     """One forward pass on device tensors: query (B, L, E), key / value (B, S, E),
     key_padding_mask (B, S) bool (True = key dropped) or None.
-    Returns (output (B, L, E), weights or None)."""
+    Returns (output (B, L, E), weights or None). The call returns once the work
+    is queued; check=True waits for it and raises what the kernels flagged (for
+    bfloat16 layers: an fp16 intermediate out of range, i.e. invalid outputs)."""
     B = int(query.shape[0])
     E, H = params.embed_dim, int(params.num_heads)
     dev = query.device
@@ -287,6 +290,9 @@ def pmha_forward(graph: Graph, params: Params, query: torch.Tensor, key: torch.T
                               _ptr(weights) if wm != PMHA_WEIGHTS_NONE else None, _ptr(ws),
                               ws.numel() * ws.element_size(), _stream_ptr(stream))
     _lib.check(st, "pmha_forward")
+    if check:
+        with torch.cuda.device(dev):
+            pmha_device_status(stream)
     return out, (weights if wm != PMHA_WEIGHTS_NONE else None)
 
 
@@ -410,7 +416,8 @@ def pmha_backward(graph: Graph, params: Params, query: torch.Tensor, key: torch.
 
 
 def pmha_device_status(stream=None) -> None:
-    """Synchronize the stream; raise if a bounded device-side wait gave up."""
+    """Synchronize the stream; raise if a kernel flagged a condition since the last
+    check: a bounded device-side wait gave up, or an fp16 intermediate overflowed."""
     _lib.check(_lib.load().pmha_device_status(_stream_ptr(stream)), "pmha_device_status")
 
 

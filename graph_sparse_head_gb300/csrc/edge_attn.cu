@@ -72,26 +72,68 @@ __global__ void __launch_bounds__(256) k_kpm_bits(const int32_t *__restrict__ co
 // weights[b, e, h] = 2^(s - m) / l for the target of edge e; averaged over
 // heads when out has one entry per edge. Runs in place when out == scores
 // (per-head layout: each thread reads its H scores before writing them).
-__global__ void k_weights(const float *scores, const float *__restrict__ ml,
-                          const int32_t *__restrict__ tgt_of_edge, long long B, long long nnz, int L,
-                          int H, bool average, float *out)
+// HC = H known at compile time (every score and (m, l) pair of the edge is
+// loaded with 16-byte loads before any arithmetic), or 0 for any H.
+__device__ __forceinline__ float edge_weight(float s, float m, float l)
+{
+    // a dropped key (score -inf) or a target with no live key (l = 0) weighs 0
+    return (l == 0.f || s == -INFINITY) ? 0.f : __fmul_rn(ex2(__fsub_rn(s, m)), __frcp_rn(l));
+}
+
+template <int HC>
+__global__ void __launch_bounds__(256) k_weights(const float *scores, const float *__restrict__ ml,
+                                                 const int32_t *__restrict__ tgt_of_edge, long long B,
+                                                 long long nnz, int L, int H_rt, bool average, float *out)
 {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= B * nnz) return;
     const long long b = i / nnz, e = i - b * nnz;
-    const int t = tgt_of_edge[e];
-    const float *s = scores + i * H;
-    const float *st = ml + ((b * L + t) * H) * 2;
-    float sum = 0.f;
-    for (int h = 0; h < H; ++h) {
-        // a dropped key (score -inf) or a target with no live key (l = 0) weighs 0
-        const float w = (st[2 * h + 1] == 0.f || s[h] == -INFINITY)
-                            ? 0.f
-                            : __fmul_rn(ex2(__fsub_rn(s[h], st[2 * h])), __frcp_rn(st[2 * h + 1]));
-        if (average) sum = __fadd_rn(sum, w);
-        else out[i * H + h] = w;
+    const int t = __ldg(tgt_of_edge + e);
+    if constexpr (HC > 0) {
+        static_assert(HC % 4 == 0, "16-byte loads of the scores");
+        float s[HC], st[2 * HC];
+#pragma unroll
+        for (int j = 0; j < HC / 4; ++j) {
+            const float4 v = reinterpret_cast<const float4 *>(scores + i * HC)[j];
+            s[4 * j] = v.x;
+            s[4 * j + 1] = v.y;
+            s[4 * j + 2] = v.z;
+            s[4 * j + 3] = v.w;
+        }
+        const float4 *mlp = reinterpret_cast<const float4 *>(ml + ((b * L + t) * HC) * 2);
+#pragma unroll
+        for (int j = 0; j < HC / 2; ++j) {
+            const float4 v = __ldg(mlp + j);
+            st[4 * j] = v.x;
+            st[4 * j + 1] = v.y;
+            st[4 * j + 2] = v.z;
+            st[4 * j + 3] = v.w;
+        }
+        float w[HC], sum = 0.f;
+#pragma unroll
+        for (int h = 0; h < HC; ++h) {
+            w[h] = edge_weight(s[h], st[2 * h], st[2 * h + 1]);
+            sum = __fadd_rn(sum, w[h]);
+        }
+        if (average) {
+            out[i] = __fdiv_rn(sum, (float)HC);
+        } else {
+#pragma unroll
+            for (int j = 0; j < HC / 4; ++j)
+                reinterpret_cast<float4 *>(out + i * HC)[j] = make_float4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+    } else {
+        const int H = H_rt;
+        const float *s = scores + i * H;
+        const float *st = ml + ((b * L + t) * H) * 2;
+        float sum = 0.f;
+        for (int h = 0; h < H; ++h) {
+            const float w = edge_weight(s[h], st[2 * h], st[2 * h + 1]);
+            if (average) sum = __fadd_rn(sum, w);
+            else out[i * H + h] = w;
+        }
+        if (average) out[i] = __fdiv_rn(sum, (float)H);
     }
-    if (average) out[i] = __fdiv_rn(sum, (float)H);
 }
 
 // Lane shape: a lane owns CPL channels (a whole head when the head has at
@@ -220,8 +262,20 @@ pmha_status weights_finalize(const pmha_graph *g, const EdgeArgs &a, pmha_wmode 
     if (n == 0) return PMHA_OK;
     const int TB = 256;
     StageTimer timer("weights", s);
-    k_weights<<<(unsigned)((n + TB - 1) / TB), TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L,
-                                                           (int)a.H, mode == PMHA_WEIGHTS_AVG, out);
+    const unsigned blocks = (unsigned)((n + TB - 1) / TB);
+    const bool avg = mode == PMHA_WEIGHTS_AVG;
+    // the 16-byte loads need 16-byte aligned scores, (m, l) and per-head output rows
+    const bool vec = ((uintptr_t)a.scores % 16 == 0) && ((uintptr_t)a.ml % 16 == 0) &&
+                     (avg || (uintptr_t)out % 16 == 0);
+    if (vec && a.H == 8)
+        k_weights<8><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, 8, avg, out);
+    else if (vec && a.H == 4)
+        k_weights<4><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, 4, avg, out);
+    else if (vec && a.H == 16)
+        k_weights<16><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, 16, avg, out);
+    else
+        k_weights<0><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, (int)a.H, avg,
+                                           out);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;

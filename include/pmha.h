@@ -231,6 +231,11 @@ pmha_status pmha_edge_weights(const pmha_graph *graph, const pmha_params *params
  * since the last check: a bounded device-side wait gave up (PMHA_ERR_TIMEOUT),
  * or an fp16 intermediate overflowed (PMHA_ERR_OVERFLOW); PMHA_ERR_CUDA if the
  * stream holds a CUDA error. Clears the flags. PMHA_OK otherwise.
+ * The compute calls return as soon as their work is queued, so these
+ * conditions never show in their own status: a bfloat16 layer keeps q, k, v
+ * and the mix in fp16, and inputs large enough to leave the fp16 range give
+ * invalid outputs that only this call reports. Callers that cannot bound
+ * their inputs poll it after the calls they want checked.
  */
 pmha_status pmha_device_status(pmha_stream stream);
 
@@ -244,11 +249,18 @@ pmha_status pmha_device_status(pmha_stream stream);
  * workspace comes from a scratch array of PMHA_NOALLOC_SCRATCH_BYTES built
  * into the library, which every GPU that loads this code keeps until the
  * process exits. Problems whose pmha_forward_workspace_size exceeds it are
- * rejected with PMHA_ERR_WORKSPACE and a message. The call allocates nothing.
- * Its first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture. All calls
- * share the array: calls whose GPU work overlaps (other streams, unordered
- * threads) race on it; calls queued on one stream are safe.
+ * rejected with PMHA_ERR_WORKSPACE and a message. Apart from its first call on
+ * a device, the call allocates nothing. That first call (with the device
+ * current) looks up the array's device address; under CUDA's lazy module
+ * loading it is also the moment the array is loaded onto the device, so it
+ * reserves the PMHA_NOALLOC_SCRATCH_BYTES and can fail (PMHA_ERR_CUDA, "could
+ * not reserve") when other allocations already hold the device's memory: make
+ * it early, before an allocator claims the memory, and before any stream
+ * capture. The address is cached per device and driver context; it does not
+ * survive cudaDeviceReset, so do not use this entry point on a device reset in
+ * the same process. All calls share the array: calls whose GPU work overlaps
+ * (other streams, unordered threads) race on it; calls queued on one stream
+ * are safe.
  */
 #define PMHA_NOALLOC_SCRATCH_BYTES (64u << 20)
 pmha_status pmha_forward_noalloc(const pmha_graph *graph, const pmha_params *params, const void *query,

@@ -2,8 +2,10 @@
 allocate device memory at call time (their allocator owns the device, or
 cudaMalloc / cudaFree may not run where they call the layer). It takes its
 workspace from a fixed scratch array inside the library instead of from the
-caller. Called here through the C ABI, twice in a row, and compared with
-pmha_forward on the same inputs at the tolerance the other parity tests use.
+caller. Called here through the C ABI, twice in a row: both calls must equal
+pmha_forward's results bit for bit (the same kernels run on the same inputs,
+only the workspace differs), and the first is also held to the oracle at the
+tolerance the other parity tests use.
 The file name sorts last so that a run stopping at the first failure has run
 every other test first; it also passes alone in a fresh process."""
 import ctypes
@@ -11,6 +13,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from tests._cases import Case, assert_close, assert_close_weights
 
@@ -37,14 +40,20 @@ def test_noalloc_matches_forward_on_two_calls(wid, B, wmode):
     p = params.as_struct()
     assert lib.pmha_forward_workspace_size(g.handle, ctypes.byref(p), B, pmha.WMODES[wmode]) <= (64 << 20)
     xq, xkv = c.device_inputs(DEV)
-    for _ in range(2):
+    oracle_out, oracle_w = c.oracle(need_weights=ref_w is not None)
+    for call in range(2):
         out = torch.full_like(ref_out, float("nan"))
         w = None if ref_w is None else torch.full_like(ref_w, float("nan"))
         _noalloc(lib, g, p, xq, xkv, out, wmode, w)
         pmha.pmha_device_status()
-        assert_close("noalloc output", out.float().cpu().numpy(), ref_out.float().cpu().numpy(), c.dt)
+        assert torch.equal(out, ref_out), f"call {call}: output differs from pmha_forward"
         if w is not None:
-            assert_close_weights("noalloc weights", w.cpu().numpy(), ref_w.cpu().numpy(), c.dt)
+            assert torch.equal(w, ref_w), f"call {call}: weights differ from pmha_forward"
+        if call == 0:
+            assert_close("noalloc output", out.float().cpu().numpy(), oracle_out, c.dt)
+            if w is not None:
+                wo = oracle_w if wmode == "per_head" else oracle.average_heads(oracle_w)
+                assert_close_weights("noalloc weights", w.cpu().numpy(), wo, c.dt)
     g.destroy()
 
 
