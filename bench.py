@@ -75,6 +75,12 @@ def algorithmic_bytes(stage: str, w: synth.Workload, B: int, nnz: int, wmode: st
                 + nnz * 4               # source index per CSR position
                 + (L + 1) * 4           # row pointers
                 + scores)
+    if stage == "edge_attn_out":
+        # the edge kernel with out_proj inside: q, k and v rows in, output rows
+        # out (the mixed rows it passes through L2 are not compulsory)
+        scores = (B * nnz * H * 4 + B * L * H * 8) if wmode != "none" else 0
+        return (B * L * E * bf + B * S * 2 * E * bf + E * E * bf + E * bf + B * L * E * bf
+                + nnz * 4 + (L + 1) * 4 + scores)
     if stage == "weights":
         out = B * nnz * (H if wmode == "per_head" else 1) * 4
         return B * nnz * H * 4 + B * L * H * 8 + nnz * 4 + out
@@ -124,6 +130,8 @@ KERNEL_SOURCES = {
                   "graph_sparse_head_gb300/csrc/edge_stream.cuh"],
     "proj_qkv": ["graph_sparse_head_gb300/csrc/gemm_tc.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
     "out_proj": ["graph_sparse_head_gb300/csrc/gemm_tc.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
+    "edge_attn_out": ["graph_sparse_head_gb300/csrc/edge_ring.cuh", "graph_sparse_head_gb300/csrc/edge_out.cuh",
+                      "graph_sparse_head_gb300/csrc/edge_attn_ring_out.cu", "graph_sparse_head_gb300/csrc/edge_stream.cuh"],
     "dense_attn": ["graph_sparse_head_gb300/csrc/dense_attn.cu", "graph_sparse_head_gb300/csrc/tc_util.cuh"],
 }
 
@@ -522,6 +530,26 @@ def bench_ours(args):
               "mask": "per-sample end padding, n_b ~ U[S/2, S] keys kept (value counts every edge)",
               "stages_avg_us": {k: v["avg_us"] for k, v in m_stages.items()}}
 
+    # ---- out_proj inside the edge kernel (PMHA_FUSED_OUT_PROJ=1, not the
+    # default), timed the same way
+    fused = None
+    if not args.no_fused_variant:
+        os.environ["PMHA_FUSED_OUT_PROJ"] = "1"
+        try:
+            for _ in range(3):
+                step()
+            pmha.pmha_device_status()
+            f_steps = max(3, min(args.steps, 50))
+            f_ms = max_over_ranks(statistics.mean(_timed(torch, stream, flush, f_steps, step)), world, dev)
+            f_stages = _stage_pass(pmha, torch, stream, flush, min(f_steps, 20), step)
+            pmha.pmha_device_status()
+        finally:
+            os.environ.pop("PMHA_FUSED_OUT_PROJ", None)
+        fused = {"ms_per_step": f_ms, "value": world * scores / (f_ms / 1e3), "unit": UNIT, "steps": f_steps,
+                 "what": "out_proj as tasks of the edge kernel's queue (PMHA_FUSED_OUT_PROJ=1)",
+                 "stages_avg_us": {k: v["avg_us"] for k, v in f_stages.items()},
+                 "roofline": _roofline(f_stages, w, B, nnz, peaks, pr.wmode)}
+
     # ---- the backward pass (pmha_backward: forward recompute + gradients of
     # inputs, weights and biases) for a seeded dout, timed the same way
     back = None
@@ -629,7 +657,7 @@ def bench_ours(args):
             "stages": stages,
             "stage_timing": f"a separate pass of {stage_steps} steps with the stage timer on (L2 flushed "
                             "between steps); the headline steps run without it",
-            "variants": {"key_padding_mask": masked, "backward": back},
+            "variants": {"key_padding_mask": masked, "backward": back, "fused_out_proj": fused},
             "per_workload": per_workload,
             "cpu_baseline": cpu,
             "clocks": clocks,
@@ -652,6 +680,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip timing the backward pass")
+    ap.add_argument("--no-fused-variant", action="store_true",
+                    help="skip timing out_proj inside the edge kernel (PMHA_FUSED_OUT_PROJ=1)")
     ap.add_argument("--no-per-workload", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--cpu-seconds-per-workload", type=float, default=3.0,
                     help="budget of the oracle CPU baseline of each other workload")

@@ -209,6 +209,17 @@ int64_t heavy_min_degree()
     return 0;
 }
 
+// Step 5 inside the edge kernel (where it can run there) when
+// PMHA_FUSED_OUT_PROJ=1 (read on every call); by default it runs as its own
+// tensor-core GEMM, which is the faster of the two on the measured workloads
+// (the edge kernel's warp-level products re-read Wo from shared memory for
+// every 16 rows and are bound by that bandwidth).
+bool fuse_out_proj()
+{
+    const char *e = getenv("PMHA_FUSED_OUT_PROJ");
+    return e && e[0] == '1' && e[1] == '\0';
+}
+
 bool out_proj_on_tensor_cores(const pmha_params *p)
 {
     return p->dtype == PMHA_BF16 && gemm_tc_supported(p->embed_dim);
@@ -238,8 +249,9 @@ Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode w
     if (with_values && out_proj_on_tensor_cores(p)) o += align256((size_t)(E * E) * 2);
     l.vt = o;
     if (with_values && dense_supported(g, E, H, inter_type(p->dtype))) o += align256(dense_vt_bytes(g, B, E));
-    l.counters = o;  // the light part of a split graph has its own merge list
-    o += align256((size_t)(kCounterHead + B * std::max(g->n_merge, g->light ? g->light->n_merge : (int64_t)0)) * 4);
+    l.counters = o;  // the light part of a split graph has its own merge list; then the out_proj block counts
+    o += align256((size_t)(kCounterHead + B * std::max(g->n_merge, g->light ? g->light->n_merge : (int64_t)0) +
+                           B * out_blocks(g->L)) * 4);
     l.kpm_bits = o;  // a key_padding_mask per CSR position, when one is given
     o += align256((size_t)(B * ((g->nnz + 31) / 32)) * 4);
     l.heavy = o;  // the heavy-target path's qt images and per-head mixes
@@ -256,6 +268,10 @@ pmha_status project(pmha_dtype dt, const void *X, int64_t M, int64_t E, const Ge
 {
     if (dt == PMHA_BF16 && gemm_tc_supported(E))
         return gemm_tc(TcType::BF16, TcType::F16, X, M, E, seg, Y, ldy, stage, s);
+    if (seg.cvt_frag_E) {
+        set_error("%s: the fragment-order copy of Wo needs the tensor-core GEMM", stage);
+        return PMHA_ERR_UNSUPPORTED;
+    }
     if (seg.cvt_n > 0) {
         const pmha_status st = convert_bf16_to_f16(seg.cvt_src, seg.cvt_dst, seg.cvt_n, s);
         if (st != PMHA_OK) return st;
@@ -279,21 +295,34 @@ GemmSegments segs(const void *w0, const void *b0, const void *w1 = nullptr, cons
 
 // Steps 1-4 (and the weights); with_values = false stops after the scores.
 // A non-null wo16 receives the fp16 copy of Wo that out_proj on the tensor
-// cores needs; the first projection GEMM writes it as a side job.
+// cores needs; the first projection GEMM writes it as a side job. A non-null
+// fused_out asks for step 5 inside the edge kernel, into fused_out, where
+// that kernel runs and supports it (fused_out_supported); *fused_done tells
+// whether it did (then wo16 holds Wo in the fragment order it reads).
 pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query, const void *key,
                    const void *value, const uint8_t *kpm, int64_t B, pmha_wmode wmode, float *weights, char *ws, const Layout &lay,
                    bool with_values, cudaStream_t s, const void **mixed_out, float *ml_keep = nullptr,
-                   bool allow_dense = true, EdgeArgs *args_out = nullptr, void *wo16 = nullptr)
+                   bool allow_dense = true, EdgeArgs *args_out = nullptr, void *wo16 = nullptr,
+                   void *fused_out = nullptr, bool *fused_done = nullptr)
 {
+    const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
+    const TcType it = inter_type(p->dtype);
+    // which kernels run steps 2-4: masked-dense tiles, the heavy/light split, or the edge kernel
+    const bool dense_path = allow_dense && with_values && dense_supported(g, E, H, it);
+    const bool heavy_path = !dense_path && with_values && wmode == PMHA_WEIGHTS_NONE && !kpm && !ml_keep &&
+                            !args_out && key == value && p->dtype == PMHA_BF16 && heavy_supported(g, E, H, it);
+    const bool fuse = fused_out && wo16 && with_values && !dense_path && !heavy_path && p->dtype == PMHA_BF16 &&
+                      gemm_tc_supported(E) && fused_out_supported(it, E, H);
+    if (fused_done) *fused_done = fuse;
     auto with_wo = [&](GemmSegments sg) {
         if (wo16) {
             sg.cvt_src = p->wo;
             sg.cvt_dst = wo16;
             sg.cvt_n = p->embed_dim * p->embed_dim;
+            sg.cvt_frag_E = fuse ? E : 0;
         }
         return sg;
     };
-    const int64_t E = p->embed_dim, H = p->num_heads, L = g->L, S = g->S;
     const size_t es = type_size(inter_type(p->dtype));
     char *qkv = ws + lay.qkv;
     EdgeArgs a;
@@ -348,9 +377,8 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.kpm = kpm;
     a.counters = (int *)(ws + lay.counters);
     a.kpm_bits = (uint32_t *)(ws + lay.kpm_bits);
-    const TcType it = inter_type(p->dtype);
     if (args_out) *args_out = a;
-    if (allow_dense && with_values && dense_supported(g, E, H, it)) {
+    if (dense_path) {
         // most (target, source) pairs are edges: steps 2-4 as masked-dense tiles
         DenseInputs din;
         din.q = a.q;
@@ -377,8 +405,7 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
         if (mixed_out) *mixed_out = a.mixed;
         return PMHA_OK;
     }
-    if (with_values && wmode == PMHA_WEIGHTS_NONE && !kpm && !ml_keep && !args_out && key == value &&
-        p->dtype == PMHA_BF16 && heavy_supported(g, E, H, it)) {
+    if (heavy_path) {
         // heavy targets on the tensor cores, the others on the per-edge kernel
         // over the light part of the graph (whose empty targets include the
         // heavy ones: their zero rows are overwritten by the heavy path)
@@ -398,6 +425,11 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
         if ((st = heavy_attention(g, hin, s)) != PMHA_OK) return st;
         if (mixed_out) *mixed_out = a.mixed;
         return PMHA_OK;
+    }
+    if (fuse) {
+        a.out = fused_out;
+        a.wo_frag = wo16;
+        a.bo = p->bo;
     }
     if ((st = edge_attention(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
     if ((st = empty_targets(inter_type(p->dtype), g, a, s)) != PMHA_OK) return st;
@@ -455,8 +487,11 @@ pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void
     // step 1's GEMM (same condition) leaves an fp16 copy of Wo in wo16
     const bool tc_out = out_proj_on_tensor_cores(p);
     void *wo16 = tc_out ? ws + lay.wo16 : nullptr;
-    st = attend(g, p, query, key, value, kpm, B, wmode, weights, ws, lay, true, s, &mixed, nullptr, true, nullptr, wo16);
+    bool fused = false;
+    st = attend(g, p, query, key, value, kpm, B, wmode, weights, ws, lay, true, s, &mixed, nullptr, true, nullptr, wo16,
+                fuse_out_proj() ? output : nullptr, &fused);
     if (st != PMHA_OK) return st;
+    if (fused) return PMHA_OK;  // step 5 ran inside the edge kernel
     // step 5: out_proj over the joined heads, mixed (intermediate type) -> output (layer dtype)
     const int64_t E = p->embed_dim;
     if (tc_out)

@@ -157,6 +157,13 @@ bool pick_shape(int64_t E, int64_t d, TcType t, int *cpl, int *lpe)
 
 }  // namespace
 
+bool fused_out_supported(TcType t, int64_t E, int64_t H)
+{
+    int cpl, lpe;
+    if (!PMHA_EDGE_RING || t != TcType::F16 || H < 1 || E % H || !pick_shape(E, E / H, t, &cpl, &lpe)) return false;
+    return cpl == 16 && lpe == 8;
+}
+
 bool edge_supported(int64_t E, int64_t H, TcType t)
 {
     int cpl, lpe;
@@ -202,6 +209,19 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.H = (int)a.H;
     k.d = (int)(a.E / a.H);
     k.score_scale = a.score_scale;
+    const bool fused = a.out != nullptr;
+    if (fused && (!a.with_values || !a.wo_frag || !fused_out_supported(dt, a.E, a.H))) {
+        set_error("edge attention: no fused out_proj for embed_dim %lld, num_heads %lld", (long long)a.E,
+                  (long long)a.H);
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    k.out = a.out;
+    k.wo_frag = (const uint32_t *)a.wo_frag;
+    k.bo = a.bo;
+    k.n_blk = (int)out_blocks(g->L);
+    k.blk_count = k.counters + a.B * g->n_merge;
+    k.err = device_error_word();
+    if (!k.err) return PMHA_ERR_CUDA;
     const long long slots = a.B * g->n_units;
     if (slots == 0) return PMHA_OK;
     if (a.v_off != a.E) {  // the kernel copies a row's k and v bytes as one run
@@ -217,12 +237,15 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     }
     // the ring kernel's task counter and the arrival counts of the pieces of
     // crossing targets (the edge kernel merges them)
-    PMHA_CUDA_TRY(cudaMemsetAsync(a.counters, 0, (size_t)(kCounterHead + a.B * g->n_merge) * 4, s));
-    StageTimer timer(a.with_values ? "edge_attn" : "edge_scores", s);
+    // (and, with out_proj tasks, the finished targets per block)
+    PMHA_CUDA_TRY(cudaMemsetAsync(
+        a.counters, 0, (size_t)(kCounterHead + a.B * g->n_merge + (fused ? a.B * k.n_blk : 0)) * 4, s));
+    StageTimer timer(fused ? "edge_attn_out" : (a.with_values ? "edge_attn" : "edge_scores"), s);
     // fp16 rows of 16 channels a lane and 8 to 32 lanes: the ring kernel
     // (edge_ring.cuh); other shapes and float32 layers: the streaming kernel
     const bool ring = PMHA_EDGE_RING && dt == TcType::F16 && cpl == 16 && lpe >= 8;
-    const pmha_status st = ring ? stream::launch_ring_f16(lpe, a.with_values, k, s)
+    const pmha_status st = fused ? stream::launch_ring_out_f16(lpe, k, s)
+                           : ring ? stream::launch_ring_f16(lpe, a.with_values, k, s)
                            : dt == TcType::F16 ? stream::launch_f16(cpl, lpe, a.with_values, k, slots, s)
                                                : stream::launch_f32(cpl, lpe, a.with_values, k, slots, s);
     if (st != PMHA_OK) return st;

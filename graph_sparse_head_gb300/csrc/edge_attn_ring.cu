@@ -27,9 +27,9 @@ int ring_blocks_per_sm(const void *kern, int threads, int smem)
 pmha_status launch_ring_f16(int lpe, bool wv, const Args &k, cudaStream_t s)
 {
     switch (lpe) {
-    case 8: return wv ? launch_ring<8, true>(k, s) : launch_ring<8, false>(k, s);
-    case 16: return wv ? launch_ring<16, true>(k, s) : launch_ring<16, false>(k, s);
-    case 32: return wv ? launch_ring<32, true>(k, s) : launch_ring<32, false>(k, s);
+    case 8: return wv ? launch_ring<8, true, false>(k, s) : launch_ring<8, false, false>(k, s);
+    case 16: return wv ? launch_ring<16, true, false>(k, s) : launch_ring<16, false, false>(k, s);
+    case 32: return wv ? launch_ring<32, true, false>(k, s) : launch_ring<32, false, false>(k, s);
     default: return PMHA_ERR_UNSUPPORTED;
     }
 }

@@ -40,6 +40,7 @@
 
 #include <algorithm>
 
+#include "edge_out.cuh"
 #include "edge_stream.cuh"
 
 namespace pmha {
@@ -81,6 +82,13 @@ __host__ __device__ constexpr int ring_smem_bytes()
 {
     return kRWarps * kRRing * ring_stage_bytes<WV>();
 }
+// With out_proj tasks (edge_out.cuh, embed_dim 128): one block of kFOWarps
+// warps per SM, their rings, then Wo (fp16, wo_frag_pos order) and bo (fp32)
+// for the whole block, loaded once: 16 x 12 KB + 32 KB + 512 B.
+constexpr int kFOWarps = 16;
+constexpr int kFOE = 128;
+__host__ __device__ constexpr int ring_fo_wo_offset() { return kFOWarps * kRRing * ring_stage_bytes<true>(); }
+__host__ __device__ constexpr int ring_fo_smem_bytes() { return ring_fo_wo_offset() + kFOE * kFOE * 2 + kFOE * 4; }
 
 // 32 bytes of shared memory as two 16-byte loads, from a0 and from a1
 __device__ __forceinline__ Raw<32> lds_pair(uint32_t a0, uint32_t a1)
@@ -117,11 +125,13 @@ __device__ __forceinline__ void fma_h2p(float &x, float &y, uint32_t v, uint16_t
 }
 
 // WV: mix values (else scores and (m, l) only); WS: write raw scores;
-// KPM: read a key_padding_mask (a dropped key scores -inf).
-template <int LPE, bool WV, bool WS, bool KPM>
-__global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a)
+// KPM: read a key_padding_mask (a dropped key scores -inf); FO: out_proj
+// tasks in the queue (edge_out.cuh).
+template <int LPE, bool WV, bool WS, bool KPM, bool FO>
+__global__ void __launch_bounds__((FO ? kFOWarps : kRWarps) * 32, FO ? 1 : 16 / kRWarps) k_edge_ring(Args a)
 {
     static_assert(LPE >= 8 && LPE <= 32, "8 to 32 lanes per row");
+    static_assert(!FO || (WV && 16 * LPE == kFOE), "out_proj needs the mixed rows, embed_dim 128");
     constexpr int P = 32 / LPE;             // slots (samples) per warp
     constexpr int NR = WV ? 2 : 1;          // row parts staged per edge: k (and v)
     constexpr int PART = LPE * kRCB;        // bytes of one row part of one slot
@@ -140,6 +150,17 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
 
     // ---- shared-memory addresses (stage offsets are added per step)
     const uint32_t wbase = smem_u32(smem_dyn) + (uint32_t)(warp * kRRing * STAGE);
+    if constexpr (FO) {
+        // the block's copy of Wo (fragment order) and bo (fp32), read by every out_proj task
+        const uint4 *wsrc = reinterpret_cast<const uint4 *>(a.wo_frag);
+        uint4 *wdst = reinterpret_cast<uint4 *>(smem_dyn + ring_fo_wo_offset());
+        for (int i = threadIdx.x; i < kFOE * kFOE * 2 / 16; i += blockDim.x) wdst[i] = wsrc[i];
+        float *bs = reinterpret_cast<float *>(smem_dyn + ring_fo_wo_offset() + kFOE * kFOE * 2);
+        const unsigned short *bo = (const unsigned short *)a.bo;
+        for (int i = threadIdx.x; i < kFOE; i += blockDim.x)
+            bs[i] = bo ? __bfloat162float(__ushort_as_bfloat16(bo[i])) : 0.f;
+        __syncthreads();
+    }
     // reads: the lane's first and second 16-byte chunk (swapped when sw = 1)
     const uint32_t rd_kv0 = wbase + (uint32_t)(slot * SLOT_ROW + 32 * grp + 16 * sw);
     const uint32_t rd_kv1 = wbase + (uint32_t)(slot * SLOT_ROW + 32 * grp + 16 * (1 - sw));
@@ -152,15 +173,34 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
     // Persistent warps: each takes tasks (sample group, unit) from one queue,
     // sample groups in order (their k|v rows stay in L2 meanwhile), within a
     // group the units with the most estimated work first, so the last tasks
-    // to start are short ones.
-    const unsigned n_tasks = (unsigned)(((a.B + P - 1) / P) * a.n_units);
+    // to start are short ones. With FO the out_proj tasks (a block of
+    // kOutRows targets of one sample each) follow all edge tasks, group by
+    // group: the warps that run out of edge tasks take the blocks of the
+    // groups already done while the last units finish.
+    const unsigned n_groups = (unsigned)((a.B + P - 1) / P);
+    const unsigned n_u = (unsigned)a.n_units;
+    const unsigned n_o = FO ? (unsigned)(P * a.n_blk) : 0u;
+    const unsigned n_tasks = n_groups * (n_u + n_o);
     for (;;) {
     unsigned task = 0;
     if (lane == 0) task = atomicAdd(a.task_counter, 1u);
     task = __shfl_sync(kAll, task, 0);
     if (task >= n_tasks) break;
-    const int u = a.unit_order[task % (unsigned)a.n_units];
-    const int b_slot = (int)(task / (unsigned)a.n_units) * P + slot;
+    unsigned grp_i = task / n_u, idx = task % n_u;
+    if constexpr (FO) {
+        if (task >= n_groups * n_u) {
+            const unsigned y = task - n_groups * n_u;
+            grp_i = y / n_o;
+            idx = y % n_o;
+            const int bb = (int)grp_i * P + (int)(idx % P);
+            if (bb < a.B)
+                out_proj_block<kFOE, kRRing * STAGE>(a, bb, (int)(idx / P), wbase,
+                                                     smem_u32(smem_dyn) + (uint32_t)ring_fo_wo_offset(), lane);
+            continue;
+        }
+    }
+    const int u = a.unit_order[idx];
+    const int b_slot = (int)grp_i * P + slot;
     const bool own = b_slot < a.B;  // slots past the batch store nothing
     const int b = own ? b_slot : a.B - 1;
     const int e0 = u * kUnitEdges;
@@ -293,6 +333,16 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
     int bound = end_in(wc, t);
     const bool first_started_here = a.row_ptr[t] == e0;
     bool is_first = true;
+    // FO: targets whose final row this slot wrote, in block cur_blk, not yet counted
+    int cur_blk = t_first / kOutRows, fin_cnt = 0;
+    auto count_block = [&]() {
+        if constexpr (FO) {
+            fence_gpu();
+            __syncwarp(kAll);
+            if (grp == 0 && fin_cnt) atomicAdd(a.blk_count + (long long)b * a.n_blk + cur_blk, fin_cnt);
+            fin_cnt = 0;
+        }
+    };
     Raw<kRCB> qr;
     float m = -INFINITY, l = 0.f;
     float acc[16];
@@ -378,6 +428,7 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
         const bool complete = (is_first ? first_started_here : true) && bound <= e1;
         if (complete) {
             if (own) {
+                if constexpr (FO) ++fin_cnt;
                 if constexpr (WV) write_mixed(acc, l > 0.f ? __frcp_rn(l) : 0.f);
                 if (a.ml && head_leader) {
                     float *p = a.ml + (((long long)b * a.L + t) * a.H + head) * 2;
@@ -412,6 +463,7 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
             if (own && prev == n_pieces - 1) {
                 fence_gpu();
                 merge_pieces(beg, u0, n_pieces);
+                if constexpr (FO) ++fin_cnt;
             }
         }
     };
@@ -425,6 +477,12 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
             ++t;
             bound = end_in(wc, t);
         } while (bound <= pos);
+        if constexpr (FO) {
+            if (t / kOutRows != cur_blk) {
+                count_block();
+                cur_blk = t / kOutRows;
+            }
+        }
         set_q(st);
         m = -INFINITY;
         l = 0.f;
@@ -579,6 +637,7 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
     }
     cp_async_wait<0>();
     finish();
+    count_block();
     }  // task loop
 }
 
@@ -586,29 +645,38 @@ __global__ void __launch_bounds__(kRWarps * 32, 16 / kRWarps) k_edge_ring(Args a
 // once per device and kernel).
 int ring_blocks_per_sm(const void *kern, int threads, int smem);
 
-template <int LPE, bool WV>
+template <int LPE, bool WV, bool FO>
 pmha_status launch_ring(const Args &k, cudaStream_t s)
 {
-    constexpr int smem = ring_smem_bytes<WV>();
+    constexpr int smem = FO ? ring_fo_smem_bytes() : ring_smem_bytes<WV>();
+    constexpr int NW = FO ? kFOWarps : kRWarps;
     constexpr int P = 32 / LPE;
     const long long warps = (k.B + P - 1) / P * k.n_units;
-    auto kern = k.kpm ? (k.scores ? k_edge_ring<LPE, WV, true, true> : k_edge_ring<LPE, WV, false, true>)
-                      : (k.scores ? k_edge_ring<LPE, WV, true, false> : k_edge_ring<LPE, WV, false, false>);
+    if ((k.B + P - 1) / P * (k.n_units + (FO ? (long long)P * k.n_blk : 0)) > 0xffffffffLL) {
+        set_error("edge attention: more than 2^32 tasks");
+        return PMHA_ERR_UNSUPPORTED;
+    }
+    auto kern = k.kpm ? (k.scores ? k_edge_ring<LPE, WV, true, true, FO> : k_edge_ring<LPE, WV, false, true, FO>)
+                      : (k.scores ? k_edge_ring<LPE, WV, true, false, FO> : k_edge_ring<LPE, WV, false, false, FO>);
     if constexpr (smem > 48 * 1024) {
         PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
     }
-    const int per_sm = ring_blocks_per_sm((const void *)kern, kRWarps * 32, smem);
+    const int per_sm = ring_blocks_per_sm((const void *)kern, NW * 32, smem);
     if (per_sm < 1) {
         set_error("edge attention: the ring kernel does not fit on an SM");
         return PMHA_ERR_UNSUPPORTED;
     }
-    const long long blocks = std::min<long long>((warps + kRWarps - 1) / kRWarps, (long long)per_sm * num_sms());
-    kern<<<(unsigned)blocks, kRWarps * 32, smem, s>>>(k);
+    // (with out_proj tasks: one block per SM, which the out_proj tasks keep busy)
+    const long long blocks =
+        FO ? (long long)per_sm * num_sms() : std::min<long long>((warps + NW - 1) / NW, (long long)per_sm * num_sms());
+    kern<<<(unsigned)blocks, NW * 32, smem, s>>>(k);
     return PMHA_OK;
 }
 
-// Entry point of the instantiating translation unit: lpe 8, 16 or 32.
+// Entry points of the instantiating translation units: lpe 8, 16 or 32; and
+// with out_proj tasks (k.out set), lpe 8.
 pmha_status launch_ring_f16(int lpe, bool wv, const Args &k, cudaStream_t s);
+pmha_status launch_ring_out_f16(int lpe, const Args &k, cudaStream_t s);
 
 }  // namespace stream
 }  // namespace pmha

@@ -88,6 +88,13 @@ struct Args {
     long long n_units, nnz;
     int B, L, S, E, H, d;
     float score_scale;
+    // out_proj inside the ring kernel (edge_out.cuh); out = null: none
+    void *out;                 // (B, L, E) bf16 rows
+    const uint32_t *wo_frag;   // Wo as fp16 in wo_frag_pos order
+    const void *bo;            // (E) bf16, or null (no bias)
+    int *blk_count;            // (B, n_blk) finished targets per block of kOutRows (zero at launch)
+    int n_blk;
+    int *err;                  // device error word (a poll that gave up sets kErrTimeoutBit)
 };
 
 template <typename T, int CPL, bool WV>

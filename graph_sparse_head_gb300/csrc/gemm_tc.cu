@@ -49,6 +49,13 @@ constexpr int kStages = PMHA_GEMM_STAGES;
 constexpr int kTileABytes = BM * BK * 2;
 constexpr int kTileBBytes = BN * BK * 2;
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
+// Row blocks are taken last-first, so the first rows of the output are the
+// last ones written and are still in L2 when the next kernel starts on them
+// (the edge kernel walks samples from the first; measured -1.7 % on the n=20k
+// layer with L2 flushed before each call).
+#ifndef PMHA_GEMM_REVERSE_M
+#define PMHA_GEMM_REVERSE_M 1
+#endif
 #ifndef PMHA_GEMM_EPI_GROUPS
 #define PMHA_GEMM_EPI_GROUPS 2
 #endif
@@ -88,6 +95,7 @@ struct TcArgs {
     const __nv_bfloat16 *cvt_src;
     __half *cvt_dst;
     int cvt_n;
+    int cvt_frag_E;  // nonzero: write the copy in wo_frag_pos order of this E x E matrix
 };
 
 // Two fp32 values to one 32-bit word of the output type. fp16 outputs also
@@ -166,6 +174,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int ks = tile % a.ksplit, mn = tile / a.ksplit;
         m_blk = mn / n_tiles_n;
         n_blk = mn % n_tiles_n;
+        if (PMHA_GEMM_REVERSE_M) m_blk = (a.M + BM - 1) / BM - 1 - m_blk;
         kb0 = ks * a.kb_per;
         kb1 = min(k_blocks, kb0 + a.kb_per);
     };
@@ -208,7 +217,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             for (int i = (int)blockIdx.x * per + lane - 1; i < end; i += 31) {
                 const float v = __bfloat162float(a.cvt_src[i]);
                 bad |= !(fabsf(v) <= 65504.f);
-                a.cvt_dst[i] = __float2half_rn(v);
+                const int64_t at = a.cvt_frag_E ? wo_frag_pos(i / a.cvt_frag_E, i % a.cvt_frag_E, a.cvt_frag_E) : i;
+                a.cvt_dst[at] = __float2half_rn(v);
             }
             if (bad) atomicOr(a.err, kErrRangeBit);
         } else {
@@ -468,6 +478,11 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     a.cvt_src = (const __nv_bfloat16 *)seg.cvt_src;
     a.cvt_dst = (__half *)seg.cvt_dst;
     a.cvt_n = seg.cvt_src && seg.cvt_dst ? (int)seg.cvt_n : 0;
+    a.cvt_frag_E = (int)seg.cvt_frag_E;
+    if (seg.cvt_frag_E && (seg.cvt_frag_E % 64 || seg.cvt_n != seg.cvt_frag_E * seg.cvt_frag_E)) {
+        set_error("gemm_tc: fragment-order conversion needs an E x E matrix with E a multiple of 64");
+        return PMHA_ERR_UNSUPPORTED;
+    }
     if (seg.cvt_n > 0x7fffffff) {
         set_error("gemm_tc: side conversion of %lld values exceeds the 32-bit index", (long long)seg.cvt_n);
         return PMHA_ERR_UNSUPPORTED;
@@ -551,6 +566,7 @@ pmha_status gemm_tc_general(TcType in, TcType out, const void *X, int64_t ldx, i
     a.cvt_src = nullptr;
     a.cvt_dst = nullptr;
     a.cvt_n = 0;
+    a.cvt_frag_E = 0;
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
     if (out == TcType::F32) kern = in_bf16 ? k_gemm_tc<__nv_bfloat16, float> : k_gemm_tc<__half, float>;
     else if (in_bf16) kern = out == TcType::F16 ? k_gemm_tc<__nv_bfloat16, __half> : k_gemm_tc<__nv_bfloat16, __nv_bfloat16>;

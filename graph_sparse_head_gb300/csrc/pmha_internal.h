@@ -119,7 +119,27 @@ struct GemmSegments {
     const void *cvt_src = nullptr;
     void *cvt_dst = nullptr;
     int64_t cvt_n = 0;
+    // nonzero: cvt_src is an E x E matrix (E = cvt_frag_E) and the copy is
+    // written in the mma.sync fragment order of wo_frag_pos
+    int64_t cvt_frag_E = 0;
 };
+
+// Place (in fp16 elements) of W[n][k] of an E x E matrix (E a multiple of
+// 64) in the B-fragment order of mma.sync m16n8k16 with B[k][n] = W[n][k]:
+// for output tile j (columns 8 j .. 8 j + 7) and k-steps 2 kp, 2 kp + 1, lane
+// l's four 32-bit registers (b0, b1 of step 2 kp, then of step 2 kp + 1) are
+// 16 consecutive bytes, and the 32 lanes' 512 bytes follow one another. b0
+// of a step holds k = 2 (l % 4) + {0, 1}, b1 the same k + 8, both for
+// n = 8 j + l / 4.
+__host__ __device__ inline int64_t wo_frag_pos(int n, int k, int E)
+{
+    const int j = n >> 3, nn = n & 7, ks = k >> 4, kk = k & 15;
+    const int kp = ks >> 1, kh = ks & 1;
+    const int lane = nn * 4 + ((kk & 7) >> 1);
+    const int r = kh * 2 + (kk >> 3);
+    const int64_t word = (((int64_t)j * (E / 32) + kp) * 32 + lane) * 4 + r;
+    return word * 2 + (kk & 1);
+}
 // Element types on the projection path. Layers stored in bf16 keep their
 // intermediates (q, k, v, mixed) in fp16; float32 layers stay float32.
 enum class TcType { BF16, F16, F32 };
@@ -155,8 +175,21 @@ struct EdgeArgs {
     int64_t B, L, S, E, H, nnz;
     float score_scale;    // log2(e) / sqrt(d)
     bool with_values;     // false: scores and (m, l) only
+    // out_proj inside the edge kernel (fused_out_supported): out (B, L, E)
+    // layer-type rows = mixed . Wo^T + bo, with Wo as fp16 in wo_frag_pos
+    // order; the mixed rows still pass through `mixed`. Null: mixed only.
+    void *out = nullptr;
+    const void *wo_frag = nullptr;
+    const void *bo = nullptr;
 };
 constexpr int kCounterHead = 64;  // words before the merge counters (256 bytes)
+// Targets per out_proj task of the fused edge kernel; the counter region
+// ends with (B, ceil(L / kOutRows)) counts of finished targets per block.
+constexpr int kOutRows = 64;
+inline int64_t out_blocks(int64_t L) { return (L + kOutRows - 1) / kOutRows; }
+// The fused out_proj runs in the ring edge kernel for fp16 intermediates,
+// embed_dim 128 (with heads of at least 16 channels): each block holds Wo.
+bool fused_out_supported(TcType t, int64_t E, int64_t H);
 // `t` is the intermediate type (F16 or F32) of q, k, v and mixed.
 bool edge_supported(int64_t E, int64_t H, TcType t);
 pmha_status edge_attention(TcType t, const pmha_graph *g, const EdgeArgs &a, cudaStream_t s);

@@ -183,6 +183,12 @@ size_t pmha_edge_weights_workspace_size(const pmha_graph *graph, const pmha_para
  *         target sum to 1 (to 0 when it has no edge).
  *  workspace, workspace_bytes  device scratch of at least
  *         pmha_forward_workspace_size() bytes, 256-byte aligned.
+ * With the environment variable PMHA_FUSED_OUT_PROJ=1 (read at each call),
+ * a bf16 layer with embed_dim 128 whose attention runs on the per-edge
+ * kernel computes out_proj inside that kernel instead of as its own GEMM
+ * (same results within rounding; slower on the measured workloads). A
+ * bounded wait there that gives up is reported by pmha_device_status as
+ * PMHA_ERR_TIMEOUT.
  * Errors: PMHA_ERR_INVALID_ARG, PMHA_ERR_UNSUPPORTED (a head size or width
  * without a kernel), PMHA_ERR_WORKSPACE, PMHA_ERR_CUDA (launch errors only;
  * the call does not synchronize).

@@ -65,3 +65,11 @@ def test_algorithmic_bytes_of_the_edge_kernel():
     got = bench.algorithmic_bytes("edge_attn", w, 16, 400_000)
     E, n, B = 128, 20_000, 16
     assert got == B * n * E * 2 + B * n * 2 * E * 2 + B * n * E * 2 + 400_000 * 4 + (n + 1) * 4
+
+
+def test_algorithmic_bytes_of_the_fused_edge_kernel():
+    # with out_proj inside: q, k|v in, the output rows out, Wo and bo once
+    w = bench.synth.workload(3)
+    got = bench.algorithmic_bytes("edge_attn_out", w, 16, 400_000)
+    E, n, B = 128, 20_000, 16
+    assert got == B * n * E * 2 + B * n * 2 * E * 2 + E * E * 2 + E * 2 + B * n * E * 2 + 400_000 * 4 + (n + 1) * 4

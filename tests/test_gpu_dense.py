@@ -40,7 +40,7 @@ def test_complete_graph(n, E, H, B):
     src, tgt = synth.complete_graph(rng, n)
     c = Case(src, tgt, n, n, E, H, B, "bf16", seed=n)
     (g, params, out, w), stages = _stages_of(lambda: c.run(DEV, "none"))
-    assert "dense_attn" in stages and "edge_attn" not in stages
+    assert "dense_attn" in stages and "edge_attn" not in stages and "edge_attn_out" not in stages
     ref_out, _ = c.oracle(need_weights=False)
     assert_close("output", out.float().cpu().numpy(), ref_out, "bf16")
     g.destroy()
@@ -115,5 +115,5 @@ def test_dense_edge_weights_bit_identical_to_forward():
 def test_sparse_graph_stays_on_the_edge_kernel():
     c = Case.workload(2, batch=1)
     (g, params, out, w), stages = _stages_of(lambda: c.run(DEV, "none"))
-    assert "edge_attn" in stages and "dense_attn" not in stages
+    assert ("edge_attn" in stages or "edge_attn_out" in stages) and "dense_attn" not in stages
     g.destroy()

@@ -97,6 +97,30 @@ def test_self_loops_appended_and_weights_in_given_order():
     g.destroy()
 
 
+@pytest.mark.parametrize("L,S,nnz,E,H,B,bip", [
+    (300, 300, 2999, 128, 8, 6, False),  # two sample groups of 4, the second half empty; last unit 7 positions
+    (200, 400, 3001, 256, 8, 3, True),   # 2 samples a warp: the second group has one; last unit 9 positions
+    (150, 150, 2113, 512, 8, 1, False),  # a whole warp per sample, d = 64 over 4 lanes; last unit 1 position
+])
+def test_sample_groups_and_ragged_last_unit(L, S, nnz, E, H, B, bip):
+    # The edge kernel walks sample groups of 32 / (E / 16) samples per warp:
+    # slots past the batch compute on the last sample and store nothing, and
+    # the graph's last unit of positions is short and odd-sized here.
+    import graph_sparse_head_gb300 as pmha
+    rng = np.random.default_rng(nnz)
+    src, tgt = synth.uniform_graph(rng, L, S, nnz, min_in_degree=1)
+    c = Case(src, tgt, L, S, E, H, B, "bf16", seed=E + B, bipartite=bip)
+    g, params, out, w = c.run(DEV, "per_head")
+    ref_out, ref_w = c.oracle()
+    assert_close("output", out.float().cpu().numpy(), ref_out, "bf16")
+    assert_close_weights("weights", w.cpu().numpy(), ref_w, "bf16")
+    xq, xkv = c.device_inputs(DEV)
+    w2 = pmha.pmha_edge_weights(g, params, xq, xkv, "per_head")
+    pmha.pmha_device_status()
+    assert torch.equal(w, w2)
+    g.destroy()
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_single_source_targets_exact(dt):
     # every target has exactly one source: weights are exactly 1, the mix is
@@ -249,8 +273,13 @@ def test_binding_refuses_mismatched_results_before_launch():
     g.destroy()
 
 
-def test_launch_counter_and_profile():
+@pytest.mark.parametrize("fused", [True, False, None])
+def test_launch_counter_and_profile(fused, monkeypatch):
     import graph_sparse_head_gb300 as pmha
+    if fused is None:  # the default: out_proj as its own GEMM
+        monkeypatch.delenv("PMHA_FUSED_OUT_PROJ", raising=False)
+    else:
+        monkeypatch.setenv("PMHA_FUSED_OUT_PROJ", "1" if fused else "0")
     c = _small(2, 1)
     n0 = pmha.pmha_launch_count()
     pmha.pmha_profile_enable(True)
@@ -258,8 +287,13 @@ def test_launch_counter_and_profile():
     prof = pmha.pmha_profile_read()
     pmha.pmha_profile_enable(False)
     assert pmha.pmha_launch_count() > n0
-    assert "edge_attn" in prof and prof["edge_attn"][0] == 1 and prof["edge_attn"][1] > 0
-    assert prof["proj_qkv"][0] == 1 and prof["out_proj"][0] == 1  # fused Q|K|V, then out_proj
+    assert prof["proj_qkv"][0] == 1  # fused Q|K|V
+    if fused:  # out_proj runs inside the edge kernel
+        assert "edge_attn_out" in prof and prof["edge_attn_out"][0] == 1 and prof["edge_attn_out"][1] > 0
+        assert "out_proj" not in prof and "edge_attn" not in prof
+    else:
+        assert "edge_attn" in prof and prof["edge_attn"][0] == 1 and prof["edge_attn"][1] > 0
+        assert prof["out_proj"][0] == 1
     g.destroy()
 
 

@@ -28,6 +28,24 @@ def test_full_workload_every_element(wid):
     g.destroy()
 
 
+@pytest.mark.parametrize("wid", [2, 3])
+def test_full_workload_fused_out_proj_every_element(wid, monkeypatch):
+    # out_proj inside the edge kernel (PMHA_FUSED_OUT_PROJ=1) at full size:
+    # every output element against the oracle
+    monkeypatch.setenv("PMHA_FUSED_OUT_PROJ", "1")
+    import graph_sparse_head_gb300 as pmha
+    c = Case.workload(wid)
+    pmha.pmha_profile_enable(True)
+    pmha.pmha_profile_read()
+    g, params, out, _ = c.run(DEV, "none")
+    stages = set(pmha.pmha_profile_read())
+    pmha.pmha_profile_enable(False)
+    assert "edge_attn_out" in stages and "out_proj" not in stages, stages
+    ref_out, _ = c.oracle(need_weights=False)
+    assert_close(f"workload {wid} fused output", out.float().cpu().numpy(), ref_out, c.dt)
+    g.destroy()
+
+
 def test_full_bipartite_every_element():
     # workload 4 at full size (B=64, 500 pathways x 20,000 genes, E=256,
     # need_weights): every output element, every per-head weight and every
