@@ -243,8 +243,8 @@ Layout layout(const pmha_graph *g, const pmha_params *p, int64_t B, pmha_wmode w
     o += align256((size_t)(B * 2 * g->n_units * (2 * H + E)) * 4);
     l.ml = o;
     if (wmode != PMHA_WEIGHTS_NONE) o += align256((size_t)(B * g->L * H * 2) * 4);
-    l.scores = o;
-    if (wmode == PMHA_WEIGHTS_AVG) o += align256((size_t)(B * g->nnz * H) * 4);
+    l.scores = o;  // raw scores by CSR position; the weights pass puts them in the given order
+    if (wmode != PMHA_WEIGHTS_NONE) o += align256((size_t)(B * g->nnz * H) * 4);
     l.wo16 = o;
     if (with_values && out_proj_on_tensor_cores(p)) o += align256((size_t)(E * E) * 2);
     l.vt = o;
@@ -365,7 +365,7 @@ pmha_status attend(const pmha_graph *g, const pmha_params *p, const void *query,
     a.mixed = with_values ? ws + lay.mixed : nullptr;
     a.part = (float *)(ws + lay.part);
     a.ml = ml_keep ? ml_keep : (wmode != PMHA_WEIGHTS_NONE ? (float *)(ws + lay.ml) : nullptr);
-    a.scores = wmode == PMHA_WEIGHTS_NONE ? nullptr : (wmode == PMHA_WEIGHTS_AVG ? (float *)(ws + lay.scores) : weights);
+    a.scores = wmode == PMHA_WEIGHTS_NONE ? nullptr : (float *)(ws + lay.scores);
     a.B = B;
     a.L = L;
     a.S = S;

@@ -81,20 +81,22 @@ __device__ __forceinline__ float edge_weight(float s, float m, float l)
 }
 
 template <int HC>
-__global__ void __launch_bounds__(256) k_weights(const float *scores, const float *__restrict__ ml,
-                                                 const int32_t *__restrict__ tgt_of_edge, long long B,
-                                                 long long nnz, int L, int H_rt, bool average, float *out)
+__global__ void __launch_bounds__(256) k_weights(const float *__restrict__ scores, const float *__restrict__ ml,
+                                                 const int32_t *__restrict__ tgt_of_edge,
+                                                 const int32_t *__restrict__ inv_perm, long long B, long long nnz,
+                                                 int L, int H_rt, bool average, float *out)
 {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= B * nnz) return;
     const long long b = i / nnz, e = i - b * nnz;
     const int t = __ldg(tgt_of_edge + e);
+    const long long si = b * nnz + __ldg(inv_perm + e);  // the edge's scores sit at its CSR position
     if constexpr (HC > 0) {
         static_assert(HC % 4 == 0, "16-byte loads of the scores");
         float s[HC], st[2 * HC];
 #pragma unroll
         for (int j = 0; j < HC / 4; ++j) {
-            const float4 v = reinterpret_cast<const float4 *>(scores + i * HC)[j];
+            const float4 v = reinterpret_cast<const float4 *>(scores + si * HC)[j];
             s[4 * j] = v.x;
             s[4 * j + 1] = v.y;
             s[4 * j + 2] = v.z;
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(256) k_weights(const float *scores, const floa
         }
     } else {
         const int H = H_rt;
-        const float *s = scores + i * H;
+        const float *s = scores + si * H;
         const float *st = ml + ((b * L + t) * H) * 2;
         float sum = 0.f;
         for (int h = 0; h < H; ++h) {
@@ -190,7 +192,6 @@ pmha_status edge_attention(TcType dt, const pmha_graph *g, const EdgeArgs &a, cu
     k.scores = a.scores;
     k.row_ptr = g->row_ptr;
     k.col = g->col;
-    k.perm = g->perm;
     k.unit_first_t = g->unit_first_t;
     k.unit_order = g->unit_order;
     k.task_counter = (unsigned *)a.counters;  // the first word of the counter region
@@ -291,13 +292,13 @@ pmha_status weights_finalize(const pmha_graph *g, const EdgeArgs &a, pmha_wmode 
     const bool vec = ((uintptr_t)a.scores % 16 == 0) && ((uintptr_t)a.ml % 16 == 0) &&
                      (avg || (uintptr_t)out % 16 == 0);
     if (vec && a.H == 8)
-        k_weights<8><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, 8, avg, out);
+        k_weights<8><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, 8, avg, out);
     else if (vec && a.H == 4)
-        k_weights<4><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, 4, avg, out);
+        k_weights<4><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, 4, avg, out);
     else if (vec && a.H == 16)
-        k_weights<16><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, 16, avg, out);
+        k_weights<16><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, 16, avg, out);
     else
-        k_weights<0><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, a.B, g->nnz, (int)g->L, (int)a.H, avg,
+        k_weights<0><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, (int)a.H, avg,
                                            out);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());

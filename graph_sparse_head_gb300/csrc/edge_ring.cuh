@@ -296,22 +296,6 @@ __global__ void __launch_bounds__((FO ? kFOWarps : kRWarps) * 32, FO ? 1 : 16 / 
     for (int j = 0; j < kRDepth; j += 2) issue2(j, j);
     static_assert(!kREarly || kRRing == kRDepth, "early release keeps every stage in flight");
 
-    // ---- given-order edge ids for the score write-out (32-wide windows)
-    int pw = 0, perm_cur = 0, perm_nxt = 0;
-    if constexpr (WS) {
-        perm_cur = lane < n ? a.perm[e0 + lane] : 0;
-        perm_nxt = 32 + lane < n ? a.perm[e0 + 32 + lane] : 0;
-    }
-    auto edge_id = [&](int j) -> int {  // j never decreases
-        if (j >= 32 * (pw + 1)) {
-            ++pw;
-            perm_cur = perm_nxt;
-            const int p = 32 * (pw + 1) + lane;
-            perm_nxt = p < n ? a.perm[e0 + p] : 0;
-        }
-        return __shfl_sync(kAll, perm_cur, j & 31);
-    };
-
     // ---- key_padding_mask per CSR position (one bit each, 32 positions a word)
     const uint32_t *kb = KPM ? a.kpm_bits + (long long)b * a.n_kw : nullptr;
     auto ldword = [&](int w) -> uint32_t { return (KPM && w < a.n_kw) ? kb[w] : 0u; };
@@ -547,10 +531,8 @@ __global__ void __launch_bounds__((FO ? kFOWarps : kRWarps) * 32, FO ? 1 : 16 / 
         if constexpr (WV) vr = lds_pair(rd_kv0 + st + PART, rd_kv1 + st + PART);
         if constexpr (KPM)
             if (masked(j)) dot = -INFINITY;
-        if constexpr (WS) {
-            const int e = edge_id(j);
-            if (head_leader) scores_b[(long long)e * a.H + head] = dot;
-        }
+        if constexpr (WS)
+            if (head_leader) scores_b[(long long)(e0 + j) * a.H + head] = dot;
         lift(dot);
         // ex2.approx(-inf) is +0, so a dropped edge gives p = 0 once some key
         // is live; before that m is -inf and the offset 0 avoids -inf - -inf
@@ -611,10 +593,9 @@ __global__ void __launch_bounds__((FO ? kFOWarps : kRWarps) * 32, FO ? 1 : 16 / 
                 if (masked(j + 1)) d1 = -INFINITY;
             }
             if constexpr (WS) {
-                const int i0 = edge_id(j), i1 = edge_id(j + 1);
                 if (head_leader) {
-                    scores_b[(long long)i0 * a.H + head] = d0;
-                    scores_b[(long long)i1 * a.H + head] = d1;
+                    scores_b[(long long)(e0 + j) * a.H + head] = d0;
+                    scores_b[(long long)(e0 + j + 1) * a.H + head] = d1;
                 }
             }
             lift(fmaxf(d0, d1));

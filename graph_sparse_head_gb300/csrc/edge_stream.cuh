@@ -72,10 +72,9 @@ struct Args {
     void *mixed;
     float *part;
     float *ml;
-    float *scores;
+    float *scores;  // (B, nnz, H) raw scores by CSR position, or null
     const int32_t *row_ptr;
     const int32_t *col;
-    const int32_t *perm;
     const int32_t *unit_first_t;
     const int32_t *unit_order;  // units by decreasing estimated work (the ring kernel's queue order)
     unsigned *task_counter;     // next task of the ring kernel's queue (zero at launch)
@@ -373,22 +372,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
 #pragma unroll
     for (int j = 0; j < kDepth; j += 2) issue2(j, j);
 
-    // ---- given-order edge ids for the score write-out
-    int pw = 0, perm_cur = 0, perm_nxt = 0;
-    if constexpr (WS) {
-        perm_cur = grp < n ? a.perm[e0 + grp] : 0;
-        perm_nxt = LPE + grp < n ? a.perm[e0 + LPE + grp] : 0;
-    }
-    auto edge_id = [&](int j) -> int {  // j never decreases
-        if (j >= (pw + 1) * LPE) {
-            ++pw;
-            perm_cur = perm_nxt;
-            const int p = (pw + 1) * LPE + grp;
-            perm_nxt = p < n ? a.perm[e0 + p] : 0;
-        }
-        return __shfl_sync(smask, perm_cur, j & (LPE - 1), LPE);
-    };
-
     // ---- key_padding_mask per CSR position (one bit each, 32 positions a
     // word, the next word prefetched): every lane holds the same word
     const uint32_t *kb = KPM ? a.kpm_bits + (long long)b * a.n_kw : nullptr;
@@ -618,8 +601,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
         if constexpr (KPM)
             if (masked(j)) dot = -INFINITY;
         if constexpr (WS) {
-            const int e = edge_id(j);
-            if (head_leader) scores_b[(long long)e * a.H + head] = dot;
+            if (head_leader) scores_b[(long long)(e0 + j) * a.H + head] = dot;
         }
         lift(dot);
         // ex2.approx(-inf) is +0, so a dropped edge gives p = 0 once some key
@@ -660,10 +642,9 @@ __global__ void __launch_bounds__(kWarps * 32) k_edge_stream(Args a)
                 if (masked(j + 1)) d1 = -INFINITY;
             }
             if constexpr (WS) {
-                const int i0 = edge_id(j), i1 = edge_id(j + 1);
                 if (head_leader) {
-                    scores_b[(long long)i0 * a.H + head] = d0;
-                    scores_b[(long long)i1 * a.H + head] = d1;
+                    scores_b[(long long)(e0 + j) * a.H + head] = d0;
+                    scores_b[(long long)(e0 + j + 1) * a.H + head] = d1;
                 }
             }
             lift(fmaxf(d0, d1));

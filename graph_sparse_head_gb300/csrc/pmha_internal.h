@@ -41,6 +41,7 @@ struct pmha_graph {
     int32_t *col = nullptr;           // nnz, source per CSR position
     int32_t *perm = nullptr;          // nnz, given-order edge id per CSR position
     int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
+    int32_t *inv_perm = nullptr;      // nnz, CSR position per given-order edge id
     int32_t *unit_first_t = nullptr;  // n_units, target of each unit's first position
     int32_t *unit_order = nullptr;    // n_units, the units by decreasing estimated work (ties by index)
     int32_t *merge_t = nullptr;       // n_merge, targets to merge (crossing a unit boundary, or without edges)
@@ -167,7 +168,7 @@ struct EdgeArgs {
     float *part;          // (B, 2 n_units, 2H + E): per slot m[H], l[H], acc[E] of a crossing target
     float *ml;            // (B, L, H, 2): softmax reference m (log2 units, at most 8 below the largest
                           // score) and l = sum of 2^(s - m), per target/head
-    float *scores;        // (B, nnz, H): raw scores (log2 units) by given-order edge id, or null
+    float *scores;        // (B, nnz, H): raw scores (log2 units) by CSR position, or null
     int *counters;        // kCounterHead words (a task counter), then (B, n_merge) pieces written per
                           // crossing target; zeroed by edge_attention before the edge kernel
     const uint8_t *kpm;   // (B, S) key_padding_mask, nonzero = key dropped, or null
