@@ -126,6 +126,41 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // a row's reference maximum moves only when a score passes it by more than this (log2 units)
 constexpr float kLazy = 8.f;
 
+// 2^x on the FMA pipe, for a share of the softmax's exponentials (the
+// multi-function unit gives 16 exponentials a clock per SM, a quarter of
+// what the tensor pipe feeds at head_dim 64). Range reduction x = j + f with
+// j = round(x) (the 1.5 * 2^23 shift puts j in the low mantissa bits of t)
+// and f in [-1/2, 1/2]; 2^f from a cubic fitted for this kernel as the
+// minimax of the relative error on [-1/2, 1/2] (7.5e-5, under half an fp16
+// step: P enters P V in fp16); j is added to the exponent field (the bits of
+// t shifted by 23 are j << 23, since those of 1.5 * 2^23 end in 23 zeros).
+// x is at most kLazy + the step's rounding; inputs below -125 give about
+// 2^-125 instead of 0, which rounds to 0 in fp16 and is nothing against a
+// row sum of at least 2^-kLazy.
+constexpr float kExpC0 = 9.999280572e-01f, kExpC1 = 6.932609677e-01f, kExpC2 = 2.426113188e-01f,
+                kExpC3 = 5.517175049e-02f;
+__device__ __forceinline__ float ex2_fma(float x)
+{
+    x = fmaxf(x, -125.f);
+    const float t = __fadd_rn(x, 12582912.f);
+    const float f = __fsub_rn(x, __fsub_rn(t, 12582912.f));
+    float p = __fmaf_rn(kExpC3, f, kExpC2);
+    p = __fmaf_rn(p, f, kExpC1);
+    p = __fmaf_rn(p, f, kExpC0);
+    return __int_as_float(__float_as_int(p) + (int)((uint32_t)__float_as_int(t) << 23));
+}
+// Pairs of columns (of 16 in 32) whose exponentials take ex2_fma: every
+// (16 / kEmuPairs)-th pair. 0 keeps every exponential on ex2.approx.
+#ifndef PMHA_DENSE_EMU_PAIRS
+#define PMHA_DENSE_EMU_PAIRS 0
+#endif
+constexpr int kEmuPairs = PMHA_DENSE_EMU_PAIRS;
+static_assert(kEmuPairs == 0 || (16 % kEmuPairs == 0), "an even spread of emulated pairs");
+__device__ __forceinline__ constexpr bool emulated_pair(int i)
+{
+    return kEmuPairs > 0 && (i % (16 / (kEmuPairs > 0 ? kEmuPairs : 1))) == (16 / (kEmuPairs > 0 ? kEmuPairs : 1)) - 1;
+}
+
 // head_dim 64: two CTAs per SM (registers capped at 170 a thread); 128: one
 template <int D>
 __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
@@ -352,8 +387,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (c + 1 < kTN / 32) tmem_ld32_async(tmem_s + lane_off + (uint32_t)((c + 1) * 32), nxt);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float p0 = ex2_approx(__fmaf_rn(__uint_as_float(cur[2 * i]), a.score_scale, -m_off));
-                    float p1 = ex2_approx(__fmaf_rn(__uint_as_float(cur[2 * i + 1]), a.score_scale, -m_off));
+                    const float x0 = __fmaf_rn(__uint_as_float(cur[2 * i]), a.score_scale, -m_off);
+                    const float x1 = __fmaf_rn(__uint_as_float(cur[2 * i + 1]), a.score_scale, -m_off);
+                    float p0 = emulated_pair(i) ? ex2_fma(x0) : ex2_approx(x0);
+                    float p1 = emulated_pair(i) ? ex2_fma(x1) : ex2_approx(x1);
                     if (!full) {
                         p0 = ((rb[c] >> (2 * i)) & 1u) ? p0 : 0.f;
                         p1 = ((rb[c] >> (2 * i + 1)) & 1u) ? p1 : 0.f;

@@ -209,19 +209,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
-        if (lane != 0) {
-            // ---------------- idle lanes of the producer warp: this CTA's share of the side conversion
-            const int per = (a.cvt_n + (int)gridDim.x - 1) / (int)gridDim.x;
-            const int end = min(a.cvt_n, ((int)blockIdx.x + 1) * per);
-            bool bad = false;
-            for (int i = (int)blockIdx.x * per + lane - 1; i < end; i += 31) {
-                const float v = __bfloat162float(a.cvt_src[i]);
-                bad |= !(fabsf(v) <= 65504.f);
-                const int64_t at = a.cvt_frag_E ? wo_frag_pos(i / a.cvt_frag_E, i % a.cvt_frag_E, a.cvt_frag_E) : i;
-                a.cvt_dst[at] = __float2half_rn(v);
-            }
-            if (bad) atomicOr(a.err, kErrRangeBit);
-        } else {
+        if (lane == 0) {
             // ---------------- TMA producer
             int stage = 0;
             uint32_t phase = 0;
@@ -303,6 +291,44 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int et = threadIdx.x - 64 - 128 * g;  // 0..127 within the group
         const int r = quarter * 32 + lane;  // tile row of this thread
         float *bias_g = bias_s + g * BN;
+        {
+            // Side job before the first accumulator is ready: this CTA's share
+            // of the bf16 -> fp16 copy, 8 values (one 16-byte load) a thread
+            // and step. (On the producer's idle lanes it held the first TMA
+            // loads back by up to 14 us at E = 512: divergent lanes of one warp.)
+            const int n8 = a.cvt_n / 8;  // cvt_n is a multiple of 8 (E x E, E a multiple of 64)
+            const int per = (n8 + (int)gridDim.x - 1) / (int)gridDim.x;
+            const int end = min(n8, ((int)blockIdx.x + 1) * per);
+            bool bad = false;
+            for (int c = (int)blockIdx.x * per + (threadIdx.x - 64); c < end; c += 128 * kEpi) {
+                const uint4 raw = reinterpret_cast<const uint4 *>(a.cvt_src)[c];
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+                __half h[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float v = __bfloat162float(__ushort_as_bfloat16((unsigned short)(w[q / 2] >> (16 * (q % 2)))));
+                    bad |= !(fabsf(v) <= 65504.f);
+                    h[q] = __float2half_rn(v);
+                }
+                const int i0 = 8 * c;
+                if (a.cvt_frag_E) {
+                    // k .. k + 7 of one row n: pairs land in four lanes' words
+#pragma unroll
+                    for (int q = 0; q < 8; q += 2) {
+                        const int64_t at = wo_frag_pos((i0 + q) / a.cvt_frag_E, (i0 + q) % a.cvt_frag_E, a.cvt_frag_E);
+                        *reinterpret_cast<__half2 *>(a.cvt_dst + at) = __halves2half2(h[q], h[q + 1]);
+                    }
+                } else {
+                    uint4 o;
+                    o.x = (uint32_t)__half_as_ushort(h[0]) | ((uint32_t)__half_as_ushort(h[1]) << 16);
+                    o.y = (uint32_t)__half_as_ushort(h[2]) | ((uint32_t)__half_as_ushort(h[3]) << 16);
+                    o.z = (uint32_t)__half_as_ushort(h[4]) | ((uint32_t)__half_as_ushort(h[5]) << 16);
+                    o.w = (uint32_t)__half_as_ushort(h[6]) | ((uint32_t)__half_as_ushort(h[7]) << 16);
+                    reinterpret_cast<uint4 *>(a.cvt_dst)[c] = o;
+                }
+            }
+            if (bad) atomicOr(a.err, kErrRangeBit);
+        }
         for (int i = g;; i += kEpi) {
             const int tile = blockIdx.x + i * gridDim.x;
             if (tile >= n_tiles) break;
