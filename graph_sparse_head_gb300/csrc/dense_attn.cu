@@ -161,6 +161,41 @@ __device__ __forceinline__ constexpr bool emulated_pair(int i)
     return kEmuPairs > 0 && (i % (16 / (kEmuPairs > 0 ? kEmuPairs : 1))) == (16 / (kEmuPairs > 0 ? kEmuPairs : 1)) - 1;
 }
 
+// Paired fp32 arithmetic for the softmax pass (each half rounds like the
+// scalar instruction) and a three-input maximum: fewer instructions per
+// score in a pass that is bound by instruction issue.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float x, float y)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(f32x2 r)
+{
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // head_dim 64: two CTAs per SM (registers capped at 170 a thread); 128: one
 template <int D>
 __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
@@ -361,9 +396,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (c + 1 < kTN / 32) tmem_ld32_async(tmem_s + lane_off + (uint32_t)((c + 1) * 32), nxt);
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = __uint_as_float(cur[i]);
-                    m4[i & 3] = fmaxf(m4[i & 3], full ? x : (((rb[c] >> i) & 1u) ? x : -INFINITY));
+                for (int i = 0; i < 16; ++i) {
+                    const float x0 = __uint_as_float(cur[2 * i]), x1 = __uint_as_float(cur[2 * i + 1]);
+                    m4[i & 3] = max3(m4[i & 3], full ? x0 : (((rb[c] >> (2 * i)) & 1u) ? x0 : -INFINITY),
+                                     full ? x1 : (((rb[c] >> (2 * i + 1)) & 1u) ? x1 : -INFINITY));
                 }
                 mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 if (c + 1 < kTN / 32) tmem_wait_ld();
@@ -376,7 +412,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const float m_off = m_new == -INFINITY ? 0.f : m_new;
             const float alpha = move ? ex2_approx(__fsub_rn(m, m_off)) : 1.f;
             // pass 2: P = 2^(s * scale - m) in fp16 (kept in registers) and the row sum
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            f32x2 sum2[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+            const f32x2 scale2 = pack2(a.score_scale, a.score_scale), neg_m2 = pack2(-m_off, -m_off);
             uint32_t pk[kTN / 32][16];
             tmem_ld32_async(tmem_s + lane_off, v0);
             tmem_wait_ld();
@@ -387,16 +424,15 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 if (c + 1 < kTN / 32) tmem_ld32_async(tmem_s + lane_off + (uint32_t)((c + 1) * 32), nxt);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float x0 = __fmaf_rn(__uint_as_float(cur[2 * i]), a.score_scale, -m_off);
-                    const float x1 = __fmaf_rn(__uint_as_float(cur[2 * i + 1]), a.score_scale, -m_off);
-                    float p0 = emulated_pair(i) ? ex2_fma(x0) : ex2_approx(x0);
-                    float p1 = emulated_pair(i) ? ex2_fma(x1) : ex2_approx(x1);
+                    const float2 x = unpack2(
+                        fma2(pack2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), scale2, neg_m2));
+                    float p0 = emulated_pair(i) ? ex2_fma(x.x) : ex2_approx(x.x);
+                    float p1 = emulated_pair(i) ? ex2_fma(x.y) : ex2_approx(x.y);
                     if (!full) {
                         p0 = ((rb[c] >> (2 * i)) & 1u) ? p0 : 0.f;
                         p1 = ((rb[c] >> (2 * i + 1)) & 1u) ? p1 : 0.f;
                     }
-                    sum4[(2 * i) & 3] = __fadd_rn(sum4[(2 * i) & 3], p0);
-                    sum4[(2 * i + 1) & 3] = __fadd_rn(sum4[(2 * i + 1) & 3], p1);
+                    sum2[i & 1] = add2(sum2[i & 1], pack2(p0, p1));
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     pk[c][i] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
@@ -439,7 +475,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             tc_fence_before();
             fence_async_shared();
             mbar_arrive(smem_u32(p_full));
-            const float sum = __fadd_rn(__fadd_rn(sum4[0], sum4[1]), __fadd_rn(sum4[2], sum4[3]));
+            const float2 sa = unpack2(sum2[0]), sb = unpack2(sum2[1]);
+            const float sum = __fadd_rn(__fadd_rn(sa.x, sb.x), __fadd_rn(sa.y, sb.y));
             l = __fadd_rn(__fmul_rn(l, alpha), sum);
             m = m_new;
         }
