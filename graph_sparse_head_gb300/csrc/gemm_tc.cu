@@ -47,8 +47,6 @@ constexpr int BM = 128, BN = 128, BK = 64;
 #endif
 constexpr int kStages = PMHA_GEMM_STAGES;
 constexpr int kTileABytes = BM * BK * 2;
-constexpr int kTileBBytes = BN * BK * 2;
-constexpr int kStageBytes = kTileABytes + kTileBBytes;
 // Row blocks are taken last-first, so the first rows of the output are the
 // last ones written and are still in L2 when the next kernel starts on them
 // (the edge kernel walks samples from the first; measured -1.7 % on the n=20k
@@ -62,23 +60,39 @@ constexpr int kStageBytes = kTileABytes + kTileBBytes;
 constexpr int kEpi = PMHA_GEMM_EPI_GROUPS;  // epilogue warpgroups (1 to 3)
 static_assert(kEpi >= 1 && kEpi <= 3, "one to three epilogue groups");
 constexpr int kAcc = kEpi == 1 ? 2 : kEpi;   // TMEM accumulators (one per group, or two for one group)
-constexpr int kBufs = kEpi == 1 ? 2 : kEpi;  // staging tiles (one per group, or two for one group)
 constexpr int kThreads = 64 + 128 * kEpi;
-constexpr int kTmemCols = kAcc * BN <= 256 ? 256 : 512;  // a power of two
 constexpr int kOutBoxBytes = BM * 128;             // 128 rows x 64 16-bit columns, 128-byte swizzle
 constexpr int kOutTileBytes = 2 * kOutBoxBytes;     // one 128 x 128 output tile
-constexpr int kBiasBytes = kEpi * BN * 4;  // fp32 bias of the tile, per group
-constexpr int kSmemBytes = kStages * kStageBytes + kBufs * kOutTileBytes + kBiasBytes + 1024 /*align*/ + 256 /*barriers*/;
-static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
+
+// Tile width WN: 128 columns (BN), or 256 for the wide layers. A tensor-bound
+// tile waits for its operands, which reach shared memory at about 95 GB/s
+// per SM (a 128 x 128 x 16 MMA itself takes 65 cycles when its operands are
+// in place); a 256-column tile reads 25 % fewer operand bytes per output.
+// Wide tiles hold four 48 KB stages and store their output straight from
+// registers (16-byte stores, each thread a row).
+template <int WN>
+struct Tile {
+    static_assert(WN == 128 || WN == 256, "128- or 256-column tiles");
+    static constexpr bool kDirect = WN > BN;  // epilogue stores from registers, no staging tile
+    static constexpr int kStages = kDirect ? 4 : ::pmha::kStages;
+    static constexpr int kTileB = WN * BK * 2;
+    static constexpr int kStage = kTileABytes + kTileB;
+    static constexpr int kBufs = kDirect ? 0 : (kEpi == 1 ? 2 : kEpi);  // staging tiles
+    static constexpr int kTmemCols = kAcc * WN <= 256 ? 256 : 512;      // a power of two
+    static constexpr int kBias = kEpi * WN * 4;                         // fp32 bias of the tile, per group
+    static constexpr int kSmem = kStages * kStage + kBufs * kOutTileBytes + kBias + 1024 /*align*/ + 256 /*barriers*/;
+    static_assert(kAcc * WN <= 512, "the accumulators fit in tensor memory");
+    static_assert(kSmem <= 232448, "shared memory of one CTA");
+};
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A and B of one 16-bit type (bits 7-9 and 10-12: 0 = f16, 1 = bf16), both
 // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-template <typename TIn>
+template <typename TIn, int WN>
 __host__ __device__ constexpr uint32_t idesc()
 {
     constexpr uint32_t f = std::is_same<TIn, __nv_bfloat16>::value ? 1u : 0u;
-    return (1u << 4) | (f << 7) | (f << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    return (1u << 4) | (f << 7) | (f << 10) | ((uint32_t)(WN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
 struct TcArgs {
@@ -144,17 +158,20 @@ __device__ __forceinline__ bool epi_sync_or(int g, bool pred)
     return r != 0;
 }
 
-template <typename TIn, typename TOut>
+template <typename TIn, typename TOut, int WN>
 __global__ void __launch_bounds__(kThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
           const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
           const __grid_constant__ CUtensorMap tm_y, TcArgs a)
 {
+    using TL = Tile<WN>;
+    constexpr int kStages = TL::kStages, kStageBytes = TL::kStage, kBufs = TL::kBufs, kTmemCols = TL::kTmemCols;
+    constexpr int kBiasBytes = TL::kBias;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *tiles = smem;
-    uint8_t *staging = smem + kStages * kStageBytes;  // two output tiles
-    float *bias_s = (float *)(staging + kBufs * kOutTileBytes);  // [kEpi][BN]
+    uint8_t *staging = smem + kStages * kStageBytes;  // output staging tiles (none for wide tiles)
+    float *bias_s = (float *)(staging + kBufs * kOutTileBytes);  // [kEpi][WN]
     uint64_t *bars = (uint64_t *)(staging + kBufs * kOutTileBytes + kBiasBytes);
     uint64_t *full = bars;                    // [kStages]
     uint64_t *empty = bars + kStages;         // [kStages]
@@ -166,7 +183,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     int *issued = (int *)(tmem_holder + 2);  // [kStages]: TMA phases armed per stage
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles_n = a.N / BN;
+    const int n_tiles_n = a.N / WN;
     const int n_tiles = ((a.M + BM - 1) / BM) * n_tiles_n * a.ksplit;
     const int k_blocks = a.K / BK;
     // tile -> (row block, column block, K split)
@@ -216,7 +233,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
                 int m_blk, n_blk, kb0, kb1;
                 decode(tile, m_blk, n_blk, kb0, kb1);
-                const int n_glob = n_blk * BN;
+                const int n_glob = n_blk * WN;
                 const int seg = n_glob / a.E;
                 const int n_loc = n_glob - seg * a.E;
                 const CUtensorMap *tw = seg == 0 ? &tm_w0 : (seg == 1 ? &tm_w1 : &tm_w2);
@@ -245,7 +262,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1u, abort_flag, a.err)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * WN);
                 int m_blk, n_blk, kb0, kb1;
                 decode(tile, m_blk, n_blk, kb0, kb1);
                 bool ok = true;
@@ -260,7 +277,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         // +32 bytes along K inside the swizzle atom = +2 in the address field
-                        mma_f16kind(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc<TIn>(),
+                        mma_f16kind(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc<TIn, WN>(),
                                     (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&empty[stage]));
@@ -290,7 +307,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int g = (warp - 2) >> 2;          // epilogue group
         const int et = threadIdx.x - 64 - 128 * g;  // 0..127 within the group
         const int r = quarter * 32 + lane;  // tile row of this thread
-        float *bias_g = bias_s + g * BN;
+        float *bias_g = bias_s + g * WN;
         {
             // Side job before the first accumulator is ready: this CTA's share
             // of the bf16 -> fp16 copy, 8 values (one 16-byte load) a thread
@@ -337,23 +354,29 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const int buf = kEpi == 1 ? acc : g;
             int m_blk, n_blk, kb0, kb1;
             decode(tile, m_blk, n_blk, kb0, kb1);
-            const int n_glob = n_blk * BN;
+            const int n_glob = n_blk * WN;
             const int seg = n_glob / a.E;
             const int n_loc = n_glob - seg * a.E;
             const __nv_bfloat16 *bias = a.bias[seg];
-            // this thread's bias value, loaded before the accumulator wait so
-            // that the wait covers the load
-            float bias_v = 0.f;
+            // this thread's bias values, loaded before the accumulator wait so
+            // that the wait covers the loads
+            float bias_v[WN / 128] = {};
             if constexpr (!std::is_same<TOut, float>::value)
-                if (bias) bias_v = __bfloat162float(bias[n_loc + et]);
+                if (bias)
+#pragma unroll
+                    for (int j = 0; j < WN / 128; ++j) bias_v[j] = __bfloat162float(bias[n_loc + et + 128 * j]);
             const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err);
             // the store that last read this group's staging tile is done
-            if (et == 0) {
-                if constexpr (kEpi >= 2) bulk_wait_read0();
-                else bulk_wait_read1();
+            if constexpr (!TL::kDirect) {
+                if (et == 0) {
+                    if constexpr (kEpi >= 2) bulk_wait_read0();
+                    else bulk_wait_read1();
+                }
             }
-            // the readers of the previous tile's bias passed the barrier before its store
-            if constexpr (!std::is_same<TOut, float>::value) bias_g[et] = bias_v;
+            // the readers of the previous tile's bias passed a barrier of the group since
+            if constexpr (!std::is_same<TOut, float>::value)
+#pragma unroll
+                for (int j = 0; j < WN / 128; ++j) bias_g[et + 128 * j] = bias_v[j];
             if (epi_sync_or(g, !ok)) break;  // one decision for all 128 threads
             tc_fence_after();
             const bool live = m_blk * BM + r < a.M;
@@ -362,9 +385,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 float *dst = (float *)a.out + (long long)(tile % a.ksplit) * a.part_stride +
                              (long long)(m_blk * BM + r) * a.ldy + n_glob;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < WN / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), v);
+                    tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * WN + c * 32), v);
                     if (live) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
@@ -375,6 +398,40 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 tc_fence_before();
                 mbar_arrive(smem_u32(&acc_empty[acc]));
                 continue;
+            } else if constexpr (TL::kDirect) {
+                // wide tile: + bias, rounded, stored from registers (64 bytes of
+                // this thread's row per 32 columns, whole 32-byte sectors)
+                uint8_t *dst = (uint8_t *)a.out + ((long long)(m_blk * BM + r) * a.ldy + n_glob) * 2;
+                bool range_bad = false;
+                const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * WN);
+#pragma unroll 1
+                for (int c = 0; c < WN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + (uint32_t)(c * 32), v);
+                    uint32_t packed[16];
+                    bool bad = false;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        float v0 = __uint_as_float(v[2 * j]), v1 = __uint_as_float(v[2 * j + 1]);
+                        if (bias) {
+                            const float2 bb = *reinterpret_cast<const float2 *>(bias_g + c * 32 + 2 * j);
+                            v0 = __fadd_rn(v0, bb.x);
+                            v1 = __fadd_rn(v1, bb.y);
+                        }
+                        packed[j] = pack2<TOut>(v0, v1, bad);
+                    }
+                    range_bad |= bad && live;
+                    if (live) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(dst + c * 64 + 16 * q) =
+                                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    }
+                }
+                if (range_bad) atomicOr(a.err, kErrRangeBit);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&acc_empty[acc]));
+                epi_sync(g);  // every thread is done with this tile's bias
             } else {
             uint8_t *sb = staging + buf * kOutTileBytes;
             bool range_bad = false;
@@ -402,9 +459,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                         make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 }
             };
-            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * WN);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < WN / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t_row + (uint32_t)(c * 32), v);
                 emit(c, v);
@@ -471,6 +528,12 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
         return PMHA_ERR_INVALID_ARG;
     }
     const bool in_bf16 = in == TcType::BF16;
+    // 256-column tiles where the GEMM is bound by its operands rather than its
+    // output: E >= 512 (complete-graph layer: q|k|v 28.7 -> 27.2 us). At
+    // E = 256 the output-heavy k|v projection was slower with them (479.9 ->
+    // 561.5 us): the register stores of the wide epilogue cost more there than
+    // the operand bytes they save.
+    const bool wide = E % 256 == 0 && E >= 512;
     CUtensorMap mx, mw[3];
     if (!make_map(&mx, X, M, E, in_bf16)) {
         set_error("gemm_tc: cuTensorMapEncodeTiled failed for X (pointer %p)", X);
@@ -478,7 +541,7 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     }
     for (int i = 0; i < 3; ++i) {
         const void *w = seg.w[i < seg.n_seg ? i : 0];
-        if (!make_map(&mw[i], w, E, E, in_bf16)) {
+        if (!make_map_box(&mw[i], w, E, E, E, in_bf16, BK, wide ? 256 : BN)) {
             set_error("gemm_tc: cuTensorMapEncodeTiled failed for W (pointer %p)", w);
             return PMHA_ERR_CUDA;
         }
@@ -515,10 +578,18 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     }
 
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
-    if (in_bf16 && out == TcType::F16) kern = k_gemm_tc<__nv_bfloat16, __half>;
-    else if (in_bf16) kern = k_gemm_tc<__nv_bfloat16, __nv_bfloat16>;
-    else if (out == TcType::BF16) kern = k_gemm_tc<__half, __nv_bfloat16>;
-    else kern = k_gemm_tc<__half, __half>;
+    if (wide) {
+        if (in_bf16 && out == TcType::F16) kern = k_gemm_tc<__nv_bfloat16, __half, 256>;
+        else if (in_bf16) kern = k_gemm_tc<__nv_bfloat16, __nv_bfloat16, 256>;
+        else if (out == TcType::BF16) kern = k_gemm_tc<__half, __nv_bfloat16, 256>;
+        else kern = k_gemm_tc<__half, __half, 256>;
+    } else {
+        if (in_bf16 && out == TcType::F16) kern = k_gemm_tc<__nv_bfloat16, __half, BN>;
+        else if (in_bf16) kern = k_gemm_tc<__nv_bfloat16, __nv_bfloat16, BN>;
+        else if (out == TcType::BF16) kern = k_gemm_tc<__half, __nv_bfloat16, BN>;
+        else kern = k_gemm_tc<__half, __half, BN>;
+    }
+    const int smem_bytes = wide ? Tile<256>::kSmem : Tile<BN>::kSmem;
     static std::mutex mu;
     static std::set<std::pair<int, void *>> configured;
     int dev = 0;
@@ -526,14 +597,14 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
     {
         std::lock_guard<std::mutex> lk(mu);
         if (!configured.count({dev, (void *)kern})) {
-            PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+            PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes));
             configured.insert({dev, (void *)kern});
         }
     }
-    const int n_tiles = (int)(((M + BM - 1) / BM) * (a.N / BN));
+    const int n_tiles = (int)(((M + BM - 1) / BM) * (a.N / (wide ? 256 : BN)));
     const int grid = std::min(n_tiles, num_sms());
     StageTimer timer(stage, stream);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw[0], mw[1], mw[2], my, a);
+    kern<<<grid, kThreads, smem_bytes, stream>>>(mx, mw[0], mw[1], mw[2], my, a);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;
@@ -594,9 +665,10 @@ pmha_status gemm_tc_general(TcType in, TcType out, const void *X, int64_t ldx, i
     a.cvt_n = 0;
     a.cvt_frag_E = 0;
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcArgs);
-    if (out == TcType::F32) kern = in_bf16 ? k_gemm_tc<__nv_bfloat16, float> : k_gemm_tc<__half, float>;
-    else if (in_bf16) kern = out == TcType::F16 ? k_gemm_tc<__nv_bfloat16, __half> : k_gemm_tc<__nv_bfloat16, __nv_bfloat16>;
-    else kern = out == TcType::BF16 ? k_gemm_tc<__half, __nv_bfloat16> : k_gemm_tc<__half, __half>;
+    if (out == TcType::F32) kern = in_bf16 ? k_gemm_tc<__nv_bfloat16, float, BN> : k_gemm_tc<__half, float, BN>;
+    else if (in_bf16)
+        kern = out == TcType::F16 ? k_gemm_tc<__nv_bfloat16, __half, BN> : k_gemm_tc<__nv_bfloat16, __nv_bfloat16, BN>;
+    else kern = out == TcType::BF16 ? k_gemm_tc<__half, __nv_bfloat16, BN> : k_gemm_tc<__half, __half, BN>;
     static std::mutex mu;
     static std::set<std::pair<int, void *>> configured;
     int dev = 0;
@@ -604,14 +676,14 @@ pmha_status gemm_tc_general(TcType in, TcType out, const void *X, int64_t ldx, i
     {
         std::lock_guard<std::mutex> lk(mu);
         if (!configured.count({dev, (void *)kern})) {
-            PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
+            PMHA_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tile<BN>::kSmem));
             configured.insert({dev, (void *)kern});
         }
     }
     const int n_tiles = (int)(((M + BM - 1) / BM) * (N / BN) * ksplit);
     const int grid = std::min(n_tiles, num_sms());
     StageTimer timer(stage, stream);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw, mw, mw, my, a);
+    kern<<<grid, kThreads, Tile<BN>::kSmem, stream>>>(mx, mw, mw, mw, my, a);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;
