@@ -311,7 +311,7 @@ template <typename K>
 __global__ void k_check_and_view(const K *__restrict__ keys, const int *__restrict__ vals,
                                  int64_t S, Summary *__restrict__ sum, int32_t *__restrict__ col,
                                  int32_t *__restrict__ perm, int32_t *__restrict__ tgt_of_edge,
-                                 int32_t *__restrict__ inv_perm)
+                                 int32_t *__restrict__ tgt_of_pos)
 {
     const int n = sum->nnz_total;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -322,7 +322,7 @@ __global__ void k_check_and_view(const K *__restrict__ keys, const int *__restri
     col[i] = (int32_t)((int64_t)k - t * S);
     perm[i] = vals[i];
     tgt_of_edge[vals[i]] = (int32_t)t;
-    inv_perm[vals[i]] = i;
+    tgt_of_pos[i] = (int32_t)t;
 }
 
 // Adjacency bits of a dense graph: block t sets bit s of row t for every
@@ -549,7 +549,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
     g->col = (int32_t *)(gm + off_col);
     g->perm = (int32_t *)(gm + off_perm);
     g->tgt_of_edge = (int32_t *)(gm + off_tge);
-    g->inv_perm = (int32_t *)(gm + off_inv);
+    g->tgt_of_pos = (int32_t *)(gm + off_inv);
     g->unit_first_t = (int32_t *)(gm + off_units);
     g->unit_order = (int32_t *)(gm + off_order);
     g->merge_t = (int32_t *)(gm + off_merge);
@@ -592,7 +592,7 @@ pmha_status build_typed(const int64_t *src, const int64_t *tgt, int64_t nnz64, i
         int *vals_s;
         radix_sort<K>(keys_a, vals_a, keys_b, vals_b, cap, bits, hist, scan_tmp, stream, &keys_s, &vals_s);
         k_check_and_view<K><<<blocks_for(cap, TB), TB, 0, stream>>>(keys_s, vals_s, S, dsum, g->col, g->perm,
-                                                                    g->tgt_of_edge, g->inv_perm);
+                                                                    g->tgt_of_edge, g->tgt_of_pos);
         k_row_ptr<K><<<blocks_for(L + 1, TB), TB, 0, stream>>>(keys_s, dsum, L, S, g->row_ptr);
         k_unit_first<<<blocks_for(max_units, TB), TB, 0, stream>>>(g->row_ptr, (int)L, dsum, g->unit_first_t);
         k_merge_flags<<<blocks_for(L, TB), TB, 0, stream>>>(g->row_ptr, (int)L, c1, dsum);

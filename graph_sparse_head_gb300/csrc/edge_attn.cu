@@ -80,17 +80,21 @@ __device__ __forceinline__ float edge_weight(float s, float m, float l)
     return (l == 0.f || s == -INFINITY) ? 0.f : __fmul_rn(ex2(__fsub_rn(s, m)), __frcp_rn(l));
 }
 
+// The edges are walked in CSR order, so the scores (written at CSR positions
+// by the edge kernel) and the targets' (m, l) are read in sequence; each
+// weight goes to its given-order place (the averaged weights, 4 bytes an
+// edge, are a small array that stays in L2 while it fills).
 template <int HC>
 __global__ void __launch_bounds__(256) k_weights(const float *__restrict__ scores, const float *__restrict__ ml,
-                                                 const int32_t *__restrict__ tgt_of_edge,
-                                                 const int32_t *__restrict__ inv_perm, long long B, long long nnz,
+                                                 const int32_t *__restrict__ tgt_of_pos,
+                                                 const int32_t *__restrict__ perm, long long B, long long nnz,
                                                  int L, int H_rt, bool average, float *out)
 {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= B * nnz) return;
-    const long long b = i / nnz, e = i - b * nnz;
-    const int t = __ldg(tgt_of_edge + e);
-    const long long si = b * nnz + __ldg(inv_perm + e);  // the edge's scores sit at its CSR position
+    const long long si = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (sample, CSR position)
+    if (si >= B * nnz) return;
+    const long long b = si / nnz, p = si - b * nnz;
+    const int t = __ldg(tgt_of_pos + p);
+    const long long i = b * nnz + __ldg(perm + p);  // (sample, given-order edge id)
     if constexpr (HC > 0) {
         static_assert(HC % 4 == 0, "16-byte loads of the scores");
         float s[HC], st[2 * HC];
@@ -292,13 +296,13 @@ pmha_status weights_finalize(const pmha_graph *g, const EdgeArgs &a, pmha_wmode 
     const bool vec = ((uintptr_t)a.scores % 16 == 0) && ((uintptr_t)a.ml % 16 == 0) &&
                      (avg || (uintptr_t)out % 16 == 0);
     if (vec && a.H == 8)
-        k_weights<8><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, 8, avg, out);
+        k_weights<8><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_pos, g->perm, a.B, g->nnz, (int)g->L, 8, avg, out);
     else if (vec && a.H == 4)
-        k_weights<4><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, 4, avg, out);
+        k_weights<4><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_pos, g->perm, a.B, g->nnz, (int)g->L, 4, avg, out);
     else if (vec && a.H == 16)
-        k_weights<16><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, 16, avg, out);
+        k_weights<16><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_pos, g->perm, a.B, g->nnz, (int)g->L, 16, avg, out);
     else
-        k_weights<0><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_edge, g->inv_perm, a.B, g->nnz, (int)g->L, (int)a.H, avg,
+        k_weights<0><<<blocks, TB, 0, s>>>(a.scores, a.ml, g->tgt_of_pos, g->perm, a.B, g->nnz, (int)g->L, (int)a.H, avg,
                                            out);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());

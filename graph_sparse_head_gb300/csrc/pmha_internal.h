@@ -41,7 +41,7 @@ struct pmha_graph {
     int32_t *col = nullptr;           // nnz, source per CSR position
     int32_t *perm = nullptr;          // nnz, given-order edge id per CSR position
     int32_t *tgt_of_edge = nullptr;   // nnz, target per given-order edge id
-    int32_t *inv_perm = nullptr;      // nnz, CSR position per given-order edge id
+    int32_t *tgt_of_pos = nullptr;    // nnz, target per CSR position
     int32_t *unit_first_t = nullptr;  // n_units, target of each unit's first position
     int32_t *unit_order = nullptr;    // n_units, the units by decreasing estimated work (ties by index)
     int32_t *merge_t = nullptr;       // n_merge, targets to merge (crossing a unit boundary, or without edges)
