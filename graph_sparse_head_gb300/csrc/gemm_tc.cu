@@ -21,6 +21,9 @@
 //             32*(w%4) .. +31), + bias (staged in shared memory once per
 //             tile), rounded to the output type, written to a
 //             128-byte-swizzled shared tile that one thread stores with TMA
+// Layers with E a multiple of 256 use 128 x 256 tiles instead (W tile
+// 256 x 64, a 3-stage ring, 512 TMEM columns): both epilogue groups drain
+// every tile, group g columns 128 g .. 128 g + 127.
 // Tiles are visited m-major with the N tiles of one row block adjacent, so
 // CTAs that share an X tile run together and the re-reads hit L2.
 //
@@ -64,22 +67,24 @@ constexpr int kThreads = 64 + 128 * kEpi;
 constexpr int kOutBoxBytes = BM * 128;             // 128 rows x 64 16-bit columns, 128-byte swizzle
 constexpr int kOutTileBytes = 2 * kOutBoxBytes;     // one 128 x 128 output tile
 
-// Tile width WN: 128 columns (BN), or 256 for the wide layers. A tensor-bound
-// tile waits for its operands, which reach shared memory at about 95 GB/s
-// per SM (a 128 x 128 x 16 MMA itself takes 65 cycles when its operands are
-// in place); a 256-column tile reads 25 % fewer operand bytes per output.
-// Wide tiles hold four 48 KB stages and store their output straight from
-// registers (16-byte stores, each thread a row).
+// Tile width WN: 128 columns (BN), or 256 for the wide layers. A tile whose
+// operands dominate its traffic waits for them: they reach shared memory at
+// about 95 GB/s per SM (a 128 x 128 x 16 MMA itself takes 65 cycles when its
+// operands are in place), and a 256-column tile reads 25 % fewer operand
+// bytes per output. Wide tiles hold three 48 KB stages; both epilogue
+// groups drain every wide tile, group g its columns 128 g .. 128 g + 127,
+// through its own staging tile and TMA store.
 template <int WN>
 struct Tile {
     static_assert(WN == 128 || WN == 256, "128- or 256-column tiles");
-    static constexpr bool kDirect = WN > BN;  // epilogue stores from registers, no staging tile
-    static constexpr int kStages = kDirect ? 4 : ::pmha::kStages;
+    static constexpr bool kSplit = WN > BN;  // every epilogue group takes 128 columns of every tile
+    static_assert(!kSplit || kEpi == WN / BN, "one epilogue group per 128 columns of a wide tile");
+    static constexpr int kStages = kSplit ? 3 : ::pmha::kStages;
     static constexpr int kTileB = WN * BK * 2;
     static constexpr int kStage = kTileABytes + kTileB;
-    static constexpr int kBufs = kDirect ? 0 : (kEpi == 1 ? 2 : kEpi);  // staging tiles
+    static constexpr int kBufs = kEpi == 1 ? 2 : kEpi;                 // staging tiles
     static constexpr int kTmemCols = kAcc * WN <= 256 ? 256 : 512;      // a power of two
-    static constexpr int kBias = kEpi * WN * 4;                         // fp32 bias of the tile, per group
+    static constexpr int kBias = kEpi * BN * 4;                         // fp32 bias of 128 columns, per group
     static constexpr int kSmem = kStages * kStage + kBufs * kOutTileBytes + kBias + 1024 /*align*/ + 256 /*barriers*/;
     static_assert(kAcc * WN <= 512, "the accumulators fit in tensor memory");
     static_assert(kSmem <= 232448, "shared memory of one CTA");
@@ -171,7 +176,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *tiles = smem;
     uint8_t *staging = smem + kStages * kStageBytes;  // output staging tiles (none for wide tiles)
-    float *bias_s = (float *)(staging + kBufs * kOutTileBytes);  // [kEpi][WN]
+    float *bias_s = (float *)(staging + kBufs * kOutTileBytes);  // [kEpi][BN]
     uint64_t *bars = (uint64_t *)(staging + kBufs * kOutTileBytes + kBiasBytes);
     uint64_t *full = bars;                    // [kStages]
     uint64_t *empty = bars + kStages;         // [kStages]
@@ -204,7 +209,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(smem_u32(&acc_full[i]), 1);
-            mbar_init(smem_u32(&acc_empty[i]), 128);
+            mbar_init(smem_u32(&acc_empty[i]), 128 * (WN / BN));  // every group that drains the accumulator
         }
         mbar_init(smem_u32(mma_done), 1);
         *abort_flag = 0;
@@ -307,7 +312,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
         const int g = (warp - 2) >> 2;          // epilogue group
         const int et = threadIdx.x - 64 - 128 * g;  // 0..127 within the group
         const int r = quarter * 32 + lane;  // tile row of this thread
-        float *bias_g = bias_s + g * WN;
+        float *bias_g = bias_s + g * BN;  // the group's 128 columns of bias
         {
             // Side job before the first accumulator is ready: this CTA's share
             // of the bf16 -> fp16 copy, 8 values (one 16-byte load) a thread
@@ -346,7 +351,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             }
             if (bad) atomicOr(a.err, kErrRangeBit);
         }
-        for (int i = g;; i += kEpi) {
+        // narrow tiles alternate between the groups; a wide tile goes to both
+        const int cg = TL::kSplit ? g * BN : 0;  // the group's first column in the tile
+        for (int i = TL::kSplit ? 0 : g;; i += TL::kSplit ? 1 : kEpi) {
             const int tile = blockIdx.x + i * gridDim.x;
             if (tile >= n_tiles) break;
             const int acc = i % kAcc;
@@ -358,25 +365,19 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             const int seg = n_glob / a.E;
             const int n_loc = n_glob - seg * a.E;
             const __nv_bfloat16 *bias = a.bias[seg];
-            // this thread's bias values, loaded before the accumulator wait so
-            // that the wait covers the loads
-            float bias_v[WN / 128] = {};
+            // this thread's bias value (column cg + et of the tile), loaded
+            // before the accumulator wait so that the wait covers the load
+            float bias_v = 0.f;
             if constexpr (!std::is_same<TOut, float>::value)
-                if (bias)
-#pragma unroll
-                    for (int j = 0; j < WN / 128; ++j) bias_v[j] = __bfloat162float(bias[n_loc + et + 128 * j]);
+                if (bias) bias_v = __bfloat162float(bias[n_loc + cg + et]);
             const bool ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.err);
             // the store that last read this group's staging tile is done
-            if constexpr (!TL::kDirect) {
-                if (et == 0) {
-                    if constexpr (kEpi >= 2) bulk_wait_read0();
-                    else bulk_wait_read1();
-                }
+            if (et == 0) {
+                if constexpr (kEpi >= 2) bulk_wait_read0();
+                else bulk_wait_read1();
             }
-            // the readers of the previous tile's bias passed a barrier of the group since
-            if constexpr (!std::is_same<TOut, float>::value)
-#pragma unroll
-                for (int j = 0; j < WN / 128; ++j) bias_g[et + 128 * j] = bias_v[j];
+            // the readers of the previous tile's bias passed the barrier before its store
+            if constexpr (!std::is_same<TOut, float>::value) bias_g[et] = bias_v;
             if (epi_sync_or(g, !ok)) break;  // one decision for all 128 threads
             tc_fence_after();
             const bool live = m_blk * BM + r < a.M;
@@ -398,40 +399,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                 tc_fence_before();
                 mbar_arrive(smem_u32(&acc_empty[acc]));
                 continue;
-            } else if constexpr (TL::kDirect) {
-                // wide tile: + bias, rounded, stored from registers (64 bytes of
-                // this thread's row per 32 columns, whole 32-byte sectors)
-                uint8_t *dst = (uint8_t *)a.out + ((long long)(m_blk * BM + r) * a.ldy + n_glob) * 2;
-                bool range_bad = false;
-                const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * WN);
-#pragma unroll 1
-                for (int c = 0; c < WN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(t_row + (uint32_t)(c * 32), v);
-                    uint32_t packed[16];
-                    bool bad = false;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float v0 = __uint_as_float(v[2 * j]), v1 = __uint_as_float(v[2 * j + 1]);
-                        if (bias) {
-                            const float2 bb = *reinterpret_cast<const float2 *>(bias_g + c * 32 + 2 * j);
-                            v0 = __fadd_rn(v0, bb.x);
-                            v1 = __fadd_rn(v1, bb.y);
-                        }
-                        packed[j] = pack2<TOut>(v0, v1, bad);
-                    }
-                    range_bad |= bad && live;
-                    if (live) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4 *>(dst + c * 64 + 16 * q) =
-                                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                    }
-                }
-                if (range_bad) atomicOr(a.err, kErrRangeBit);
-                tc_fence_before();
-                mbar_arrive(smem_u32(&acc_empty[acc]));
-                epi_sync(g);  // every thread is done with this tile's bias
             } else {
             uint8_t *sb = staging + buf * kOutTileBytes;
             bool range_bad = false;
@@ -459,9 +426,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
                         make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                 }
             };
-            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * WN);
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * WN + cg);
 #pragma unroll 1
-            for (int c = 0; c < WN / 32; ++c) {
+            for (int c = 0; c < BN / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(t_row + (uint32_t)(c * 32), v);
                 emit(c, v);
@@ -474,8 +441,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUte
             fence_async_shared();
             epi_sync(g);
             if (et == 0) {
-                tma_store_2d(&tm_y, smem_u32(sb), n_glob, m_blk * BM);
-                tma_store_2d(&tm_y, smem_u32(sb + kOutBoxBytes), n_glob + 64, m_blk * BM);
+                tma_store_2d(&tm_y, smem_u32(sb), n_glob + cg, m_blk * BM);
+                tma_store_2d(&tm_y, smem_u32(sb + kOutBoxBytes), n_glob + cg + 64, m_blk * BM);
                 bulk_commit();
             }
             }  // 16-bit output
@@ -528,12 +495,8 @@ pmha_status gemm_tc(TcType in, TcType out, const void *X, int64_t M, int64_t E, 
         return PMHA_ERR_INVALID_ARG;
     }
     const bool in_bf16 = in == TcType::BF16;
-    // 256-column tiles where the GEMM is bound by its operands rather than its
-    // output: E >= 512 (complete-graph layer: q|k|v 28.7 -> 27.2 us). At
-    // E = 256 the output-heavy k|v projection was slower with them (479.9 ->
-    // 561.5 us): the register stores of the wide epilogue cost more there than
-    // the operand bytes they save.
-    const bool wide = E % 256 == 0 && E >= 512;
+    // 256-column tiles where every tile lies inside one weight matrix
+    const bool wide = E % 256 == 0;
     CUtensorMap mx, mw[3];
     if (!make_map(&mx, X, M, E, in_bf16)) {
         set_error("gemm_tc: cuTensorMapEncodeTiled failed for X (pointer %p)", X);
