@@ -619,8 +619,18 @@ __global__ void k_sum_chunks(const float *__restrict__ P, long long n, int chunk
 {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
+    // chunk order 0, 1, 2, ...; sixteen loads in flight at a time (one dependent
+    // load per chunk made this pass a chain of L2 round trips)
     float acc = 0.f;
-    for (int c = 0; c < chunks; ++c) acc = __fadd_rn(acc, P[(long long)c * n + i]);
+    int c = 0;
+    for (; c + 16 <= chunks; c += 16) {
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = P[(long long)(c + q) * n + i];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc = __fadd_rn(acc, v[q]);
+    }
+    for (; c < chunks; ++c) acc = __fadd_rn(acc, P[(long long)c * n + i]);
     out[i] = acc;
 }
 
@@ -638,7 +648,8 @@ __global__ void k_convert(const float *__restrict__ in, long long n, TO *__restr
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(256) k_transpose_cvt(const TIn *__restrict__ in, long long ld_in, long long M, int E,
                                                        long long Mpad, TOut *__restrict__ out, long long ld_out,
-                                                       float *__restrict__ colsum)
+                                                       float *__restrict__ colsum, __half *__restrict__ rows16,
+                                                       long long ld16)
 {
     __shared__ float tile[64][65];
     const long long r0 = (long long)blockIdx.x * 64;
@@ -648,7 +659,10 @@ __global__ void __launch_bounds__(256) k_transpose_cvt(const TIn *__restrict__ i
     for (int k = 0; k < 16; ++k) {
         const int rr = hi + 4 * k;
         const long long r = r0 + rr;
-        tile[rr][lo] = (r < M && c0 + lo < E) ? to_f(in[r * ld_in + c0 + lo]) : 0.f;
+        const float v = (r < M && c0 + lo < E) ? to_f(in[r * ld_in + c0 + lo]) : 0.f;
+        tile[rr][lo] = v;
+        // with rows16: the same rows in fp16, untransposed (pitch ld16)
+        if (rows16 && r < M && c0 + lo < E) rows16[r * ld16 + c0 + lo] = __float2half_rn(v);
     }
     __syncthreads();
     if (colsum && threadIdx.x < 64 && c0 + threadIdx.x < E) {
@@ -937,12 +951,12 @@ struct Bump {
 
 template <typename TIn, typename TOut>
 void transpose_cvt(const void *in, int64_t ld_in, int64_t M, int64_t E, int64_t Mpad, void *out, int64_t ld_out,
-                   cudaStream_t s, float *colsum = nullptr)
+                   cudaStream_t s, float *colsum = nullptr, __half *rows16 = nullptr, int64_t ld16 = 0)
 {
     StageTimer timer("bwd_transpose", s);
     dim3 grid(blocks(Mpad, 64), blocks(E, 64));
     k_transpose_cvt<TIn, TOut><<<grid, 256, 0, s>>>((const TIn *)in, ld_in, M, (int)E, Mpad, (TOut *)out, ld_out,
-                                                    colsum);
+                                                    colsum, rows16, ld16);
     count_launch();
 }
 
@@ -1074,12 +1088,38 @@ pmha_status bwd_step1(const BwdGemmArgs &g, cudaStream_t s)
     __half *dy16 = bump.take<__half>((size_t)(std::max(rows[0], rows[1]) * 3 * E));
     float *part = bump.take<float>((size_t)(kMaxSplit * E * E));
     float *cs = bump.take<float>((size_t)(Mp / 64 * E));
+    // The input gradient of each input (below) is one product over the roles it
+    // feeds, with their dY rows side by side in fp16: the roles of input group
+    // lead (its first role) fill a region of dy16 of rows x (n_roles E), slot
+    // i of role i of the group. Regions of different inputs do not overlap.
+    __half *pack16[3] = {nullptr, nullptr, nullptr};  // where role r's fp16 dY rows go (null: no input gradient)
+    int64_t pack_ld[3] = {0, 0, 0};
+    {
+        int64_t off = 0;
+        for (int r = 0; r < 3; ++r) {
+            bool seen = false;
+            for (int q = 0; q < r; ++q) seen |= g.in[q] == g.in[r];
+            if (seen || !g.gx[r]) continue;
+            int nr = 0;
+            for (int q = r; q < 3; ++q) nr += g.in[q] == g.in[r];
+            for (int q = r, i = 0; q < 3; ++q)
+                if (g.in[q] == g.in[r]) {
+                    pack16[q] = dy16 + off + i++ * E;
+                    pack_ld[q] = nr * E;
+                }
+            off += rows[r] * nr * E;
+        }
+    }
+    bool packed[3] = {false, false, false};
     // weight gradients dW_r = dY_r^T X_r: both transposed to fp16 (tokens along K);
-    // the bias gradient (column sums of dY_r) comes out of the same transpose
+    // the bias gradient (column sums of dY_r) comes out of the same transpose, and
+    // so do dY_r's fp16 rows for the input gradient
     for (int r = 0; r < 3; ++r) {
         if (!g.gw[r] && !g.gb[r]) continue;
         const int64_t mp = pad64(rows[r]);
-        transpose_cvt<float, __half>(g.dy[r], E, rows[r], E, mp, dyT[r], mp, s, g.gb[r] ? cs : nullptr);
+        transpose_cvt<float, __half>(g.dy[r], E, rows[r], E, mp, dyT[r], mp, s, g.gb[r] ? cs : nullptr, pack16[r],
+                                     pack_ld[r]);
+        packed[r] = pack16[r] != nullptr;
         if (g.gb[r]) bias_from_tiles(cs, rows[r], E, g.gb[r], s);
         if (!g.gw[r]) continue;
         int src = r;
@@ -1102,15 +1142,15 @@ pmha_status bwd_step1(const BwdGemmArgs &g, cudaStream_t s)
         const int64_t K = nr * E;
         for (int i = 0; i < nr; ++i) {
             const int q = roles[i];
-            {
+            if (!packed[q]) {
                 StageTimer pack_timer("bwd_pack", s);
-                k_rows_f16<<<blocks(rows[r] * E / 4, 256), 256, 0, s>>>(g.dy[q], rows[r], (int)E, dy16 + i * E, K);
+                k_rows_f16<<<blocks(rows[r] * E / 4, 256), 256, 0, s>>>(g.dy[q], rows[r], (int)E, pack16[q], K);
                 count_launch();
             }
             transpose_cvt<__nv_bfloat16, __half>(g.w[q], E, E, E, E, wsub + i * E, K, s);
         }
-        if ((st = gemm_tc_general(TcType::F16, g.pt, dy16, K, rows[r], K, wsub, K, E, g.gx[r], E, 1, "bwd_dx", s)) !=
-            PMHA_OK)
+        if ((st = gemm_tc_general(TcType::F16, g.pt, pack16[r], K, rows[r], K, wsub, K, E, g.gx[r], E, 1, "bwd_dx",
+                                  s)) != PMHA_OK)
             return st;
     }
     PMHA_CUDA_TRY(cudaGetLastError());
