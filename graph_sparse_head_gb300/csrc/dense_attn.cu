@@ -155,7 +155,7 @@ __device__ __forceinline__ float ex2_fma(float x)
 #define PMHA_DENSE_EMU_PAIRS 0
 #endif
 constexpr int kEmuPairs = PMHA_DENSE_EMU_PAIRS;
-static_assert(kEmuPairs == 0 || (16 % kEmuPairs == 0), "an even spread of emulated pairs");
+static_assert(kEmuPairs == 0 || (16 % (kEmuPairs > 0 ? kEmuPairs : 1) == 0), "an even spread of emulated pairs");
 __device__ __forceinline__ constexpr bool emulated_pair(int i)
 {
     return kEmuPairs > 0 && (i % (16 / (kEmuPairs > 0 ? kEmuPairs : 1))) == (16 / (kEmuPairs > 0 ? kEmuPairs : 1)) - 1;
