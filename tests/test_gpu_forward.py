@@ -58,9 +58,10 @@ def test_forward_shapes_and_dtypes(L, S, nnz, E, H, B, dt, bip):
     g.destroy()
 
 
-def test_key_differs_from_value_and_no_bias():
+@pytest.mark.parametrize("E", [128, 256, 512])  # 256, 512: the 128 x 256 projection tiles, without bias
+def test_key_differs_from_value_and_no_bias(E):
     rng = np.random.default_rng(3)
-    L, S, E, H, B = 300, 500, 128, 8, 2
+    L, S, H, B = 300, 500, 8, 2
     src, tgt = synth.bipartite_membership_graph(rng, L, S, 5, 60)
     c = Case(src, tgt, L, S, E, H, B, "bf16", seed=4, bipartite=True, bias=False)
     xv = synth.make_tokens(rng, B, S, E, "bf16")
