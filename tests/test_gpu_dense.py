@@ -117,3 +117,37 @@ def test_sparse_graph_stays_on_the_edge_kernel():
     (g, params, out, w), stages = _stages_of(lambda: c.run(DEV, "none"))
     assert ("edge_attn" in stages or "edge_attn_out" in stages) and "dense_attn" not in stages
     g.destroy()
+
+
+def test_dense_reference_moves_after_the_first_step():
+    # Keys scaled by 1, 3, 1 and 5 in consecutive blocks of 128 sources (the
+    # dense kernel's steps): in the second and last steps about 40 % of the
+    # rows' maxima pass the running softmax reference by more than its lazy
+    # threshold and the others do not, so warps rescale O and l for some rows
+    # and keep them for the rest; scores reach about 34 log2 units.
+    from tests._cases import score_bound
+    rng = np.random.default_rng(21)
+    L, S, E, H, B = 256, 512, 256, 4, 2
+    src, tgt = _dense_pairs(rng, L, S, 1.1)
+    xq = synth.make_tokens(rng, B, L, E, "bf16")
+    gain = np.repeat(np.array([1.0, 3.0, 1.0, 5.0], np.float32), 128)
+    xkv = synth.bf16_round(synth.make_tokens(rng, B, S, E, "bf16") * gain[None, :, None])
+    c = Case(src, tgt, L, S, E, H, B, "bf16", seed=22, bipartite=True, xq=xq, xkv=xkv)
+    # the moves are real: per (sample, head, target), the step maxima in log2 units
+    d = E // H
+    moved = []
+    for b in range(B):
+        q = oracle.linear(c.xq[b], c.params["wq"], c.params["bq"]).reshape(L, H, d)
+        k = oracle.linear(c.xkv[b], c.params["wk"], c.params["bk"]).reshape(S, H, d)
+        s = np.einsum("thc,shc->hts", q, k) * (1.4426950408889634 / np.sqrt(d))
+        step_max = s.reshape(H, L, 4, 128).max(axis=3)
+        run = np.maximum.accumulate(step_max, axis=2)
+        moved.append(step_max[:, :, 1:] > run[:, :, :-1] + 8.0)
+    moved = np.stack(moved)
+    assert 0.1 < moved[..., 0].mean() < 0.9 and 0.1 < moved[..., 2].mean() < 0.9, moved.mean(axis=(0, 1, 2))
+    (g, params, out, w), stages = _stages_of(lambda: c.run(DEV, "per_head"))
+    assert "dense_attn" in stages
+    ref_out, ref_w = c.oracle()
+    assert_close("output", out.float().cpu().numpy(), ref_out, "bf16")
+    assert_close_weights("weights", w.cpu().numpy(), ref_w, "bf16", score_bound=score_bound(c))
+    g.destroy()
