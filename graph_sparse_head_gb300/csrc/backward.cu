@@ -470,17 +470,34 @@ __global__ void __launch_bounds__(256) k_bwd_merge(const int32_t *__restrict__ m
     const int r = merge_rows[gw - (long long)b * n_merge];
     const int beg = row_ptr[r], end = row_ptr[r + 1];
     const float *base = part + (long long)b * 2 * n_units * W;
+    const int u0 = beg / kUnitEdges, n_pc = end > beg ? (end - 1) / kUnitEdges - u0 + 1 : 0;
+    const int first_slot = 2 * u0 + (beg != u0 * kUnitEdges ? 1 : 0);  // piece 0; piece i > 0 is slot 2 (u0 + i)
+    float *o0 = out0 + ((long long)b * n_rows + r) * E;
+    float *o1 = out1 ? out1 + ((long long)b * n_rows + r) * E : nullptr;  // column c >= E goes to o1[c - E]
+    if ((E & 3) == 0) {
+        // four columns a lane (16-byte loads and stores; a group of four never straddles E)
+        for (int c = 4 * lane; c < W; c += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int i = 0; i < n_pc; ++i) {
+                const int slot = i == 0 ? first_slot : 2 * (u0 + i);
+                const float4 v = *reinterpret_cast<const float4 *>(base + (long long)slot * W + c);
+                acc.x = __fadd_rn(acc.x, v.x);
+                acc.y = __fadd_rn(acc.y, v.y);
+                acc.z = __fadd_rn(acc.z, v.z);
+                acc.w = __fadd_rn(acc.w, v.w);
+            }
+            *reinterpret_cast<float4 *>(c < E ? o0 + c : o1 + (c - E)) = acc;
+        }
+        return;
+    }
     for (int c = lane; c < W; c += 32) {
         float acc = 0.f;
-        if (end > beg) {
-            const int u0 = beg / kUnitEdges, u1 = (end - 1) / kUnitEdges;
-            for (int i = 0; i <= u1 - u0; ++i) {
-                const int slot = 2 * (u0 + i) + ((i == 0 && beg != u0 * kUnitEdges) ? 1 : 0);
-                acc = __fadd_rn(acc, base[(long long)slot * W + c]);
-            }
+        for (int i = 0; i < n_pc; ++i) {
+            const int slot = i == 0 ? first_slot : 2 * (u0 + i);
+            acc = __fadd_rn(acc, base[(long long)slot * W + c]);
         }
-        float *o = c < E ? out0 + ((long long)b * n_rows + r) * E + c : out1 + ((long long)b * n_rows + r) * E + c - E;
-        *o = acc;
+        *(c < E ? o0 + c : o1 + (c - E)) = acc;
     }
 }
 
@@ -614,24 +631,39 @@ __global__ void __launch_bounds__(256) k_sum_tiles(const float *__restrict__ P, 
     if (threadIdx.x == 0) out[c] = red[0];
 }
 
-// out[i] = sum over chunks of P[chunk][i], in chunk order
-__global__ void k_sum_chunks(const float *__restrict__ P, long long n, int chunks, float *__restrict__ out)
+// out[i] = sum over chunks of P[chunk][i], in a fixed order
+__global__ void __launch_bounds__(256) k_sum_chunks(const float *__restrict__ P, long long n, int chunks,
+                                                    float *__restrict__ out)
 {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    // chunk order 0, 1, 2, ...; sixteen loads in flight at a time (one dependent
-    // load per chunk made this pass a chain of L2 round trips)
+    // out[i] = sum over c of P[c * n + i]. Eight warps share 32 consecutive
+    // outputs: warp g adds the g-th eighth of the chunks in chunk order
+    // (sixteen loads in flight at a time), then warp 0 adds the eight sums in
+    // order. A fixed order, so the result is deterministic; a single thread
+    // per output made this pass a chain of dependent L2 round trips.
+    __shared__ float part[8][32];
+    const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const long long i = (long long)blockIdx.x * 32 + lane;
+    const int per = (chunks + 7) / 8, c_lo = min(chunks, g * per), c_hi = min(chunks, c_lo + per);
     float acc = 0.f;
-    int c = 0;
-    for (; c + 16 <= chunks; c += 16) {
-        float v[16];
+    if (i < n) {
+        int c = c_lo;
+        for (; c + 16 <= c_hi; c += 16) {
+            float v[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) v[q] = P[(long long)(c + q) * n + i];
+            for (int q = 0; q < 16; ++q) v[q] = P[(long long)(c + q) * n + i];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) acc = __fadd_rn(acc, v[q]);
+            for (int q = 0; q < 16; ++q) acc = __fadd_rn(acc, v[q]);
+        }
+        for (; c < c_hi; ++c) acc = __fadd_rn(acc, P[(long long)c * n + i]);
     }
-    for (; c < chunks; ++c) acc = __fadd_rn(acc, P[(long long)c * n + i]);
-    out[i] = acc;
+    part[g][lane] = acc;
+    __syncthreads();
+    if (g == 0 && i < n) {
+        float t = part[0][lane];
+#pragma unroll
+        for (int q = 1; q < 8; ++q) t = __fadd_rn(t, part[q][lane]);
+        out[i] = t;
+    }
 }
 
 template <typename TO>
@@ -641,40 +673,88 @@ __global__ void k_convert(const float *__restrict__ in, long long n, TO *__restr
     if (i < n) out[i] = from_f<TO>(in[i]);
 }
 
-// out[c * ld_out + r] = in[r * ld_in + c] for r < M, c < E (converted); the
-// columns r in [M, Mpad) of out are zero. 64 x 64 tiles.
+// out[c * ld_out + r] = in[r * ld_in + c] for r < M, c < E (converted to a
+// 16-bit type); the columns r in [M, Mpad) of out are zero. 64 x 64 tiles
+// through shared memory, 16-byte global loads and stores: a thread loads
+// 16-byte pieces of input rows and stores 8 consecutive r of one output row.
 // With colsum non-null, also writes the tile's 64-row column sums of the
-// input (in row order) to colsum[blockIdx.x * E + c].
+// input (in row order) to colsum[blockIdx.x * E + c]. With rows16 non-null,
+// also writes the input rows in fp16, untransposed (pitch ld16).
+// Shapes (checked by transpose_cvt): E and Mpad multiples of 64; ld_in,
+// ld_out and ld16 multiples of 8 elements; every pointer 16-byte aligned.
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(256) k_transpose_cvt(const TIn *__restrict__ in, long long ld_in, long long M, int E,
                                                        long long Mpad, TOut *__restrict__ out, long long ld_out,
                                                        float *__restrict__ colsum, __half *__restrict__ rows16,
                                                        long long ld16)
 {
+    static_assert(sizeof(TOut) == 2, "16-bit outputs");
+    constexpr int V = 16 / (int)sizeof(TIn);  // elements per 16-byte load: 4 (fp32) or 8
+    constexpr int TPR = 64 / V;              // threads per tile row
+    constexpr int RPP = 256 / TPR;           // tile rows per pass
+    constexpr int NP = 64 / RPP;             // passes
     __shared__ float tile[64][65];
     const long long r0 = (long long)blockIdx.x * 64;
     const int c0 = blockIdx.y * 64;
-    const int lo = threadIdx.x & 63, hi = threadIdx.x >> 6;
-#pragma unroll 4
-    for (int k = 0; k < 16; ++k) {
-        const int rr = hi + 4 * k;
-        const long long r = r0 + rr;
-        const float v = (r < M && c0 + lo < E) ? to_f(in[r * ld_in + c0 + lo]) : 0.f;
-        tile[rr][lo] = v;
-        // with rows16: the same rows in fp16, untransposed (pitch ld16)
-        if (rows16 && r < M && c0 + lo < E) rows16[r * ld16 + c0 + lo] = __float2half_rn(v);
+    const int cl = (threadIdx.x % TPR) * V, rl = threadIdx.x / TPR;
+    uint4 raw[NP];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {  // every load in flight before the first use
+        const long long r = r0 + rl + k * RPP;
+        raw[k] = r < M ? *reinterpret_cast<const uint4 *>(in + r * ld_in + c0 + cl) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        const int rr = rl + k * RPP;
+        const TIn *x = reinterpret_cast<const TIn *>(&raw[k]);
+        float v[V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            v[j] = to_f(x[j]);
+            tile[rr][cl + j] = v[j];
+        }
+        if (rows16 && r0 + rr < M) {
+            __half *dst = rows16 + (r0 + rr) * ld16 + c0 + cl;
+            if constexpr (V == 8) {
+                uint4 w;
+                uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __half2 h = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+                    wp[j] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+                *reinterpret_cast<uint4 *>(dst) = w;
+            } else {
+                uint2 w;
+                const __half2 a = __floats2half2_rn(v[0], v[1]), b = __floats2half2_rn(v[2], v[3]);
+                w.x = *reinterpret_cast<const uint32_t *>(&a);
+                w.y = *reinterpret_cast<const uint32_t *>(&b);
+                *reinterpret_cast<uint2 *>(dst) = w;
+            }
+        }
     }
     __syncthreads();
-    if (colsum && threadIdx.x < 64 && c0 + threadIdx.x < E) {
+    if (colsum && threadIdx.x < 64) {
         float acc = 0.f;
         for (int rr = 0; rr < 64; ++rr) acc = __fadd_rn(acc, tile[rr][threadIdx.x]);
         colsum[(long long)blockIdx.x * E + c0 + threadIdx.x] = acc;
     }
-#pragma unroll 4
-    for (int k = 0; k < 16; ++k) {
-        const int cc = hi + 4 * k;
-        const long long r = r0 + lo;
-        if (c0 + cc < E && r < Mpad) out[(long long)(c0 + cc) * ld_out + r] = from_f<TOut>(tile[lo][cc]);
+    // output row c0 + cc, tile rows 8 seg .. 8 seg + 7: a warp takes 8 columns
+    // x 4 segments (shared-memory banks (8 seg + cc + i) mod 32 all differ)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cc = warp * 8 + (lane >> 2);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int seg = 4 * k + (lane & 3);
+        uint4 w;
+        uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const TOut lo = from_f<TOut>(tile[8 * seg + 2 * j][cc]), hi = from_f<TOut>(tile[8 * seg + 2 * j + 1][cc]);
+            wp[j] = (uint32_t)*reinterpret_cast<const unsigned short *>(&lo) |
+                    ((uint32_t)*reinterpret_cast<const unsigned short *>(&hi) << 16);
+        }
+        *reinterpret_cast<uint4 *>(out + (long long)(c0 + cc) * ld_out + r0 + 8 * seg) = w;
     }
 }
 
@@ -916,14 +996,14 @@ pmha_status bwd_gemm_tn(TcType ta, TcType tb, const void *A, int64_t lda, const 
             return PMHA_ERR_UNSUPPORTED;
         }
 #undef PMHA_TN
-        k_sum_chunks<<<blocks(K * N, 256), 256, 0, s>>>(scratch, K * N, (int)chunks, dW);
+        k_sum_chunks<<<blocks(K * N, 32), 256, 0, s>>>(scratch, K * N, (int)chunks, dW);
         count_launch(2);
     }
     if (db) {
         dim3 grid(blocks(K, 256), (unsigned)chunks);
         if (ta == TcType::F32) k_colsum_part<float><<<grid, 256, 0, s>>>((const float *)A, lda, M, (int)K, rpc, scratch);
         else k_colsum_part<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16 *)A, lda, M, (int)K, rpc, scratch);
-        k_sum_chunks<<<blocks(K, 256), 256, 0, s>>>(scratch, K, (int)chunks, db);
+        k_sum_chunks<<<blocks(K, 32), 256, 0, s>>>(scratch, K, (int)chunks, db);
         count_launch(2);
     }
     PMHA_CUDA_TRY(cudaGetLastError());
@@ -950,14 +1030,22 @@ struct Bump {
 };
 
 template <typename TIn, typename TOut>
-void transpose_cvt(const void *in, int64_t ld_in, int64_t M, int64_t E, int64_t Mpad, void *out, int64_t ld_out,
-                   cudaStream_t s, float *colsum = nullptr, __half *rows16 = nullptr, int64_t ld16 = 0)
+pmha_status transpose_cvt(const void *in, int64_t ld_in, int64_t M, int64_t E, int64_t Mpad, void *out, int64_t ld_out,
+                          cudaStream_t s, float *colsum = nullptr, __half *rows16 = nullptr, int64_t ld16 = 0)
 {
+    auto a16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
+    if (E % 64 || Mpad % 64 || Mpad < M || ld_in % 8 || ld_out % 8 || (rows16 && ld16 % 8) || !a16(in) || !a16(out) ||
+        !a16(rows16)) {
+        set_error("backward transpose: shape or alignment outside what its kernel takes (E %lld, Mpad %lld)",
+                  (long long)E, (long long)Mpad);
+        return PMHA_ERR_UNSUPPORTED;
+    }
     StageTimer timer("bwd_transpose", s);
     dim3 grid(blocks(Mpad, 64), blocks(E, 64));
     k_transpose_cvt<TIn, TOut><<<grid, 256, 0, s>>>((const TIn *)in, ld_in, M, (int)E, Mpad, (TOut *)out, ld_out,
                                                     colsum, rows16, ld16);
     count_launch();
+    return PMHA_OK;
 }
 
 // db (E) = column sums of an (M x E) matrix from the per-64-row-tile sums a
@@ -979,7 +1067,7 @@ pmha_status dw_tc(const __half *dyT, const __half *xT, int64_t E, int64_t Mpad, 
                                      "bwd_dw", s);
     if (st != PMHA_OK) return st;
     const int64_t kb = Mpad / 64, per = (kb + ksplit - 1) / ksplit, used = (kb + per - 1) / per;
-    k_sum_chunks<<<blocks(E * E, 256), 256, 0, s>>>(part, E * E, (int)used, dW);
+    k_sum_chunks<<<blocks(E * E, 32), 256, 0, s>>>(part, E * E, (int)used, dW);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;
@@ -1012,7 +1100,7 @@ pmha_status bwd_step5(const BwdGemmArgs &g, cudaStream_t s)
     if (use_tc(g)) {
         Bump bump{(char *)g.scratch};
         __nv_bfloat16 *woT = bump.take<__nv_bfloat16>((size_t)(E * E));
-        transpose_cvt<__nv_bfloat16, __nv_bfloat16>(g.w[3], E, E, E, E, woT, E, s);
+        if ((st = transpose_cvt<__nv_bfloat16, __nv_bfloat16>(g.w[3], E, E, E, E, woT, E, s)) != PMHA_OK) return st;
         // dmixed = dout Wo = dout (Wo^T)^T
         if ((st = gemm_tc_general(TcType::BF16, g.it, g.dout, E, M, E, woT, E, E, g.dmixed, E, 1, "bwd_dmixed", s)) !=
             PMHA_OK)
@@ -1023,8 +1111,8 @@ pmha_status bwd_step5(const BwdGemmArgs &g, cudaStream_t s)
             __half *mixT = bump.take<__half>((size_t)(E * Mp));
             float *part = bump.take<float>((size_t)(kMaxSplit * E * E));
             float *cs = g.gb[3] ? bump.take<float>((size_t)(Mp / 64 * E)) : nullptr;
-            transpose_cvt<__nv_bfloat16, __half>(g.dout, E, M, E, Mp, doutT, Mp, s, cs);
-            transpose_cvt<__half, __half>(g.mixed, E, M, E, Mp, mixT, Mp, s);
+            if ((st = transpose_cvt<__nv_bfloat16, __half>(g.dout, E, M, E, Mp, doutT, Mp, s, cs)) != PMHA_OK) return st;
+            if ((st = transpose_cvt<__half, __half>(g.mixed, E, M, E, Mp, mixT, Mp, s)) != PMHA_OK) return st;
             if ((st = dw_tc(doutT, mixT, E, Mp, g.gw[3], part, s)) != PMHA_OK) return st;
             if (cs) bias_from_tiles(cs, M, E, g.gb[3], s);
         }
@@ -1117,8 +1205,9 @@ pmha_status bwd_step1(const BwdGemmArgs &g, cudaStream_t s)
     for (int r = 0; r < 3; ++r) {
         if (!g.gw[r] && !g.gb[r]) continue;
         const int64_t mp = pad64(rows[r]);
-        transpose_cvt<float, __half>(g.dy[r], E, rows[r], E, mp, dyT[r], mp, s, g.gb[r] ? cs : nullptr, pack16[r],
-                                     pack_ld[r]);
+        if ((st = transpose_cvt<float, __half>(g.dy[r], E, rows[r], E, mp, dyT[r], mp, s, g.gb[r] ? cs : nullptr,
+                                               pack16[r], pack_ld[r])) != PMHA_OK)
+            return st;
         packed[r] = pack16[r] != nullptr;
         if (g.gb[r]) bias_from_tiles(cs, rows[r], E, g.gb[r], s);
         if (!g.gw[r]) continue;
@@ -1128,7 +1217,9 @@ pmha_status bwd_step1(const BwdGemmArgs &g, cudaStream_t s)
                 src = q;
                 break;
             }
-        if (src == r) transpose_cvt<__nv_bfloat16, __half>(g.in[r], E, rows[r], E, mp, xT[r], mp, s);
+        if (src == r)
+            if ((st = transpose_cvt<__nv_bfloat16, __half>(g.in[r], E, rows[r], E, mp, xT[r], mp, s)) != PMHA_OK)
+                return st;
         if ((st = dw_tc(dyT[r], xT[src], E, mp, g.gw[r], part, s)) != PMHA_OK) return st;
     }
     // input gradients: dX = sum over the roles of X of dY_r W_r, one K = n_roles * E product
@@ -1147,7 +1238,8 @@ pmha_status bwd_step1(const BwdGemmArgs &g, cudaStream_t s)
                 k_rows_f16<<<blocks(rows[r] * E / 4, 256), 256, 0, s>>>(g.dy[q], rows[r], (int)E, pack16[q], K);
                 count_launch();
             }
-            transpose_cvt<__nv_bfloat16, __half>(g.w[q], E, E, E, E, wsub + i * E, K, s);
+            if ((st = transpose_cvt<__nv_bfloat16, __half>(g.w[q], E, E, E, E, wsub + i * E, K, s)) != PMHA_OK)
+                return st;
         }
         if ((st = gemm_tc_general(TcType::F16, g.pt, pack16[r], K, rows[r], K, wsub, K, E, g.gx[r], E, 1, "bwd_dx",
                                   s)) != PMHA_OK)
