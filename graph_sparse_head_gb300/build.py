@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpmha.so")
 SOURCES = ["api.cu", "csr.cu", "gemm_simt.cu", "gemm_tc.cu", "edge_attn.cu", "edge_attn_f16.cu", "edge_attn_f32.cu", "edge_attn_ring.cu", "edge_attn_ring_out.cu",
-           "dense_attn.cu", "backward.cu", "noalloc.cu", "heavy.cu"]
+           "dense_attn.cu", "backward.cu", "bwd_ring.cu", "noalloc.cu", "heavy.cu"]
 HEADERS = [os.path.join(CSRC, "pmha_internal.h"), os.path.join(CSRC, "edge_stream.cuh"), os.path.join(CSRC, "edge_ring.cuh"), os.path.join(CSRC, "edge_out.cuh"), os.path.join(CSRC, "bwd_stream.cuh"),
            os.path.join(CSRC, "tc_util.cuh"),
            os.path.join(ROOT, "include", "pmha.h")]

@@ -501,11 +501,13 @@ pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void
 }
 
 // Workspace of the backward pass: the forward's regions, then (m, l), D,
+// the per-row records {m, 1/l, D, 0} and task counters of the ring kernels,
 // dmixed, dq, dk, dv, partial sums, an fp32 input-gradient accumulator and
 // the chunk partials of the weight-gradient sums.
 struct BwdLayout {
     Layout f;
-    size_t ml = 0, D = 0, dmixed = 0, dq = 0, dk = 0, dv = 0, pdq = 0, pdkv = 0, dx = 0, scratch = 0, total = 0;
+    size_t ml = 0, D = 0, rec = 0, ctr = 0, dmixed = 0, dq = 0, dk = 0, dv = 0, pdq = 0, pdkv = 0, dx = 0, scratch = 0,
+           total = 0;
     int64_t chunks = 1;
 };
 
@@ -520,6 +522,10 @@ BwdLayout bwd_layout(const pmha_graph *g, const pmha_params *p, int64_t B)
     o += align256((size_t)(B * L * H * 2) * 4);
     b.D = o;
     o += align256((size_t)(B * L * H) * 4);
+    b.rec = o;
+    o += align256((size_t)(B * L * H) * 16);
+    b.ctr = o;
+    o += 256;
     b.dmixed = o;
     o += align256((size_t)(B * L * E) * es);
     b.dq = o;
@@ -886,7 +892,8 @@ pmha_status pmha_backward(const pmha_graph *g, const pmha_params *p, const void 
     gm.chunks = bl.chunks;
     if ((st = bwd_step5(gm, s)) != PMHA_OK) return st;
     // steps 2-4
-    if ((st = bwd_rowdot(it, dmixed, mixed, B * L, E, H, D, s)) != PMHA_OK) return st;
+    float4 *rec = (float4 *)(ws + bl.rec);
+    if ((st = bwd_rowdot(it, dmixed, mixed, B * L, E, H, D, ml, rec, s)) != PMHA_OK) return st;
     BwdAttnArgs x;
     x.q = a.q;
     x.q_ld = a.q_ld;
@@ -896,6 +903,8 @@ pmha_status pmha_backward(const pmha_graph *g, const pmha_params *p, const void 
     x.dmixed = dmixed;
     x.ml = ml;
     x.D = D;
+    x.rec = rec;
+    x.ctr = (unsigned *)(ws + bl.ctr);
     x.kpm = key_padding_mask;
     x.dq = dq;
     x.dk = dk;

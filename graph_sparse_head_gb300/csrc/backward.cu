@@ -86,7 +86,8 @@ __device__ __forceinline__ void widen16<float>(const uint4 &u, float (&f)[4])
 
 template <typename T>
 __global__ void __launch_bounds__(256) k_rowdot(const T *__restrict__ dmixed, const T *__restrict__ mixed,
-                                                long long rows, int E, int H, float *__restrict__ D)
+                                                long long rows, int E, int H, float *__restrict__ D,
+                                                const float *__restrict__ ml, float4 *__restrict__ rec)
 {
     constexpr int PER = 16 / (int)sizeof(T);  // channels per vector
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // row * H + head
@@ -98,19 +99,22 @@ __global__ void __launch_bounds__(256) k_rowdot(const T *__restrict__ dmixed, co
     float acc = 0.f;
     if (d % PER) {  // heads narrower than a vector (float32 heads of 1 or 2 channels)
         for (int c = 0; c < d; ++c) acc = __fadd_rn(acc, __fmul_rn(to_f(gs[c]), to_f(os[c])));
-        D[i] = acc;
-        return;
-    }
-    const uint4 *g = reinterpret_cast<const uint4 *>(gs);
-    const uint4 *o = reinterpret_cast<const uint4 *>(os);
-    for (int v = 0; v < d / PER; ++v) {
-        float fg[PER], fo[PER];
-        widen16<T>(__ldg(g + v), fg);
-        widen16<T>(__ldg(o + v), fo);
+    } else {
+        const uint4 *g = reinterpret_cast<const uint4 *>(gs);
+        const uint4 *o = reinterpret_cast<const uint4 *>(os);
+        for (int v = 0; v < d / PER; ++v) {
+            float fg[PER], fo[PER];
+            widen16<T>(__ldg(g + v), fg);
+            widen16<T>(__ldg(o + v), fo);
 #pragma unroll
-        for (int c = 0; c < PER; ++c) acc = __fadd_rn(acc, __fmul_rn(fg[c], fo[c]));
+            for (int c = 0; c < PER; ++c) acc = __fadd_rn(acc, __fmul_rn(fg[c], fo[c]));
+        }
     }
     D[i] = acc;
+    if (rec) {  // the per-edge kernels' record of (row, head): m, 1/l, D
+        const float2 s = reinterpret_cast<const float2 *>(ml)[i];
+        rec[i] = make_float4(s.x, s.y > 0.f ? __frcp_rn(s.y) : 0.f, acc, 0.f);
+    }
 }
 
 struct WalkArgs {
@@ -844,15 +848,15 @@ bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lpe, TcType t)
 }
 
 pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t rows, int64_t E, int64_t H, float *D,
-                       cudaStream_t s)
+                       const float *ml, float4 *rec, cudaStream_t s)
 {
     StageTimer timer("bwd_rowdot", s);
     if (t == TcType::F16)
         k_rowdot<__half><<<blocks(rows * H, 256), 256, 0, s>>>((const __half *)dmixed, (const __half *)mixed, rows,
-                                                              (int)E, (int)H, D);
+                                                              (int)E, (int)H, D, ml, rec);
     else
         k_rowdot<float><<<blocks(rows * H, 256), 256, 0, s>>>((const float *)dmixed, (const float *)mixed, rows,
-                                                             (int)E, (int)H, D);
+                                                             (int)E, (int)H, D, ml, rec);
     count_launch();
     PMHA_CUDA_TRY(cudaGetLastError());
     return PMHA_OK;
@@ -899,7 +903,53 @@ pmha_status bwd_attention(TcType t, const pmha_graph *g, const BwdAttnArgs &x, c
     dkv.out0 = x.dk;
     dkv.out1 = x.dv;
     dkv.part = x.part_dkv;
-    if (x.B * g->n_units > 0) {
+    if (x.B * g->n_units > 0 && x.rec && t == TcType::F16 && bwd_ring_supported(x.E, x.H)) {
+        // the ring kernels: persistent warps on a queue per view
+        StageTimer timer("bwd_edges", s);
+        PMHA_CUDA_TRY(cudaMemsetAsync(x.ctr, 0, 2 * sizeof(unsigned), s));
+        BwdRingArgs r;
+        r.q = x.q;
+        r.q_ld = x.q_ld;
+        r.k = x.k;
+        r.v = x.v;
+        r.kv_ld = x.kv_ld;
+        r.g = x.dmixed;
+        r.rec = x.rec;
+        r.kpm = x.kpm;
+        r.n_units = g->n_units;
+        r.nnz = g->nnz;
+        r.B = (int)x.B;
+        r.L = (int)g->L;
+        r.S = (int)g->S;
+        r.E = (int)x.E;
+        r.H = (int)x.H;
+        r.score_scale = dq.score_scale;
+        r.inv_sqrt_d = dq.inv_sqrt_d;
+        BwdRingArgs rk = r;
+        r.row_ptr = g->row_ptr;
+        r.idx = g->col;
+        r.unit_first = g->unit_first_t;
+        r.unit_order = g->unit_order;
+        r.n_rows = (int)g->L;
+        r.out0 = x.dq;
+        r.out1 = nullptr;
+        r.part = x.part_dq;
+        r.task_counter = x.ctr;
+        rk.row_ptr = g->src_row_ptr;
+        rk.idx = g->tgt_by_src;
+        rk.unit_first = g->unit_first_s;
+        rk.unit_order = nullptr;
+        rk.n_rows = (int)g->S;
+        rk.out0 = x.dk;
+        rk.out1 = x.dv;
+        rk.part = x.part_dkv;
+        rk.task_counter = x.ctr + 1;
+        pmha_status st = launch_bwd_ring(false, r, s);
+        if (st == PMHA_OK) st = launch_bwd_ring(true, rk, s);
+        if (st != PMHA_OK) return st;
+        count_launch(2);
+        PMHA_CUDA_TRY(cudaGetLastError());
+    } else if (x.B * g->n_units > 0) {
         StageTimer timer("bwd_edges", s);
         const bool ok = t == TcType::F16 ? launch_walks<__half>(cpl, lpe, dq, dkv, s)
                                          : launch_walks<float>(cpl, lpe, dq, dkv, s);

@@ -213,17 +213,45 @@ struct BwdAttnArgs {
     const void *dmixed;    // (B, L, E) intermediate type
     const float *ml;       // (B, L, H, 2) forward softmax statistics (log2 units)
     const float *D;        // (B, L, H) dot(dmixed, mixed) per head
+    const float4 *rec;     // (B, L, H) {m, 1/l, D, 0}, or null (then no ring kernels)
+    unsigned *ctr;         // two task counters for the ring kernels
     const uint8_t *kpm;    // (B, S) or null
     float *dq, *dk, *dv;   // (B, L, E), (B, S, E), (B, S, E), scaled
     float *part_dq;        // (B, 2 n_units, E) partial sums of rows crossing a unit
     float *part_dkv;       // (B, 2 n_units, 2E)
     int64_t B, E, H;
 };
+// The per-edge backward kernels on the ring design (bwd_ring.cu): fp16
+// intermediates, embed_dim 128, 256 or 512, heads of a multiple of 16
+// channels. One launch walks one view: dq over the per-target view (rows =
+// targets, idx = sources) or dk, dv over the per-source view.
+struct BwdRingArgs {
+    const void *q;          // projected q rows (B, L) of pitch q_ld, fp16
+    long long q_ld;
+    const void *k, *v;      // projected k, v rows (B, S) of pitch kv_ld, fp16
+    long long kv_ld;
+    const void *g;          // dmixed (B, L, E), fp16
+    const float4 *rec;      // (B, L, H): m (log2 units), 1/l (0 when l = 0), D, 0
+    const uint8_t *kpm;     // (B, S) or null
+    const int32_t *row_ptr, *idx, *unit_first;  // the walked view
+    const int32_t *unit_order;                  // the order of its units in the queue, or null (index order)
+    long long n_units, nnz;
+    int B, L, S, E, H, n_rows;                  // n_rows: L (dq) or S (dk, dv)
+    float score_scale;      // log2(e) / sqrt(d)
+    float inv_sqrt_d;
+    float *out0, *out1;     // dq | dk, dv rows (B, n_rows, E), fp32
+    float *part;            // (B, 2 n_units, W) partial sums of rows crossing a unit (W = E, or 2E for dk|dv)
+    unsigned *task_counter; // zero before the launch
+};
+bool bwd_ring_supported(int64_t E, int64_t H);
+pmha_status launch_bwd_ring(bool dkv, const BwdRingArgs &a, cudaStream_t s);
 // Lane shape of the per-edge backward kernels for intermediate type t
 // (channels per lane, lanes per sample; false: no kernel).
 bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lpe, TcType t);
+// D (rows, H) = dmixed . mixed per head; with rec non-null also the records
+// {m, 1/l, D, 0} from ml (rows, H, 2).
 pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t rows, int64_t E, int64_t H, float *D,
-                       cudaStream_t s);
+                       const float *ml, float4 *rec, cudaStream_t s);
 // Steps 2-4 backward: dq over the per-target view, dk and dv over the per-source view.
 pmha_status bwd_attention(TcType t, const pmha_graph *g, const BwdAttnArgs &x, cudaStream_t s);
 // C (M x N) (+)= A (M x K) . B (K x N) on CUDA cores, fp32 accumulation.
