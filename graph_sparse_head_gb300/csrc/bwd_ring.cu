@@ -28,8 +28,11 @@
 // at once (early release). Chunk placement and the swapped read order of
 // lanes with sw = 1 are the forward's (no shared-memory bank conflicts);
 // a lane's accumulators are swapped alike and stored back in row order.
-// The dot products take mixed-precision FMAs (fp16 x fp16, fp32 accumulate,
-// exact products); the sums over edges widen the fp16 rows to fp32.
+// Rows are widened to fp32 once and serve both the dot products and the sums
+// over edges (paired fp32 FMAs); the dot of two fp16 rows that are not summed
+// (dmixed . v for dq) takes mixed-precision FMAs (fp16 x fp16, fp32
+// accumulate). fp16 products are exact in fp32, so both forms give the same
+// dot product for the same summation order.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -83,15 +86,38 @@ __device__ __forceinline__ float dot16(const Raw<32> &x, const Raw<32> &y, int l
     return d;
 }
 
-// acc += c * x for the lane's 16 fp16 channels
-__device__ __forceinline__ void axpy16(f2 (&acc)[8], float c, const Raw<32> &x)
+// the lane's 16 fp16 channels as fp32 pairs
+__device__ __forceinline__ void widen16(const Raw<32> &x, f2 (&f)[8])
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&x.w[i]));
+        f[i] = pk(v.x, v.y);
+    }
+}
+
+// dot16 on widened channels: the same products (exact in fp32), sums and
+// order, so the same result
+__device__ __forceinline__ float dot16w(const f2 (&x)[8], const f2 (&y)[8], int lph)
+{
+    f2 a2 = 0ull, b2 = 0ull;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        a2 = ffma2(x[i], y[i], a2);
+        b2 = ffma2(x[i + 1], y[i + 1], b2);
+    }
+    const float2 fa = upk(a2), fb = upk(b2);
+    float d = __fadd_rn(__fadd_rn(fa.x, fb.x), __fadd_rn(fa.y, fb.y));
+    for (int o = 1; o < lph; o <<= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
+    return d;
+}
+
+// acc += c * x for the lane's 16 widened channels
+__device__ __forceinline__ void axpy16(f2 (&acc)[8], float c, const f2 (&x)[8])
 {
     const f2 c2 = pk(c, c);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&x.w[i]));
-        acc[i] = ffma2(c2, pk(f.x, f.y), acc[i]);
-    }
+    for (int i = 0; i < 8; ++i) acc[i] = ffma2(c2, x[i], acc[i]);
 }
 
 // 16 fp32 values of a lane (its two chunks in read order) times `scale` to
@@ -114,8 +140,10 @@ __device__ __forceinline__ void store16(float *row, const f2 (&acc)[8], float sc
 
 // DKV: the per-source view (dk, dv), else the per-target view (dq).
 // KPM: a key_padding_mask drops keys (their edges have weight 0).
+// Shared memory allows 6 blocks (12 warps) per SM, so the register budget
+// is set for that many (168 a thread).
 template <int LPE, bool DKV, bool KPM>
-__global__ void __launch_bounds__(kBRWarps * 32) k_bwd_ring(BwdRingArgs a)
+__global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
 {
     static_assert(LPE >= 8 && LPE <= 32, "8 to 32 lanes per row");
     constexpr int P = 32 / LPE;      // slots (samples) per warp
@@ -265,7 +293,9 @@ __global__ void __launch_bounds__(kBRWarps * 32) k_bwd_ring(BwdRingArgs a)
     int bound = end_in(wc, r);
     const bool first_started_here = a.row_ptr[r] == e0;
     bool is_first = true;
-    Raw<32> rowC, rowD;           // dq: q, dmixed of the target; dkv: k, v of the source
+    // dq: the target's q (widened) and dmixed (fp16); dkv: the source's k and v (widened)
+    f2 rowCw[8], rowDw[8];
+    Raw<32> rowD;
     float rm = 0.f, rinv = 0.f, rD = 0.f;  // dq: the target's record
     bool r_dropped = false;       // dkv: the source is a padded key
     f2 acc0[8], acc1[8];          // dq: acc0; dkv: dk (acc0), dv (acc1)
@@ -277,8 +307,9 @@ __global__ void __launch_bounds__(kBRWarps * 32) k_bwd_ring(BwdRingArgs a)
         }
     };
     auto set_row = [&](uint32_t st) {
-        rowC = lds_pair(rd0 + st + kOffC, rd1 + st + kOffC);
+        widen16(lds_pair(rd0 + st + kOffC, rd1 + st + kOffC), rowCw);
         rowD = lds_pair(rd0 + st + kOffD, rd1 + st + kOffD);
+        if constexpr (DKV) widen16(rowD, rowDw);
         if constexpr (!DKV) {
             float pad;
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -317,21 +348,26 @@ __global__ void __launch_bounds__(kBRWarps * 32) k_bwd_ring(BwdRingArgs a)
     // target's record (dkv), o its other end (dq: the source, for the mask)
     auto edge = [&](const Raw<32> &A, const Raw<32> &B, float4 rec, int o) {
         if constexpr (DKV) {
-            const float d1 = dot16(A, rowC, lph), d2 = dot16(B, rowD, lph);
+            f2 qw[8], gw[8];
+            widen16(A, qw);
+            widen16(B, gw);
+            const float d1 = dot16w(qw, rowCw, lph), d2 = dot16w(gw, rowDw, lph);
             const float w = (rec.y > 0.f && !r_dropped)
                                 ? __fmul_rn(ex2(__fsub_rn(__fmul_rn(d1, a.score_scale), rec.x)), rec.y)
                                 : 0.f;
             const float ds = __fmul_rn(w, __fsub_rn(d2, rec.z));
-            axpy16(acc0, ds, A);
-            axpy16(acc1, w, B);
+            axpy16(acc0, ds, qw);
+            axpy16(acc1, w, gw);
         } else {
-            const float d1 = dot16(rowC, A, lph), d2 = dot16(rowD, B, lph);
+            f2 kw[8];
+            widen16(A, kw);
+            const float d1 = dot16w(rowCw, kw, lph), d2 = dot16(rowD, B, lph);
             const bool drop = KPM && kpm_b[o] != 0;
             const float w = (rinv > 0.f && !drop)
                                 ? __fmul_rn(ex2(__fsub_rn(__fmul_rn(d1, a.score_scale), rm)), rinv)
                                 : 0.f;
             const float ds = __fmul_rn(w, __fsub_rn(d2, rD));
-            axpy16(acc0, ds, A);
+            axpy16(acc0, ds, kw);
         }
     };
     auto ld_rec = [&](uint32_t st) -> float4 {
@@ -374,10 +410,10 @@ __global__ void __launch_bounds__(kBRWarps * 32) k_bwd_ring(BwdRingArgs a)
             const Raw<32> B1 = lds_pair(rd0 + st1 + kOffB, rd1 + st1 + kOffB);
             const float4 q0 = ld_rec(st0), q1 = ld_rec(st1);
             const int o0 = other_end(j), o1 = other_end(j + 1);
-            // every lane's loads of both stages have returned before the warp refills them
-            const uint32_t touch = A0.w[0] ^ A0.w[4] ^ B0.w[0] ^ B0.w[4] ^ A1.w[0] ^ A1.w[4] ^ B1.w[0] ^ B1.w[4] ^
-                                   __float_as_uint(q0.x) ^ __float_as_uint(q1.x);
-            asm volatile("" ::"r"(touch));
+            // every lane's loads of both stages have returned before the warp
+            // refills them (one word of each 16-byte load is an input here)
+            asm volatile("" ::"r"(A0.w[0]), "r"(A0.w[4]), "r"(B0.w[0]), "r"(B0.w[4]), "r"(A1.w[0]), "r"(A1.w[4]),
+                         "r"(B1.w[0]), "r"(B1.w[4]), "f"(q0.x), "f"(q1.x));
             __syncwarp(kAll);
             issue2(j + kBRDepth, rs_now);
             edge(A0, B0, q0, o0);
