@@ -566,11 +566,13 @@ def bench_ours(args):
         pmha.pmha_device_status()
         back_steps = max(3, min(args.steps, 30))
         b_ms = max_over_ranks(statistics.mean(_timed(torch, stream, flush, back_steps, back_step)), world, dev)
-        b_stages = _stage_pass(pmha, torch, stream, flush, min(back_steps, 10), back_step)
+        b_calls = min(back_steps, 10)
+        b_stages = _stage_pass(pmha, torch, stream, flush, b_calls, back_step)
         pmha.pmha_device_status()
         back = {"ms_per_step": b_ms, "value": world * scores / (b_ms / 1e3), "unit": UNIT,
                 "steps": back_steps, "what": "pmha_backward: forward recompute, input, weight and bias gradients",
-                "stages_avg_us": {k: v["avg_us"] for k, v in b_stages.items()}}
+                "stages_avg_us": {k: v["avg_us"] for k, v in b_stages.items()},
+                "stages_us_per_call": {k: 1e3 * v["total_ms"] / b_calls for k, v in b_stages.items()}}
 
     # ---- end to end through the C ABI with host buffers (pinned), per step:
     # copy the step's tokens in, run, copy the output back. Steps rotate over

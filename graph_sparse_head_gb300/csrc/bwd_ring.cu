@@ -28,11 +28,11 @@
 // at once (early release). Chunk placement and the swapped read order of
 // lanes with sw = 1 are the forward's (no shared-memory bank conflicts);
 // a lane's accumulators are swapped alike and stored back in row order.
-// Rows are widened to fp32 once and serve both the dot products and the sums
-// over edges (paired fp32 FMAs); the dot of two fp16 rows that are not summed
-// (dmixed . v for dq) takes mixed-precision FMAs (fp16 x fp16, fp32
-// accumulate). fp16 products are exact in fp32, so both forms give the same
-// dot product for the same summation order.
+// Dot products take mixed-precision FMAs (fp16 x fp16, fp32 accumulate) or,
+// where a row is widened to fp32 anyway (dq's k, summed into dq, and the
+// target's q), paired fp32 FMAs: fp16 products are exact in fp32, so both
+// forms give the same dot product for the same summation order. The sums
+// over edges widen the fp16 rows (paired fp32 FMAs).
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -293,9 +293,9 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
     int bound = end_in(wc, r);
     const bool first_started_here = a.row_ptr[r] == e0;
     bool is_first = true;
-    // dq: the target's q (widened) and dmixed (fp16); dkv: the source's k and v (widened)
-    f2 rowCw[8], rowDw[8];
-    Raw<32> rowD;
+    // dq: the target's q (widened) and dmixed; dkv: the source's k and v
+    f2 rowCw[8];
+    Raw<32> rowC, rowD;
     float rm = 0.f, rinv = 0.f, rD = 0.f;  // dq: the target's record
     bool r_dropped = false;       // dkv: the source is a padded key
     f2 acc0[8], acc1[8];          // dq: acc0; dkv: dk (acc0), dv (acc1)
@@ -307,9 +307,9 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
         }
     };
     auto set_row = [&](uint32_t st) {
-        widen16(lds_pair(rd0 + st + kOffC, rd1 + st + kOffC), rowCw);
+        rowC = lds_pair(rd0 + st + kOffC, rd1 + st + kOffC);
         rowD = lds_pair(rd0 + st + kOffD, rd1 + st + kOffD);
-        if constexpr (DKV) widen16(rowD, rowDw);
+        if constexpr (!DKV) widen16(rowC, rowCw);
         if constexpr (!DKV) {
             float pad;
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -348,16 +348,16 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
     // target's record (dkv), o its other end (dq: the source, for the mask)
     auto edge = [&](const Raw<32> &A, const Raw<32> &B, float4 rec, int o) {
         if constexpr (DKV) {
-            f2 qw[8], gw[8];
-            widen16(A, qw);
-            widen16(B, gw);
-            const float d1 = dot16w(qw, rowCw, lph), d2 = dot16w(gw, rowDw, lph);
+            const float d1 = dot16(A, rowC, lph), d2 = dot16(B, rowD, lph);
             const float w = (rec.y > 0.f && !r_dropped)
                                 ? __fmul_rn(ex2(__fsub_rn(__fmul_rn(d1, a.score_scale), rec.x)), rec.y)
                                 : 0.f;
             const float ds = __fmul_rn(w, __fsub_rn(d2, rec.z));
-            axpy16(acc0, ds, qw);
-            axpy16(acc1, w, gw);
+            f2 xw[8];
+            widen16(A, xw);
+            axpy16(acc0, ds, xw);
+            widen16(B, xw);
+            axpy16(acc1, w, xw);
         } else {
             f2 kw[8];
             widen16(A, kw);
