@@ -501,7 +501,7 @@ pmha_status forward_device(const pmha_graph *g, const pmha_params *p, const void
 }
 
 // Workspace of the backward pass: the forward's regions, then (m, l), D,
-// the per-row records {m, 1/l, D, 0} and task counters of the ring kernels,
+// the per-row records {m + log2(l), D} and task counters of the ring kernels,
 // dmixed, dq, dk, dv, partial sums, an fp32 input-gradient accumulator and
 // the chunk partials of the weight-gradient sums.
 struct BwdLayout {
@@ -523,7 +523,7 @@ BwdLayout bwd_layout(const pmha_graph *g, const pmha_params *p, int64_t B)
     b.D = o;
     o += align256((size_t)(B * L * H) * 4);
     b.rec = o;
-    o += align256((size_t)(B * L * H) * 16);
+    o += align256((size_t)(B * L * H) * 8);
     b.ctr = o;
     o += 256;
     b.dmixed = o;
@@ -892,7 +892,7 @@ pmha_status pmha_backward(const pmha_graph *g, const pmha_params *p, const void 
     gm.chunks = bl.chunks;
     if ((st = bwd_step5(gm, s)) != PMHA_OK) return st;
     // steps 2-4
-    float4 *rec = (float4 *)(ws + bl.rec);
+    float2 *rec = (float2 *)(ws + bl.rec);
     if ((st = bwd_rowdot(it, dmixed, mixed, B * L, E, H, D, ml, rec, s)) != PMHA_OK) return st;
     BwdAttnArgs x;
     x.q = a.q;

@@ -87,7 +87,7 @@ __device__ __forceinline__ void widen16<float>(const uint4 &u, float (&f)[4])
 template <typename T>
 __global__ void __launch_bounds__(256) k_rowdot(const T *__restrict__ dmixed, const T *__restrict__ mixed,
                                                 long long rows, int E, int H, float *__restrict__ D,
-                                                const float *__restrict__ ml, float4 *__restrict__ rec)
+                                                const float *__restrict__ ml, float2 *__restrict__ rec)
 {
     constexpr int PER = 16 / (int)sizeof(T);  // channels per vector
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // row * H + head
@@ -111,9 +111,9 @@ __global__ void __launch_bounds__(256) k_rowdot(const T *__restrict__ dmixed, co
         }
     }
     D[i] = acc;
-    if (rec) {  // the per-edge kernels' record of (row, head): m, 1/l, D
+    if (rec) {  // the ring kernels' record of (row, head): w = 2^(s - c) with c = m + log2(l)
         const float2 s = reinterpret_cast<const float2 *>(ml)[i];
-        rec[i] = make_float4(s.x, s.y > 0.f ? __frcp_rn(s.y) : 0.f, acc, 0.f);
+        rec[i] = make_float2(s.y > 0.f ? __fadd_rn(s.x, log2f(s.y)) : INFINITY, acc);
     }
 }
 
@@ -848,7 +848,7 @@ bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lpe, TcType t)
 }
 
 pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t rows, int64_t E, int64_t H, float *D,
-                       const float *ml, float4 *rec, cudaStream_t s)
+                       const float *ml, float2 *rec, cudaStream_t s)
 {
     StageTimer timer("bwd_rowdot", s);
     if (t == TcType::F16)

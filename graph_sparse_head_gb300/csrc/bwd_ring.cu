@@ -3,8 +3,8 @@
 // the structure of the forward's ring kernel (edge_ring.cuh):
 //
 //   dq  (per-target view): per edge the source's k and v rows; per row the
-//       target's q and dmixed rows and its record {m, 1/l, D}
-//       w = 2^(q.k log2(e)/sqrt(d) - m) / l, ds = w (dmixed.v - D),
+//       target's q and dmixed rows and its record {c, D}, c = m + log2(l)
+//       w = 2^(q.k log2(e)/sqrt(d) - c) (= 2^(s - m) / l), ds = w (dmixed.v - D),
 //       dq_t = sum ds k / sqrt(d)
 //   dkv (per-source view): per edge the target's q and dmixed rows and its
 //       record; per row the source's k and v rows
@@ -65,10 +65,10 @@ constexpr int kBRDepth = PMHA_BRING_DEPTH;  // stages = edges in flight (early r
 static_assert(kBRDepth % 2 == 0 && kBRDepth >= 2, "edges go two per step");
 constexpr int kPartBytes = 32 * 32;         // one row part of the warp: 32 lanes x 16 fp16
 // a stage: parts A, B (the edge's rows), C, D (the row's rows), then one
-// 16-byte record per lane
+// 8-byte record per lane
 constexpr int kOffA = 0, kOffB = kPartBytes, kOffC = 2 * kPartBytes, kOffD = 3 * kPartBytes,
               kOffRec = 4 * kPartBytes;
-constexpr int kStage = 4 * kPartBytes + 32 * 16;
+constexpr int kStage = 4 * kPartBytes + 32 * 8;
 constexpr int kBRSmem = kBRWarps * kBRDepth * kStage;
 
 // dot product of a lane's 16 channels (two independent partial sums each
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
     const uint32_t rd0 = wbase + (uint32_t)(slot * PART + 32 * grp + 16 * sw);
     const uint32_t rd1 = wbase + (uint32_t)(slot * PART + 32 * grp + 16 * (1 - sw));
     const uint32_t fill = wbase + (uint32_t)(slot * PART + 16 * grp);
-    const uint32_t rec_at = wbase + (uint32_t)(kOffRec + 16 * lane);
+    const uint32_t rec_at = wbase + (uint32_t)(kOffRec + 8 * lane);
 
     const unsigned n_groups = (unsigned)((a.B + P - 1) / P);
     const unsigned n_u = (unsigned)a.n_units;
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
     const char *K0 = (const char *)a.k + ((long long)b * a.S * a.kv_ld) * 2 + 16 * grp;
     const char *V0 = (const char *)a.v + ((long long)b * a.S * a.kv_ld) * 2 + 16 * grp;
     const unsigned q_row = (unsigned)(a.q_ld * 2), g_row = (unsigned)(a.E * 2), kv_row = (unsigned)(a.kv_ld * 2);
-    const float4 *REC = a.rec + (long long)b * a.L * a.H + head;
+    const float2 *REC = a.rec + (long long)b * a.L * a.H + head;
     const uint8_t *kpm_b = KPM ? a.kpm + (long long)b * a.S : nullptr;
 
     // two 16-byte chunks (grp and LPE + grp) of a row into part `off` of stage st
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
         cp_async16_at<PART / 2, 16 * LPE>(fill + st + off, src);
     };
     auto copy_rec = [&](uint32_t st, int t) {
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(rec_at + st),
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(rec_at + st),
                      "l"(REC + (long long)(unsigned)t * a.H)
                      : "memory");
     };
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
     // dq: the target's q (widened) and dmixed; dkv: the source's k and v
     f2 rowCw[8];
     Raw<32> rowC, rowD;
-    float rm = 0.f, rinv = 0.f, rD = 0.f;  // dq: the target's record
+    float rc = 0.f, rD = 0.f;  // dq: the target's record
     bool r_dropped = false;       // dkv: the source is a padded key
     f2 acc0[8], acc1[8];          // dq: acc0; dkv: dk (acc0), dv (acc1)
     auto zero = [&]() {
@@ -311,10 +311,7 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
         rowD = lds_pair(rd0 + st + kOffD, rd1 + st + kOffD);
         if constexpr (!DKV) widen16(rowC, rowCw);
         if constexpr (!DKV) {
-            float pad;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(rm), "=f"(rinv), "=f"(rD), "=f"(pad)
-                         : "r"(rec_at + st));
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(rc), "=f"(rD) : "r"(rec_at + st));
         } else if constexpr (KPM) {
             r_dropped = kpm_b[r] != 0;
         }
@@ -346,13 +343,12 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
     };
     // one edge: A, B are the edge's rows (dq: k, v; dkv: q, dmixed), rec its
     // target's record (dkv), o its other end (dq: the source, for the mask)
-    auto edge = [&](const Raw<32> &A, const Raw<32> &B, float4 rec, int o) {
+    auto edge = [&](const Raw<32> &A, const Raw<32> &B, float2 rec, int o) {
         if constexpr (DKV) {
             const float d1 = dot16(A, rowC, lph), d2 = dot16(B, rowD, lph);
-            const float w = (rec.y > 0.f && !r_dropped)
-                                ? __fmul_rn(ex2(__fsub_rn(__fmul_rn(d1, a.score_scale), rec.x)), rec.y)
-                                : 0.f;
-            const float ds = __fmul_rn(w, __fsub_rn(d2, rec.z));
+            // c = +inf for a target without a live key: ex2(-inf) = +0
+            const float w = r_dropped ? 0.f : ex2(__fsub_rn(__fmul_rn(d1, a.score_scale), rec.x));
+            const float ds = __fmul_rn(w, __fsub_rn(d2, rec.y));
             f2 xw[8];
             widen16(A, xw);
             axpy16(acc0, ds, xw);
@@ -363,19 +359,14 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
             widen16(A, kw);
             const float d1 = dot16w(rowCw, kw, lph), d2 = dot16(rowD, B, lph);
             const bool drop = KPM && kpm_b[o] != 0;
-            const float w = (rinv > 0.f && !drop)
-                                ? __fmul_rn(ex2(__fsub_rn(__fmul_rn(d1, a.score_scale), rm)), rinv)
-                                : 0.f;
+            const float w = drop ? 0.f : ex2(__fsub_rn(__fmul_rn(d1, a.score_scale), rc));
             const float ds = __fmul_rn(w, __fsub_rn(d2, rD));
             axpy16(acc0, ds, kw);
         }
     };
-    auto ld_rec = [&](uint32_t st) -> float4 {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if constexpr (DKV)
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                         : "r"(rec_at + st));
+    auto ld_rec = [&](uint32_t st) -> float2 {
+        float2 v = make_float2(0.f, 0.f);
+        if constexpr (DKV) asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(rec_at + st));
         return v;
     };
     auto other_end = [&](int j) -> int {  // dq with a mask: the source of position e0 + j
@@ -408,7 +399,7 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
             const Raw<32> B0 = lds_pair(rd0 + st0 + kOffB, rd1 + st0 + kOffB);
             const Raw<32> A1 = lds_pair(rd0 + st1 + kOffA, rd1 + st1 + kOffA);
             const Raw<32> B1 = lds_pair(rd0 + st1 + kOffB, rd1 + st1 + kOffB);
-            const float4 q0 = ld_rec(st0), q1 = ld_rec(st1);
+            const float2 q0 = ld_rec(st0), q1 = ld_rec(st1);
             const int o0 = other_end(j), o1 = other_end(j + 1);
             // every lane's loads of both stages have returned before the warp
             // refills them (one word of each 16-byte load is an input here)

@@ -213,7 +213,7 @@ struct BwdAttnArgs {
     const void *dmixed;    // (B, L, E) intermediate type
     const float *ml;       // (B, L, H, 2) forward softmax statistics (log2 units)
     const float *D;        // (B, L, H) dot(dmixed, mixed) per head
-    const float4 *rec;     // (B, L, H) {m, 1/l, D, 0}, or null (then no ring kernels)
+    const float2 *rec;     // (B, L, H) {m + log2(l), D}, or null (then no ring kernels)
     unsigned *ctr;         // two task counters for the ring kernels
     const uint8_t *kpm;    // (B, S) or null
     float *dq, *dk, *dv;   // (B, L, E), (B, S, E), (B, S, E), scaled
@@ -231,7 +231,7 @@ struct BwdRingArgs {
     const void *k, *v;      // projected k, v rows (B, S) of pitch kv_ld, fp16
     long long kv_ld;
     const void *g;          // dmixed (B, L, E), fp16
-    const float4 *rec;      // (B, L, H): m (log2 units), 1/l (0 when l = 0), D, 0
+    const float2 *rec;      // (B, L, H): c = m + log2(l) (log2 units; +inf when l = 0), D
     const uint8_t *kpm;     // (B, S) or null
     const int32_t *row_ptr, *idx, *unit_first;  // the walked view
     const int32_t *unit_order;                  // the order of its units in the queue, or null (index order)
@@ -249,9 +249,9 @@ pmha_status launch_bwd_ring(bool dkv, const BwdRingArgs &a, cudaStream_t s);
 // (channels per lane, lanes per sample; false: no kernel).
 bool bwd_shape(int64_t E, int64_t H, int *cpl, int *lpe, TcType t);
 // D (rows, H) = dmixed . mixed per head; with rec non-null also the records
-// {m, 1/l, D, 0} from ml (rows, H, 2).
+// {m + log2(l) (+inf when l = 0), D} from ml (rows, H, 2).
 pmha_status bwd_rowdot(TcType t, const void *dmixed, const void *mixed, int64_t rows, int64_t E, int64_t H, float *D,
-                       const float *ml, float4 *rec, cudaStream_t s);
+                       const float *ml, float2 *rec, cudaStream_t s);
 // Steps 2-4 backward: dq over the per-target view, dk and dv over the per-source view.
 pmha_status bwd_attention(TcType t, const pmha_graph *g, const BwdAttnArgs &x, cudaStream_t s);
 // C (M x N) (+)= A (M x K) . B (K x N) on CUDA cores, fp32 accumulation.

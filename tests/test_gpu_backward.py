@@ -111,6 +111,26 @@ def test_backward_with_mask_and_separate_value():
     g.destroy()
 
 
+@pytest.mark.parametrize("E,H,B", [
+    (256, 8, 3),   # 16 lanes a sample, 2 lanes a head; one sample group with an idle slot
+    (512, 8, 2),   # 32 lanes a sample, 4 lanes a head
+    (256, 16, 5),  # one lane a head; 3 sample groups, the last half idle
+])
+def test_backward_wide_rows_with_mask(E, H, B):
+    # the per-edge ring kernels for rows of 16 and 32 lanes, heads over
+    # several lanes, with dropped keys: a dropped key's k gradient is exactly 0
+    rng = np.random.default_rng(E + H + B)
+    L, S = 180, 400
+    src, tgt = synth.bipartite_membership_graph(rng, L, S, 4, 40)
+    c = Case(src, tgt, L, S, E, H, B, "bf16", seed=E * H + B, bipartite=True)
+    kpm = synth.scattered_mask(rng, B, S, 0.25)
+    g, got, ref, tensors = _run(c, kpm=kpm)
+    _check(got, ref, tensors, "bf16")
+    dk = got["dkey"].float().cpu().numpy()
+    assert np.all(dk[kpm] == 0.0)
+    g.destroy()
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_backward_self_loops_and_no_bias(dt):
     rng = np.random.default_rng(50)
