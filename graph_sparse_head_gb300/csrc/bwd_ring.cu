@@ -54,7 +54,6 @@ using stream::lds_pair;
 using stream::pk;
 using stream::Raw;
 using stream::smem_u32;
-using stream::static_for;
 using stream::upk;
 
 #ifndef PMHA_BRING_DEPTH
@@ -200,7 +199,7 @@ __global__ void __launch_bounds__(kBRWarps * 32, 6) k_bwd_ring(BwdRingArgs a)
                      "l"(REC + (long long)(unsigned)t * a.H)
                      : "memory");
     };
-    // the other end of edge position p (p past the unit: nothing)
+    // the rows an edge brings from its other end o (and, for DKV, o's record)
     auto copy_edge = [&](uint32_t st, int o) {
         if constexpr (DKV) {  // o is a target
             copy_row(st, kOffA, Q0 + (unsigned long long)(unsigned)o * q_row);
