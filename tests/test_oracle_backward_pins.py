@@ -9,8 +9,9 @@ own arithmetic:
   same mix), and through torch's key_padding_mask;
 * central finite differences of sum(output * dout) on a tiny case;
 * exact properties: the key-projection bias gets no gradient (the softmax of
-  each target is invariant to a shift shared by its scores), and a target
-  with a single source passes no gradient into the scores."""
+  each target is invariant to a shift shared by its scores), a target
+  with a single source passes no gradient into the scores, and a sample
+  whose keys are all padding passes none into its tokens."""
 import numpy as np
 import pytest
 import torch
@@ -210,6 +211,25 @@ def test_output_and_value_bias_gradients_in_closed_form(masked):
     dmixed = dout @ p["wo"].astype(np.float64)
     assert np.abs(g["dbo"] - dout.sum(axis=(0, 1))).max() < 1e-12
     assert np.abs(g["dbv"] - dmixed[live].sum(axis=0)).max() < 1e-11
+
+
+def test_fully_masked_sample_gets_no_input_gradient():
+    # every key of sample 1 is padding: its targets mix to zeros (their output
+    # is bo whatever the inputs), so nothing flows back into that sample's
+    # query, key or value tokens; the other samples do get gradients
+    rng = np.random.default_rng(37)
+    E, H, L, S, B = 16, 4, 20, 26, 3
+    p = _params(rng, E)
+    src, tgt = synth.uniform_graph(rng, L, S, 80, min_in_degree=1)
+    xq = rng.standard_normal((B, L, E))
+    xkv = rng.standard_normal((B, S, E))
+    kpm = rng.random((B, S)) < 0.3
+    kpm[1] = True
+    dout = rng.standard_normal((B, L, E))
+    g = oracle.backward(xq, xkv, xkv, p, src, tgt, H, dout, key_padding_mask=kpm)
+    for n in ("dquery", "dkey", "dvalue"):
+        assert np.all(g[n][1] == 0.0), n
+        assert np.abs(g[n][0]).max() > 0 and np.abs(g[n][2]).max() > 0, n
 
 
 def test_linear_backward_matches_numpy():
