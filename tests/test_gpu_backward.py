@@ -131,6 +131,24 @@ def test_backward_wide_rows_with_mask(E, H, B):
     g.destroy()
 
 
+def test_backward_fully_masked_sample():
+    # every key of sample 1 is padding: its targets' records are {+inf, 0}, so
+    # the per-edge kernels give that sample exactly zero dq, dk and dv, and
+    # its input gradients are exactly zero
+    rng = np.random.default_rng(43)
+    L, S, E, H, B = 150, 300, 128, 8, 3
+    src, tgt = synth.bipartite_membership_graph(rng, L, S, 5, 40)
+    c = Case(src, tgt, L, S, E, H, B, "bf16", seed=44, bipartite=True)
+    kpm = synth.scattered_mask(rng, B, S, 0.2)
+    kpm[1] = True
+    g, got, ref, tensors = _run(c, kpm=kpm)
+    _check(got, ref, tensors, "bf16")
+    for n in ("dquery", "dkey"):
+        assert int(torch.count_nonzero(got[n][1])) == 0, n
+        assert int(torch.count_nonzero(got[n][0])) > 0, n
+    g.destroy()
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_backward_self_loops_and_no_bias(dt):
     rng = np.random.default_rng(50)
